@@ -1,0 +1,131 @@
+"""Oracle of the Stable-Window-Decoding bookkeeping and the refresh set.
+
+Sources, cited by page title and section:
+  [SWD]  "Stable Window Decoding" page (wmrh.cn/news/51151):
+         3.1  the stability criterion: position i is stable at step t when its
+              top-1 token was the same over the last K steps and the mean of
+              those K top-1 probabilities exceeds tau;
+         3.2  the computation window: every unstable position u contributes
+              [u-R, u+R], clipped to the sequence; worked example L = 20;
+         3.3  the algorithm: a position already in the stable set is skipped;
+         4.2  the scheduler: a per-position history trimmed to its last K
+              (token, prob) records; the test runs once K records exist.
+  [TA]   "Diffusion latent cache with time anchors" page (mhpq.cn/news/1098081),
+         2.3 and 3.1: every cache entry carries the step it was written at; a
+         lookup at step t rejects it when t - version > 2.
+  [LaCache] "Problem statement" / "Inference workflow": the prompt and the
+         masked suffix keep their token ids inside a block; the block's first
+         step runs a full forward and refills the caches.
+
+Readings (also listed in the design notes):
+  * "exceeds" is strict: mean > tau; the mean is (sum oldest->newest)/K in fp32;
+  * a position that becomes stable commits its top-1 token (masked diffusion
+    freezes a stable position by unmasking it); at the block's last step every
+    position still unstable commits its top-1 token;
+  * unstable = active-block positions not yet stable (prompt, committed and
+    future masked positions keep fixed ids inside a block);
+  * the all-stable case adds no window (the page's "compute all" is one of two
+    options it offers; the other, ending, is what a fixed Tb gives);
+  * t is the global step counter; refresh set for step t+1 =
+      dilate_R(unstable) U {p : tok[p] != token the entry was computed from}
+      U {p : (t+1) - version[p] > expiry}  (U the active block when the
+      workload asks every active row to be recomputed).
+"""
+import numpy as np
+
+
+class SWDState:
+    """Per-sequence history of (top-1 token, top-1 prob) for active positions."""
+
+    def __init__(self, batch, block_len):
+        self.batch = batch
+        self.block_len = block_len
+        self.reset()
+
+    def reset(self):
+        self.tok = [[[] for _ in range(self.block_len)] for _ in range(self.batch)]
+        self.p = [[[] for _ in range(self.block_len)] for _ in range(self.batch)]
+        self.n = np.zeros((self.batch, self.block_len), dtype=np.int64)
+
+    def copy(self):
+        c = SWDState.__new__(SWDState)
+        c.batch, c.block_len = self.batch, self.block_len
+        c.tok = [[list(x) for x in row] for row in self.tok]
+        c.p = [[list(x) for x in row] for row in self.p]
+        c.n = self.n.copy()
+        return c
+
+
+def _mean_f32(ps, K):
+    s = np.float32(0.0)
+    for p in ps:                      # oldest -> newest
+        s = np.float32(s + np.float32(p))
+    return np.float32(s / np.float32(K))
+
+
+def swd_update(state, q0, argmax, p1, tok, stable, K, tau, last_step):
+    """One SWD update for the active block [q0, q0 + blk) of every sequence.
+
+    argmax, p1: [B, blk] (p1 is kept in fp32, as the GPU keeps it).
+    tok, stable: [B, L], updated in place.  Returns the [B, blk] bool array of
+    positions that became stable at this step.
+    """
+    B, blk = argmax.shape
+    newly = np.zeros((B, blk), dtype=bool)
+    tau32 = np.float32(tau)
+    for b in range(B):
+        for j in range(blk):
+            r = q0 + j
+            if stable[b, r]:
+                continue                         # [SWD] 3.3 d: stable is absorbing
+            hist_t, hist_p = state.tok[b][j], state.p[b][j]
+            hist_t.append(int(argmax[b, j]))
+            hist_p.append(np.float32(p1[b, j]))
+            state.n[b, j] += 1
+            if len(hist_t) > K:                  # [SWD] 4.2: keep the last K
+                del hist_t[0]
+                del hist_p[0]
+            if len(hist_t) == K and len(set(hist_t)) == 1 and _mean_f32(hist_p, K) > tau32:
+                stable[b, r] = True
+                tok[b, r] = hist_t[-1]
+                newly[b, j] = True
+        if last_step:
+            for j in range(blk):
+                r = q0 + j
+                if not stable[b, r]:
+                    tok[b, r] = int(argmax[b, j])
+    return newly
+
+
+def dilate(unstable, R, L):
+    """[SWD] 3.2: union of [u-R, u+R] over unstable positions u, clipped to
+    [0, L-1].  Returns a bool mask of length L."""
+    m = np.zeros(L, dtype=bool)
+    for u in unstable:
+        m[max(0, u - R):min(L - 1, u + R) + 1] = True
+    return m
+
+
+def expired_rows(version, t, expiry):
+    """[TA] 2.3 / 3.1: entries whose version is more than ``expiry`` steps old.
+
+    version: [n_layers, B, L]; returns a [B, L] bool mask (a row is stale when
+    any layer's entry is stale)."""
+    if expiry < 0:
+        return np.zeros(version.shape[1:], dtype=bool)
+    return np.any(t - version > expiry, axis=0)
+
+
+def refresh_rows(stable, tok, tok_w, version, q0, blk, R, t_next, expiry,
+                 refresh_active=False):
+    """Refresh set for step t_next as sorted flat row indices b*L + pos."""
+    B, L = tok.shape
+    rf = np.zeros((B, L), dtype=bool)
+    for b in range(B):
+        unstable = [q0 + j for j in range(blk) if not stable[b, q0 + j]]
+        rf[b] |= dilate(unstable, R, L)
+        if refresh_active:
+            rf[b, q0:q0 + blk] = True
+    rf |= tok != tok_w
+    rf |= expired_rows(version, t_next, expiry)
+    return np.flatnonzero(rf.reshape(-1)).astype(np.int32)

@@ -1,0 +1,404 @@
+"""Pins of the CPU oracle against the pages, closed forms and independent
+library routines (no GPU).  A plausible slip anywhere in the oracle (a dropped
+term, a wrong sign or index, a transposed operand) fails one of these."""
+import itertools
+import math
+
+import numpy as np
+import pytest
+from scipy import special, stats
+
+import oracle as O
+from conftest import parse_ranges, read_golden
+from workloads import configs as C
+from workloads import generate as G
+
+RNG = np.random.default_rng(1234)
+
+
+# --- storage rounding ---------------------------------------------------------
+def test_bf16_round_ties_and_cases():
+    one = 1.0
+    cases = [
+        (one + 2.0 ** -8, one),                          # tie -> even (down)
+        (one + 3 * 2.0 ** -8, one + 2.0 ** -6),          # tie -> even (up)
+        (one + 2.0 ** -8 + 2.0 ** -20, one + 2.0 ** -7),  # above the tie -> up
+        (-(one + 2.0 ** -8 + 2.0 ** -20), -(one + 2.0 ** -7)),
+        (3.0, 3.0), (0.0, 0.0),
+    ]
+    for x, want in cases:
+        assert O.round_store(np.array([x]), "bf16")[0] == want
+
+
+def test_bf16_round_matches_independent_fp32_encoder():
+    # The input generator encodes fp32 -> bf16 from the fp32 bit pattern; the
+    # oracle rounds fp64 at bit 45.  For fp32 inputs the two must agree.
+    x = (RNG.standard_normal(20000) * np.exp(RNG.uniform(-20, 20, 20000))).astype(np.float32)
+    a = O.round_store(x.astype(np.float64), "bf16")
+    b = O.bf16_bits_to_f64(G.f32_to_bf16_bits(x))
+    assert np.array_equal(a, b)
+
+
+# --- normalisation, RoPE, GELU -----------------------------------------------------
+def test_rms_scale_closed_form():
+    x = RNG.standard_normal((7, 64)) * 3.0
+    y = x * O.rms_scale(x, eps=0.0)
+    assert np.allclose(np.sqrt(np.mean(y * y, axis=1)), 1.0, rtol=1e-13)
+    assert np.allclose(O.rms_scale(5.0 * x, 0.0) * 5.0, O.rms_scale(x, 0.0), rtol=1e-13)
+
+
+def test_rope_identity_at_zero_and_complex_form():
+    H, dh = 3, 16
+    x = RNG.standard_normal((5, H, dh))
+    assert np.array_equal(O.rope(x, np.zeros(5, dtype=int)), x)
+    pos = np.array([0, 1, 7, 100, 4095])
+    y = O.rope(x, pos, theta=10000.0)
+    # independent formulation: pair (x_i, x_{i+dh/2}) as a complex number
+    # multiplied by exp(i * pos * theta^(-2i/dh))
+    half = dh // 2
+    z = x[..., :half] + 1j * x[..., half:]
+    freq = 10000.0 ** (-np.arange(0, dh, 2) / dh)
+    zr = z * np.exp(1j * pos[:, None, None] * freq[None, None, :])
+    assert np.allclose(y[..., :half], zr.real, atol=1e-12)
+    assert np.allclose(y[..., half:], zr.imag, atol=1e-12)
+
+
+def test_rope_relative_position_property():
+    # <rope(q, m), rope(k, n)> depends only on m - n
+    q = RNG.standard_normal((1, 1, 32))
+    k = RNG.standard_normal((1, 1, 32))
+    d0 = np.sum(O.rope(q, [5]) * O.rope(k, [2]))
+    d1 = np.sum(O.rope(q, [105]) * O.rope(k, [102]))
+    d2 = np.sum(O.rope(q, [6]) * O.rope(k, [2]))
+    assert abs(d0 - d1) < 1e-12
+    assert abs(d0 - d2) > 1e-6
+    assert np.allclose(np.linalg.norm(O.rope(q, [77])), np.linalg.norm(q))
+
+
+def test_gelu_closed_form():
+    xs = np.array([-3.0, -1.0, -0.5, 0.0, 0.25, 1.0, 2.0])
+    want = np.array([x * 0.5 * (1 + math.erf(x / math.sqrt(2))) for x in xs])
+    assert np.allclose(O.gelu(xs), want, atol=1e-15)
+    assert np.allclose(O.gelu(xs) - O.gelu(-xs), xs, atol=1e-15)
+
+
+# --- projection ---------------------------------------------------------------------
+def test_project_qkv_with_permutation_weights():
+    # W_qkv = [P; I; 2I] with P a non-symmetric permutation: q = rope(P xn),
+    # k = rope(xn), v = 2 xn.  A transposed operand gives P^T instead of P.
+    H, dh = 2, 8
+    d = H * dh
+    perm = RNG.permutation(d)
+    P = np.eye(d)[perm]
+    assert not np.array_equal(P, P.T)
+    W = np.concatenate([P, np.eye(d), 2 * np.eye(d)])
+    x = RNG.standard_normal((3, d))
+    pos = np.array([0, 3, 9])
+    q, k, v = O.project_qkv(x, W, pos, H, "f32", 10000.0, 1e-6)
+    xn = x / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + 1e-6)
+    f32 = lambda a: a.astype(np.float32).astype(np.float64)
+    assert np.allclose(q, f32(O.rope(xn[:, perm].reshape(3, H, dh), pos)), atol=1e-6)
+    assert np.allclose(k, f32(O.rope(xn.reshape(3, H, dh), pos)), atol=1e-6)
+    assert np.allclose(v, f32(2 * xn.reshape(3, H, dh)), atol=1e-6)
+
+
+# --- attention ------------------------------------------------------------------------
+def test_attention_single_key_and_identical_keys():
+    q = RNG.standard_normal((4, 2, 8))
+    k = RNG.standard_normal((1, 2, 8))
+    v = RNG.standard_normal((1, 2, 8))
+    assert np.allclose(O.attention(q, k, v), np.broadcast_to(v, (4, 2, 8)), atol=1e-15)
+    kk = np.repeat(k, 6, axis=0)
+    vv = RNG.standard_normal((6, 2, 8))
+    assert np.allclose(O.attention(q, kk, vv), vv.mean(axis=0)[None], atol=1e-14)
+
+
+def test_attention_vs_scipy_softmax_and_permutation():
+    q = RNG.standard_normal((5, 3, 16))
+    k = RNG.standard_normal((40, 3, 16))
+    v = RNG.standard_normal((40, 3, 16))
+    o = O.attention(q, k, v)
+    for h in range(3):
+        w = special.softmax(q[:, h] @ k[:, h].T / 4.0, axis=1)
+        assert np.allclose(o[:, h], w @ v[:, h], atol=1e-13)
+    p = RNG.permutation(40)
+    assert np.allclose(O.attention(q, k[p], v[p]), o, atol=1e-13)
+    # queries are independent (no causal mask, no mixing across queries)
+    assert np.allclose(O.attention(q[2:3], k, v), o[2:3], atol=1e-14)
+
+
+def test_out_proj_and_ffn_reduce():
+    x = O.round_store(RNG.standard_normal((3, 8)), "bf16")
+    o = RNG.standard_normal((3, 8))
+    assert np.array_equal(O.out_proj(o, np.zeros((8, 8)), x, "bf16"), x)
+    ws = np.diag(np.arange(1, 9, dtype=float))
+    h = O.out_proj(o, ws, x, "f32")
+    want = (x + O.round_store(o, "f32") * np.arange(1, 9)).astype(np.float32)
+    assert np.allclose(h, want, atol=1e-6)
+    assert np.array_equal(O.ffn(x, np.ones((4, 8)), np.zeros((8, 4)), "bf16"), x)
+
+
+# --- LM head confidence ----------------------------------------------------------------------
+def test_lm_head_uniform_logits():
+    V = 50
+    h = RNG.standard_normal((4, 8))
+    am, p1, ent, _ = O.lm_head_conf(h, np.zeros((V, 8)), mask_id=0)
+    assert np.all(am == 1)                          # lowest id other than the mask
+    assert np.allclose(p1, 1.0 / (V - 1))
+    assert np.allclose(ent, np.log(V - 1))
+
+
+def test_lm_head_vs_scipy_and_mask_exclusion():
+    V, d = 300, 16
+    h = RNG.standard_normal((6, d))
+    W = RNG.standard_normal((V, d)) * 0.7
+    W[0] = 10 * h.mean(axis=0)                      # make the mask id's logit large
+    am, p1, ent, margin = O.lm_head_conf(h, W, mask_id=0)
+    hn = h / np.sqrt(np.mean(h * h, axis=1, keepdims=True) + 1e-6)
+    lg = hn @ W.T
+    lg_ex = lg[:, 1:]
+    p = special.softmax(lg_ex, axis=1)
+    assert np.all(am != 0)
+    assert np.array_equal(am, np.argmax(lg_ex, axis=1) + 1)
+    assert np.allclose(p1, p.max(axis=1), rtol=1e-12)
+    assert np.allclose(ent, stats.entropy(p, axis=1), rtol=1e-10)
+    assert np.all(ent >= 0) and np.all(ent <= np.log(V - 1) + 1e-12)
+    srt = np.sort(lg_ex, axis=1)
+    assert np.allclose(margin, srt[:, -1] - srt[:, -2])
+
+
+def test_lm_head_tie_goes_to_lowest_index():
+    W = np.zeros((10, 4))
+    W[3] = W[7] = [1, 0, 0, 0]
+    am, _, _, margin = O.lm_head_conf(np.array([[1.0, 0.5, 0.5, 0.5]]), W, mask_id=0)
+    assert am[0] == 3 and margin[0] == 0.0
+
+
+# --- SWD stability rule: brute force over small histories --------------------------------------
+def _drive(tokens, probs, K, tau):
+    """Feed one position's per-step (token, prob) into the oracle; return the
+    step at which it became stable (or None) and the committed token."""
+    st = O.SWDState(1, 1)
+    tok = np.zeros((1, 1), dtype=np.int64)
+    stable = np.zeros((1, 1), dtype=bool)
+    when = None
+    for i, (a, p) in enumerate(zip(tokens, probs)):
+        was = bool(stable[0, 0])
+        O.swd_update(st, 0, np.array([[a]]), np.array([[p]]), tok, stable, K, tau, False)
+        if was:
+            assert stable[0, 0]                       # absorbing
+        if stable[0, 0] and when is None:
+            when = i
+    return when, int(tok[0, 0])
+
+
+def _first_run_end(tokens, K):
+    """First index where a run of K equal tokens ends (itertools.groupby)."""
+    i = 0
+    for _, grp in itertools.groupby(tokens):
+        n = len(list(grp))
+        if n >= K:
+            return i + K - 1
+        i += n
+    return None
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+def test_swd_brute_force_low_tau_is_run_length(K):
+    # tau below every probability: stable exactly when the first run of K
+    # equal top-1 tokens completes; the committed token is that run's token.
+    for n in range(1, 7):
+        for toks in itertools.product([1, 2, 3], repeat=n):
+            when, tok = _drive(toks, [0.5] * n, K, tau=0.1)
+            want = _first_run_end(toks, K)
+            assert when == want, (toks, K)
+            if want is not None:
+                assert tok == toks[want]
+
+
+def test_swd_brute_force_constant_prob_threshold():
+    # constant probability c, constant token: stable at step K-1 iff c > tau
+    grid = [0.85, 0.9, 0.9 + 1e-6, 0.95]
+    for K in (1, 2, 3):
+        for c in grid:
+            when, _ = _drive([5] * 6, [c] * 6, K, tau=0.9)
+            assert when == (K - 1 if np.float32(c) > np.float32(0.9) else None), (K, c)
+
+
+def test_swd_brute_force_mean_over_last_K_only():
+    # K = 3, tau = 0.9: probabilities enter the mean only while in the window
+    rng = np.random.default_rng(7)
+    for _ in range(3000):
+        n = rng.integers(1, 8)
+        toks = rng.integers(1, 3, size=n)
+        ps = rng.choice([0.6, 0.85, 0.9, 0.95, 0.99], size=n)
+        when, _ = _drive(list(toks), list(ps), 3, 0.9)
+        # independent statement of the page's formula over full arrays
+        first = None
+        for t in range(2, n):
+            same = toks[t - 2] == toks[t - 1] == toks[t]
+            mean = np.float32(np.float32(np.float32(ps[t - 2]) + np.float32(ps[t - 1])) + np.float32(ps[t])) / np.float32(3)
+            if same and mean > np.float32(0.9):
+                first = t
+                break
+        assert when == first, (toks, ps)
+
+
+def test_swd_forced_commit_at_last_step():
+    st = O.SWDState(1, 4)
+    tok = np.zeros((1, 10), dtype=np.int64)
+    stable = np.zeros((1, 10), dtype=bool)
+    stable[0, 5] = True
+    tok[0, 5] = 99
+    O.swd_update(st, 4, np.array([[11, 12, 13, 14]]), np.full((1, 4), 0.1), tok, stable, 3, 0.9, True)
+    assert list(tok[0, 4:8]) == [11, 99, 13, 14]       # stable row keeps its commit
+    assert list(tok[0, :4]) == [0, 0, 0, 0]
+
+
+# --- dilation, expiry, refresh set --------------------------------------------------------
+def test_dilation_page_example():
+    g = read_golden("swd_dilation_L20.txt")
+    L = int(g["L"])
+    stable1 = set(parse_ranges(g["stable"]))
+    unstable0 = [p - 1 for p in range(1, L + 1) if p not in stable1]
+    assert [p + 1 for p in unstable0] == parse_ranges(g["unstable_windows"])
+    for R in (0, 1, 2, 5):
+        m = O.dilate(unstable0, R, L)
+        assert [i + 1 for i in np.flatnonzero(m)] == parse_ranges(g[f"window_R{R}"]), R
+
+
+def test_dilation_vs_convolution():
+    rng = np.random.default_rng(3)
+    for _ in range(500):
+        L = int(rng.integers(1, 40))
+        R = int(rng.integers(0, 4))
+        u = rng.random(L) < 0.2
+        m = O.dilate(np.flatnonzero(u), R, L)
+        conv = np.convolve(u.astype(int), np.ones(2 * R + 1, dtype=int), mode="same")[:L] > 0
+        if 2 * R + 1 > L:     # np.convolve 'same' centres on the longer input
+            conv = np.array([u[max(0, i - R):i + R + 1].any() for i in range(L)])
+        assert np.array_equal(m, conv)
+
+
+def test_version_expiry_page_rule():
+    g = read_golden("version_expiry.txt")
+    thr = int(g["threshold"])
+    for case in g["case"]:
+        t, v, rej = (int(s) for s in case.split(","))
+        ver = np.full((1, 1, 1), v)
+        assert bool(O.expired_rows(ver, t, thr)[0, 0]) == bool(rej), case
+    assert not O.expired_rows(np.zeros((1, 1, 1)), 100, -1).any()
+
+
+def test_refresh_rows_composition():
+    B, L = 2, 12
+    tok = np.ones((B, L), dtype=np.int64)
+    tok_w = tok.copy()
+    stable = np.zeros((B, L), dtype=bool)
+    stable[:, 4:8] = True
+    stable[0, 5] = False                 # one unstable active row in sequence 0
+    tok[1, 1] = 7                        # a changed row in sequence 1
+    version = np.full((1, B, L), 10)
+    version[0, 0, 11] = 7                # expired at t=10 with expiry 2
+    rows = O.refresh_rows(stable, tok, tok_w, version, 4, 4, 1, 10, 2)
+    assert list(rows) == [4, 5, 6, 11, 12 + 1]
+    rows_all = O.refresh_rows(stable, tok, tok_w, version, 4, 4, 1, 10, 2, refresh_active=True)
+    assert list(rows_all) == [4, 5, 6, 7, 11, 12 + 1, 12 + 4, 12 + 5, 12 + 6, 12 + 7]
+
+
+# --- whole-loop pins (refresh-all == recompute; unchanged => identical K/V) ---------------
+def _load(name):
+    w = C.get(name)
+    return w, O.weights_f64(w, G.model(w)), G.prompt_tokens(w)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "mid_multi"])
+def test_refresh_all_equals_recompute(name):
+    w, W, tok0 = _load(name)
+    a = O.run_dense(w, W, tok0, n_steps=8, mode="cached", force_all=True)
+    b = O.run_dense(w, W, tok0, n_steps=8, mode="recompute")
+    for ra, rb in zip(a, b):
+        for key in ("argmax", "p1", "ent", "o", "h", "tok", "stable"):
+            assert np.array_equal(ra[key], rb[key]), (name, ra["t"], key)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32_sharp", "mid_bf16_sharp"])
+def test_single_layer_cached_equals_recompute(name):
+    w, W, tok0 = _load(name)
+    a = O.run_dense(w, W, tok0, mode="cached")
+    b = O.run_dense(w, W, tok0, mode="recompute")
+    assert sum(int(r["newly"].sum()) for r in a) > 0          # commits happened
+    assert any(len(r["rows"]) < w.batch * w.seq_len for r in a)
+    for ra, rb in zip(a, b):
+        for key in ("argmax", "p1", "ent", "o", "h", "tok"):
+            assert np.array_equal(ra[key], rb[key]), (name, ra["t"], key)
+
+
+def test_unchanged_tokens_have_identical_cached_kv():
+    w, W, tok0 = _load("mid_bf16_sharp")
+    tr = O.run_dense(w, W, tok0, mode="cached", keep_pre=True)
+    L, H, dh = w.seq_len, w.n_heads, w.head_dim
+    checked = 0
+    for r in tr[1:]:
+        pre = r["pre"]
+        same = (pre["tok"] == pre["tok_w"]).reshape(-1)
+        rows = np.flatnonzero(same)
+        x = W["embed"][pre["tok"].reshape(-1)[rows]]
+        q, k, v = O.project_qkv(x, W["w_qkv"][0], rows % L, H, w.dtype)
+        for c, val in zip(pre["caches"], (q, k, v)):
+            assert np.array_equal(c[0].reshape(-1, H, dh)[rows], val)
+        checked += len(rows)
+    assert checked > 0
+
+
+def test_block_start_and_expiry_refresh_pattern():
+    # with nothing stable and expiry 2, block-local steps 0, 3, 6, ... refresh
+    # every row; the others refresh the dilated active block only
+    w, W, tok0 = _load("mid_bf16")
+    tr = O.run_dense(w, W, tok0, mode="cached")
+    full = w.batch * w.seq_len
+    for r in tr:
+        if r["s"] % 3 == 0:
+            assert len(r["rows"]) == full
+        else:
+            lo = max(0, r["q0"] - w.swd_R)
+            hi = min(w.seq_len - 1, r["q0"] + w.block_len - 1 + w.swd_R)
+            assert len(r["rows"]) == w.batch * (hi - lo + 1)
+
+
+# --- sink + rolling cache --------------------------------------------------------------------
+def test_sink_ring_page_example():
+    g = read_golden("sink_s3_c7.txt")
+    S, Cmax, W = int(g["attention_sinks"]), int(g["max_cache_length"]), int(g["rolling_window"])
+    assert W == Cmax - S
+    shape = [int(s) for s in g["k_cache_shape"].split(",")]
+    assert shape[2] == Cmax
+    sim = O.RingSim(S, W)
+    for n in range(60):
+        sim.push(n)
+        held = sim.held()
+        assert len(held) == min(n + 1, S + W)              # constant S+W after warm-up
+        assert held[:min(S, n + 1)] == list(range(min(S, n + 1)))   # sinks never move
+        assert held == list(range(S)) + list(range(max(S, n - W + 1), n + 1)) or n < S
+
+
+def test_sink_stream_outputs_bit_stable_sinks():
+    w = C.get("mid_sink")
+    W = O.weights_f64(w, G.model(w))
+    stream = G.stream_tokens(w)
+    out, held = O.run_stream(w, W, stream, n_tokens=w.stream_len)
+    S = w.sink
+    for n, h in held.items():
+        assert len(h) == min(n + 1, w.sink + w.window)
+    # the first query attends to itself only: O_0 = v_0
+    x = W["embed"][stream[:1]]
+    _, _, v0 = O.project_qkv(x, W["w_qkv"][0], np.array([0]), w.n_heads, w.dtype)
+    assert np.array_equal(out[0], O.round_store(v0[0], w.dtype))
+    assert all(h[:S] == list(range(S)) for n, h in held.items() if n >= S)
+
+
+def test_sharp_variants_exercise_swd():
+    for name in ("tiny_fp32_sharp", "mid_bf16_sharp"):
+        w, W, tok0 = _load(name)
+        tr = O.run_dense(w, W, tok0, mode="cached")
+        assert sum(int(r["newly"].sum()) for r in tr) >= 8, name

@@ -1,0 +1,129 @@
+"""Workload shapes for one cached denoising step of a masked diffusion LM.
+
+Five named workloads restate the shapes the pages run their methods on (a tiny
+fp32 layer, a 2048-wide bf16 layer, an 8B-shaped layer, an attention-sink
+stream and a 12-layer denoiser), plus small shapes that the CPU oracle finishes
+in seconds and that still span several GPU tiles with ragged tails.
+
+This module holds shapes and hyper-parameters only: no arithmetic of the method.
+"""
+from dataclasses import dataclass, field, replace
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    dtype: str            # "f32" or "bf16": storage/compute type of the path
+    n_layers: int
+    batch: int
+    seq_len: int          # L (dense cache); unused by the sink stream
+    n_prompt: int
+    block_len: int        # SAR block length (active block Ac)
+    steps_per_block: int  # Tb
+    d_model: int
+    n_heads: int
+    head_dim: int
+    vocab: int
+    ffn: int = 0          # FFN hidden width (0 = single attention layer, no FFN)
+    swd_K: int = 3
+    swd_tau: float = 0.9
+    swd_R: int = 2
+    expiry: int = -1      # reject t - version > expiry; -1 = no expiry
+    mask_id: int = 0
+    rope_theta: float = 10000.0
+    rms_eps: float = 1e-6
+    seed: int = 0
+    tokens: str = "zipf"  # "uniform255" or "zipf" (Zipf(1.1) over ids 1..V-1)
+    zipf_a: float = 1.1
+    lm_scale: float = 1.0  # multiplies W_lm ("sharp" variants make SWD fire)
+    refresh_active: int = 0  # 1: every active-block row joins the refresh set
+    # attention-sink stream (sink > 0 selects streaming mode)
+    sink: int = 0
+    window: int = 0
+    stream_len: int = 0
+
+    @property
+    def n_gen(self):
+        return self.seq_len - self.n_prompt
+
+    @property
+    def n_blocks(self):
+        return self.n_gen // self.block_len
+
+    @property
+    def n_steps(self):
+        return self.n_blocks * self.steps_per_block
+
+    @property
+    def streaming(self):
+        return self.sink > 0
+
+    @property
+    def cache_len(self):
+        return self.sink + self.window if self.streaming else self.seq_len
+
+
+# --- the five workloads (shapes as the pages' settings give them) -----------
+TINY_FP32 = Workload(
+    name="tiny_fp32", dtype="f32", n_layers=1, batch=1, seq_len=64, n_prompt=32,
+    block_len=8, steps_per_block=16, d_model=64, n_heads=2, head_dim=32, vocab=256,
+    swd_K=3, swd_tau=0.95, swd_R=2, expiry=-1, seed=0, tokens="uniform255")
+
+BF16_D2048 = Workload(
+    name="bf16_d2048", dtype="bf16", n_layers=1, batch=4, seq_len=1024, n_prompt=896,
+    block_len=32, steps_per_block=32, d_model=2048, n_heads=16, head_dim=128,
+    vocab=32000, swd_K=3, swd_tau=0.9, swd_R=2, expiry=2, seed=1)
+
+LAYER_8B = Workload(
+    name="8b_shaped", dtype="bf16", n_layers=1, batch=8, seq_len=4096, n_prompt=3584,
+    block_len=32, steps_per_block=32, d_model=4096, n_heads=32, head_dim=128,
+    vocab=126464, swd_K=3, swd_tau=0.95, swd_R=1, expiry=-1, seed=2)
+
+SINK_RING = Workload(
+    name="sink_ring", dtype="bf16", n_layers=1, batch=1, seq_len=0, n_prompt=0,
+    block_len=1, steps_per_block=1, d_model=4096, n_heads=32, head_dim=128,
+    vocab=32000, seed=3, sink=4, window=4092, stream_len=32768)
+
+TWELVE_LAYER = Workload(
+    name="twelve_layer", dtype="bf16", n_layers=12, batch=16, seq_len=2048,
+    n_prompt=1536, block_len=64, steps_per_block=64, d_model=1024, n_heads=16,
+    head_dim=64, vocab=32000, ffn=4096, swd_K=3, swd_tau=0.9, swd_R=2, expiry=2,
+    seed=4, refresh_active=1)
+
+NAMED = {w.name: w for w in (TINY_FP32, BF16_D2048, LAYER_8B, SINK_RING, TWELVE_LAYER)}
+
+# --- small shapes for element-by-element parity ------------------------------
+# Ragged on purpose: 320 rows (2.5 row tiles of 128), vocab 1000 (7 column
+# tiles of 128 and a 104-wide tail), L = 160 keys (2.5 key tiles of 64).
+MID_BF16 = Workload(
+    name="mid_bf16", dtype="bf16", n_layers=1, batch=2, seq_len=160, n_prompt=128,
+    block_len=16, steps_per_block=6, d_model=256, n_heads=2, head_dim=128,
+    vocab=1000, swd_K=3, swd_tau=0.9, swd_R=2, expiry=2, seed=11)
+
+MID_BF16_DH64 = replace(MID_BF16, name="mid_bf16_dh64", n_heads=4, head_dim=64,
+                        seed=12, swd_R=1, expiry=-1)
+
+# "Sharp" variants: W_lm scaled so that top-1 probabilities clear tau and the
+# stable / commit / dilation paths run (with N(0, 0.02) weights p1 ~ 1/V).
+TINY_FP32_SHARP = replace(TINY_FP32, name="tiny_fp32_sharp", lm_scale=60.0)
+MID_BF16_SHARP = replace(MID_BF16, name="mid_bf16_sharp", lm_scale=40.0,
+                         steps_per_block=10)
+
+MID_SINK = Workload(
+    name="mid_sink", dtype="bf16", n_layers=1, batch=1, seq_len=0, n_prompt=0,
+    block_len=1, steps_per_block=1, d_model=256, n_heads=2, head_dim=128,
+    vocab=1000, seed=13, sink=4, window=92, stream_len=300)
+
+MID_MULTI = Workload(
+    name="mid_multi", dtype="bf16", n_layers=3, batch=2, seq_len=160, n_prompt=128,
+    block_len=16, steps_per_block=6, d_model=256, n_heads=4, head_dim=64,
+    vocab=1000, ffn=512, swd_K=3, swd_tau=0.9, swd_R=2, expiry=2, seed=14,
+    refresh_active=1)
+
+ALL = dict(NAMED)
+for _w in (MID_BF16, MID_BF16_DH64, TINY_FP32_SHARP, MID_BF16_SHARP, MID_SINK, MID_MULTI):
+    ALL[_w.name] = _w
+
+
+def get(name):
+    return ALL[name]
