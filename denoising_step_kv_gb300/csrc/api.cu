@@ -1,0 +1,408 @@
+// C ABI of the cached denoising step: argument validation, buffers of the
+// handle, the RoPE table, tensor-map encoding, and the entry points.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+namespace dllm {
+
+thread_local std::string g_last_error;
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+namespace {
+
+inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+dllm_status fail(dllm_status s, const std::string& msg) {
+  set_error(msg);
+  return s;
+}
+
+dllm_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(DLLM_ECUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+#define DLLM_CHECK_HANDLE(c)                                     \
+  do {                                                           \
+    if (!(c)) return fail(DLLM_EINVAL, "null dllm_cache handle"); \
+  } while (0)
+
+#define DLLM_LAUNCH(expr, where)                 \
+  do {                                           \
+    cudaError_t e_ = (expr);                     \
+    if (e_ != cudaSuccess) return cuda_fail(e_, where); \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+void free_all(dllm_cache* c) {
+  void* bufs[] = {c->q, c->k, c->v, c->version, c->tok_w, c->stable, c->hist_tok, c->hist_p, c->hist_n, c->words,
+                  c->rope, c->err, c->X, c->rs, c->lm_part, c->lm_rs, c->ffn_buf};
+  for (void* b : bufs)
+    if (b) cudaFree(b);
+}
+
+template <typename T>
+bool dalloc(T** p, size_t bytes) {
+  if (bytes == 0) bytes = 16;
+  return cudaMalloc(reinterpret_cast<void**>(p), bytes) == cudaSuccess;
+}
+
+}  // namespace
+
+bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                  uint32_t box_inner, uint32_t box_outer, bool bf16) {
+  EncodeFn fn = encode_fn();
+  if (!fn || !aligned16(base) || row_bytes % 16 != 0 || outer == 0 || inner == 0) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, static_cast<cuuint32_t>(std::min<uint64_t>(box_outer, 256))};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace dllm
+
+using namespace dllm;
+
+extern "C" {
+
+const char* dllm_last_error(void) { return g_last_error.c_str(); }
+
+dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache** out) {
+  if (!cfg || !out) return fail(DLLM_EINVAL, "dllm_cache_init: null cfg or out");
+  *out = nullptr;
+  const dllm_cache_cfg g = *cfg;
+  const bool streaming = g.sink > 0;
+  if (g.n_layers < 1 || g.batch < 1 || g.n_heads < 1 || g.head_dim < 1 || g.vocab < 1)
+    return fail(DLLM_EINVAL, "dllm_cache_init: n_layers, batch, n_heads, head_dim and vocab must be >= 1");
+  if (g.dtype != DLLM_F32 && g.dtype != DLLM_BF16) return fail(DLLM_EINVAL, "dllm_cache_init: bad dtype");
+  if (streaming) {
+    if (g.window < 1 || g.batch != 1 || g.max_pos < 1)
+      return fail(DLLM_EINVAL, "dllm_cache_init: streaming needs window >= 1, batch 1 and max_pos >= 1");
+  } else {
+    if (g.seq_len < 1 || g.block_len < 1 || g.block_len > 64 || g.block_len > g.seq_len)
+      return fail(DLLM_EINVAL, "dllm_cache_init: need 1 <= block_len <= min(64, seq_len)");
+    if (g.swd_K < 1 || g.swd_K > 8 || g.swd_R < 0)
+      return fail(DLLM_EINVAL, "dllm_cache_init: need 1 <= swd_K <= 8 and swd_R >= 0");
+    if (static_cast<long long>(g.batch) * g.seq_len > (1LL << 26))
+      return fail(DLLM_EUNSUPPORTED, "dllm_cache_init: batch * seq_len above 2^26");
+  }
+  const int d = g.n_heads * g.head_dim;
+  if (g.dtype == DLLM_BF16) {
+    if ((g.head_dim != 64 && g.head_dim != 128) || d % 128 != 0)
+      return fail(DLLM_EUNSUPPORTED, "dllm_cache_init: bf16 needs head_dim 64 or 128 and d % 128 == 0");
+    if (g.ffn % 128 != 0) return fail(DLLM_EUNSUPPORTED, "dllm_cache_init: bf16 needs ffn % 128 == 0");
+  } else {
+    const bool ok = (d % 128 == 0 && (g.head_dim == 32 || g.head_dim == 64 || g.head_dim == 128)) ||
+                    (d % 64 == 0 && (g.head_dim == 32 || g.head_dim == 64));
+    if (!ok) return fail(DLLM_EUNSUPPORTED, "dllm_cache_init: fp32 needs head_dim 32/64 (d % 64 == 0) or 128");
+    if (g.ffn % 32 != 0) return fail(DLLM_EUNSUPPORTED, "dllm_cache_init: fp32 needs ffn % 32 == 0");
+  }
+  if (!(g.rope_theta > 0.f) || !(g.rms_eps >= 0.f)) return fail(DLLM_EINVAL, "dllm_cache_init: bad theta/eps");
+
+  dllm_cache* c = new dllm_cache();
+  c->cfg = g;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    delete c;
+    return fail(DLLM_ECUDA, "dllm_cache_init: no CUDA device");
+  }
+  c->d = d;
+  c->elem = g.dtype == DLLM_BF16 ? 2 : 4;
+  c->rows = streaming ? g.sink + g.window : g.batch * g.seq_len;
+  c->seq_rows = c->rows;
+  c->max_pos = g.max_pos > 0 ? g.max_pos : g.seq_len;
+  if (!streaming && c->max_pos < g.seq_len) c->max_pos = g.seq_len;
+  c->Lw = streaming ? 1 : cdiv(g.seq_len, 32);
+  const size_t nl = g.n_layers, rows = c->rows, sr = c->seq_rows;
+  const int blk = streaming ? 1 : g.block_len;
+  const int K = streaming ? 1 : g.swd_K;
+  c->lm_rows_cap = g.batch * blk;
+  c->lm_tiles_cap = cdiv(g.vocab, 128);
+  c->ffn_cap = g.ffn;
+  bool ok = dalloc(&c->q, nl * rows * d * c->elem) && dalloc(&c->k, nl * rows * d * c->elem) &&
+            dalloc(&c->v, nl * rows * d * c->elem) && dalloc(&c->version, nl * sr * sizeof(int)) &&
+            dalloc(&c->tok_w, sr * sizeof(int)) && dalloc(&c->stable, sr) &&
+            dalloc(&c->hist_tok, static_cast<size_t>(g.batch) * blk * K * sizeof(int)) &&
+            dalloc(&c->hist_p, static_cast<size_t>(g.batch) * blk * K * sizeof(float)) &&
+            dalloc(&c->hist_n, static_cast<size_t>(g.batch) * blk * sizeof(int)) &&
+            dalloc(&c->words, static_cast<size_t>(g.batch) * c->Lw * sizeof(uint32_t)) &&
+            dalloc(&c->rope, static_cast<size_t>(c->max_pos) * (g.head_dim / 2) * sizeof(float2)) &&
+            dalloc(&c->err, sizeof(unsigned)) && dalloc(&c->X, sr * d * c->elem) && dalloc(&c->rs, sr * sizeof(float)) &&
+            dalloc(&c->lm_part, static_cast<size_t>(c->lm_rows_cap) * c->lm_tiles_cap * 16) &&
+            dalloc(&c->lm_rs, static_cast<size_t>(c->lm_rows_cap) * sizeof(float)) &&
+            dalloc(&c->ffn_buf, sr * static_cast<size_t>(g.ffn) * c->elem);
+  if (!ok) {
+    free_all(c);
+    delete c;
+    cudaGetLastError();
+    return fail(DLLM_ENOMEM, "dllm_cache_init: cudaMalloc failed");
+  }
+  // RoPE table: cos/sin of pos * theta^(-2i/dh), computed in double on the host
+  {
+    const int half = g.head_dim / 2;
+    std::vector<float2> tab(static_cast<size_t>(c->max_pos) * half);
+    for (int i = 0; i < half; ++i) {
+      const double inv = std::pow(static_cast<double>(g.rope_theta), -2.0 * i / g.head_dim);
+      for (int p = 0; p < c->max_pos; ++p) {
+        const double a = p * inv;
+        tab[static_cast<size_t>(p) * half + i] = make_float2(static_cast<float>(std::cos(a)),
+                                                             static_cast<float>(std::sin(a)));
+      }
+    }
+    if (cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess) {
+      free_all(c);
+      delete c;
+      return fail(DLLM_ECUDA, "dllm_cache_init: RoPE table upload failed");
+    }
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaMemsetAsync(c->q, 0, nl * rows * d * c->elem, st);
+  cudaMemsetAsync(c->k, 0, nl * rows * d * c->elem, st);
+  cudaMemsetAsync(c->v, 0, nl * rows * d * c->elem, st);
+  cudaMemsetAsync(c->hist_tok, 0, static_cast<size_t>(g.batch) * blk * K * sizeof(int), st);
+  cudaMemsetAsync(c->hist_p, 0, static_cast<size_t>(g.batch) * blk * K * sizeof(float), st);
+  if (launch_reset(c, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess) {
+    free_all(c);
+    delete c;
+    return fail(DLLM_ECUDA, "dllm_cache_init: reset failed");
+  }
+  *out = c;
+  return DLLM_OK;
+}
+
+dllm_status dllm_cache_free(dllm_cache* c) {
+  DLLM_CHECK_HANDLE(c);
+  cudaDeviceSynchronize();
+  free_all(c);
+  delete c;
+  return DLLM_OK;
+}
+
+dllm_status dllm_cache_reset(dllm_cache* c, void* stream) {
+  DLLM_CHECK_HANDLE(c);
+  DLLM_LAUNCH(launch_reset(c, static_cast<cudaStream_t>(stream)), "dllm_cache_reset");
+  return DLLM_OK;
+}
+
+dllm_status dllm_cache_check(dllm_cache* c, void* stream, uint32_t* err_word) {
+  DLLM_CHECK_HANDLE(c);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DLLM_LAUNCH(cudaStreamSynchronize(st), "dllm_cache_check: synchronize");
+  unsigned w = 0;
+  DLLM_LAUNCH(cudaMemcpy(&w, c->err, sizeof(w), cudaMemcpyDeviceToHost), "dllm_cache_check: read");
+  DLLM_LAUNCH(cudaMemset(c->err, 0, sizeof(unsigned)), "dllm_cache_check: clear");
+  if (err_word) *err_word = w;
+  if (w) {
+    std::string m = "device error word 0x";
+    char buf[16];
+    snprintf(buf, sizeof(buf), "%x", w);
+    m += buf;
+    if (w & DLLM_ERR_ROW) m += " (row out of range)";
+    if (w & DLLM_ERR_TOKEN) m += " (token out of range)";
+    if (w & DLLM_ERR_TIMEOUT) m += " (barrier wait timed out)";
+    if (w & DLLM_ERR_POS) m += " (position outside the RoPE table)";
+    return fail(DLLM_EDEVICE, m);
+  }
+  return DLLM_OK;
+}
+
+dllm_status dllm_state_copy(dllm_cache* c, int field, int layer, void* host, size_t bytes, int to_device,
+                            size_t* bytes_out) {
+  DLLM_CHECK_HANDLE(c);
+  const dllm_cache_cfg& g = c->cfg;
+  void* ptr = nullptr;
+  size_t size = 0;
+  const size_t blk = g.sink > 0 ? 1 : g.block_len, K = g.sink > 0 ? 1 : g.swd_K;
+  if (field <= DLLM_FIELD_V) {
+    if (layer < 0 || layer >= g.n_layers) return fail(DLLM_EINVAL, "dllm_state_copy: bad layer");
+    size = static_cast<size_t>(c->rows) * c->d * c->elem;
+    void* base = field == DLLM_FIELD_Q ? c->q : field == DLLM_FIELD_K ? c->k : c->v;
+    ptr = static_cast<char*>(base) + static_cast<size_t>(layer) * size;
+  } else if (field == DLLM_FIELD_VERSION) {
+    ptr = c->version;
+    size = static_cast<size_t>(g.n_layers) * c->seq_rows * sizeof(int);
+  } else if (field == DLLM_FIELD_TOK_W) {
+    ptr = c->tok_w;
+    size = static_cast<size_t>(c->seq_rows) * sizeof(int);
+  } else if (field == DLLM_FIELD_STABLE) {
+    ptr = c->stable;
+    size = c->seq_rows;
+  } else if (field == DLLM_FIELD_HIST_TOK) {
+    ptr = c->hist_tok;
+    size = g.batch * blk * K * sizeof(int);
+  } else if (field == DLLM_FIELD_HIST_P) {
+    ptr = c->hist_p;
+    size = g.batch * blk * K * sizeof(float);
+  } else if (field == DLLM_FIELD_HIST_N) {
+    ptr = c->hist_n;
+    size = g.batch * blk * sizeof(int);
+  } else {
+    return fail(DLLM_EINVAL, "dllm_state_copy: unknown field");
+  }
+  if (bytes_out) *bytes_out = size;
+  if (!host) return DLLM_OK;
+  if (bytes != size) return fail(DLLM_EINVAL, "dllm_state_copy: byte count does not match the field");
+  DLLM_LAUNCH(cudaDeviceSynchronize(), "dllm_state_copy: synchronize");
+  DLLM_LAUNCH(cudaMemcpy(to_device ? ptr : host, to_device ? host : ptr, size,
+                         to_device ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToHost),
+              "dllm_state_copy");
+  return DLLM_OK;
+}
+
+dllm_status refresh_all(dllm_cache* c, int q_start, int32_t* rows_dev, int32_t* n_rows_dev, void* stream) {
+  DLLM_CHECK_HANDLE(c);
+  if (c->cfg.sink > 0) return fail(DLLM_EINVAL, "refresh_all: dense mode only");
+  if (!rows_dev || !n_rows_dev) return fail(DLLM_EINVAL, "refresh_all: null rows or count");
+  DLLM_LAUNCH(launch_refresh_all(c, q_start, rows_dev, n_rows_dev, static_cast<cudaStream_t>(stream)),
+              "refresh_all");
+  return DLLM_OK;
+}
+
+dllm_status kv_refresh(dllm_cache* c, int layer, const void* x_dev, const int32_t* tok_dev, const void* embed_dev,
+                       const void* w_qkv_dev, const int32_t* rows_dev, const int32_t* n_rows_dev, int t,
+                       void* stream) {
+  DLLM_CHECK_HANDLE(c);
+  const dllm_cache_cfg& g = c->cfg;
+  const bool streaming = g.sink > 0;
+  if (layer < 0 || layer >= g.n_layers) return fail(DLLM_EINVAL, "kv_refresh: layer out of range");
+  if (!w_qkv_dev) return fail(DLLM_EINVAL, "kv_refresh: null w_qkv");
+  if (!x_dev && (!tok_dev || !embed_dev)) return fail(DLLM_EINVAL, "kv_refresh: need x, or tok and embed");
+  if (!rows_dev != !n_rows_dev) return fail(DLLM_EINVAL, "kv_refresh: rows and n_rows go together");
+  if (streaming && !rows_dev) return fail(DLLM_EINVAL, "kv_refresh: streaming mode needs a row list");
+  if (!aligned16(w_qkv_dev) || (x_dev && !aligned16(x_dev)) || (embed_dev && !aligned16(embed_dev)))
+    return fail(DLLM_EINVAL, "kv_refresh: pointers must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int n_host = rows_dev ? 0 : c->seq_rows;
+  DLLM_LAUNCH(launch_gather(c, layer, rows_dev, n_rows_dev, n_host, x_dev, tok_dev, embed_dev, t, st),
+              "kv_refresh: gather");
+  const void* A = x_dev ? x_dev : c->X;
+  DLLM_LAUNCH(gemm_qkv(c, layer, A, c->seq_rows, rows_dev ? n_rows_dev : nullptr, rows_dev, w_qkv_dev, st),
+              "kv_refresh: projection");
+  return DLLM_OK;
+}
+
+dllm_status block_attn(dllm_cache* c, int layer, int q_start, int q_len, void* out_dev, void* stream) {
+  DLLM_CHECK_HANDLE(c);
+  const dllm_cache_cfg& g = c->cfg;
+  if (layer < 0 || layer >= g.n_layers) return fail(DLLM_EINVAL, "block_attn: layer out of range");
+  if (!out_dev) return fail(DLLM_EINVAL, "block_attn: null out");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (g.sink > 0) {
+    if (q_len != 1 || q_start < 0 || q_start >= c->max_pos)
+      return fail(DLLM_EINVAL, "block_attn: streaming takes one query 0 <= n < max_pos");
+    const int slot = q_start < g.sink ? q_start : g.sink + (q_start - g.sink) % g.window;
+    const int kv_len = std::min(q_start + 1, g.sink + g.window);
+    DLLM_LAUNCH(attn_dense(c, layer, slot, 0, 1, 0, 0, kv_len, 1, out_dev, 0, st), "block_attn");
+    return DLLM_OK;
+  }
+  if (q_start < 0 || q_len < 1 || q_start + q_len > g.seq_len)
+    return fail(DLLM_EINVAL, "block_attn: query range outside the sequence");
+  if (g.dtype == DLLM_BF16 && q_len > 64) return fail(DLLM_EUNSUPPORTED, "block_attn: q_len > 64");
+  DLLM_LAUNCH(attn_dense(c, layer, q_start, g.seq_len, q_len, 0, g.seq_len, g.seq_len, g.batch, out_dev, q_len, st),
+              "block_attn");
+  return DLLM_OK;
+}
+
+dllm_status block_attn_rows(dllm_cache* c, int layer, const int32_t* q_rows_dev, const int32_t* n_q_dev,
+                            void* out_dev, void* stream) {
+  DLLM_CHECK_HANDLE(c);
+  (void)layer; (void)q_rows_dev; (void)n_q_dev; (void)out_dev; (void)stream;
+  return fail(DLLM_EUNSUPPORTED, "block_attn_rows: not built yet");
+}
+
+dllm_status attn_out(dllm_cache* c, const void* o_dev, const void* w_o_dev, const void* x_res_dev,
+                     const int32_t* tok_dev, const void* embed_dev, int q_start, int q_len, const int32_t* m_dev,
+                     void* h_dev, void* stream) {
+  DLLM_CHECK_HANDLE(c);
+  const dllm_cache_cfg& g = c->cfg;
+  if (!o_dev || !w_o_dev || !h_dev) return fail(DLLM_EINVAL, "attn_out: null o, w_o or h");
+  if (!x_res_dev && (!tok_dev || !embed_dev)) return fail(DLLM_EINVAL, "attn_out: need x_res, or tok and embed");
+  if (!x_res_dev && (q_len < 1 || q_start < 0 || q_start + q_len > g.seq_len))
+    return fail(DLLM_EINVAL, "attn_out: query range outside the sequence");
+  if (!aligned16(o_dev) || !aligned16(w_o_dev) || !aligned16(h_dev))
+    return fail(DLLM_EINVAL, "attn_out: pointers must be 16-byte aligned");
+  const int M = g.batch * std::max(q_len, 1);
+  DLLM_LAUNCH(gemm_resid(c, o_dev, w_o_dev, M, c->seq_rows, m_dev, c->d, c->d, x_res_dev, tok_dev, embed_dev,
+                         q_start, std::max(q_len, 1), h_dev, static_cast<cudaStream_t>(stream)),
+              "attn_out");
+  return DLLM_OK;
+}
+
+dllm_status ffn_gelu(dllm_cache* c, const void* h_dev, const void* w1_dev, const void* w2_dev, int F, int M,
+                     const int32_t* m_dev, void* out_dev, void* stream) {
+  DLLM_CHECK_HANDLE(c);
+  if (!h_dev || !w1_dev || !w2_dev || !out_dev) return fail(DLLM_EINVAL, "ffn_gelu: null pointer");
+  if (F != c->ffn_cap || F <= 0) return fail(DLLM_EINVAL, "ffn_gelu: F must equal the cache's ffn");
+  if (!m_dev && (M < 0 || M > c->seq_rows)) return fail(DLLM_EINVAL, "ffn_gelu: M outside [0, B*L]");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int cap = m_dev ? c->seq_rows : M;
+  DLLM_LAUNCH(launch_rownorm(c, h_dev, cap, m_dev, c->d, c->rs, st), "ffn_gelu: norm");
+  DLLM_LAUNCH(gemm_gelu(c, h_dev, w1_dev, M, c->seq_rows, m_dev, F, c->d, c->rs, c->ffn_buf, st), "ffn_gelu: W1");
+  DLLM_LAUNCH(gemm_resid(c, c->ffn_buf, w2_dev, M, c->seq_rows, m_dev, c->d, F, h_dev, nullptr, nullptr, 0, 1,
+                         out_dev, st),
+              "ffn_gelu: W2");
+  return DLLM_OK;
+}
+
+dllm_status lmhead_conf(dllm_cache* c, const void* h_dev, const void* w_lm_dev, int M, int V, int d, int mask_id,
+                        int32_t* argmax_dev, float* p_top1_dev, float* entropy_dev, void* stream) {
+  DLLM_CHECK_HANDLE(c);
+  if (!h_dev || !w_lm_dev || !argmax_dev || !p_top1_dev || !entropy_dev)
+    return fail(DLLM_EINVAL, "lmhead_conf: null pointer");
+  if (M < 0 || M > c->lm_rows_cap) return fail(DLLM_EINVAL, "lmhead_conf: M outside [0, batch * block_len]");
+  if (V < 2 || V > c->cfg.vocab) return fail(DLLM_EINVAL, "lmhead_conf: V outside [2, vocab]");
+  if (d != c->d) return fail(DLLM_EINVAL, "lmhead_conf: d must equal n_heads * head_dim");
+  if (mask_id >= V) return fail(DLLM_EINVAL, "lmhead_conf: mask_id >= V");
+  if (!aligned16(h_dev) || !aligned16(w_lm_dev)) return fail(DLLM_EINVAL, "lmhead_conf: pointers not 16-byte aligned");
+  if (M == 0) return DLLM_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int n_tiles = cdiv(V, 128);
+  DLLM_LAUNCH(launch_rownorm(c, h_dev, M, nullptr, d, c->lm_rs, st), "lmhead_conf: norm");
+  DLLM_LAUNCH(gemm_lm(c, h_dev, w_lm_dev, M, V, d, c->lm_rs, mask_id, c->lm_part, n_tiles, st), "lmhead_conf: gemm");
+  DLLM_LAUNCH(launch_lm_merge(c->lm_part, M, n_tiles, argmax_dev, p_top1_dev, entropy_dev, st), "lmhead_conf: merge");
+  return DLLM_OK;
+}
+
+dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p_top1_dev, int32_t* tok_dev,
+                        int q_start, int t, int last_step, int32_t* rows_dev, int32_t* n_rows_dev, void* stream) {
+  DLLM_CHECK_HANDLE(c);
+  const dllm_cache_cfg& g = c->cfg;
+  if (g.sink > 0) return fail(DLLM_EINVAL, "stab_update: dense mode only");
+  if (!argmax_dev || !p_top1_dev || !tok_dev || !rows_dev || !n_rows_dev)
+    return fail(DLLM_EINVAL, "stab_update: null pointer");
+  if (q_start < 0 || q_start + g.block_len > g.seq_len)
+    return fail(DLLM_EINVAL, "stab_update: active block outside the sequence");
+  DLLM_LAUNCH(launch_stab(c, argmax_dev, p_top1_dev, tok_dev, q_start, t, last_step ? 1 : 0, rows_dev, n_rows_dev,
+                          static_cast<cudaStream_t>(stream)),
+              "stab_update");
+  return DLLM_OK;
+}
+
+}  // extern "C"

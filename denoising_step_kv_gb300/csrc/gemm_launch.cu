@@ -1,0 +1,128 @@
+// Instantiations and launchers of the projection GEMMs.
+#include <algorithm>
+
+#include "epilogue.cuh"
+#include "gemm.cuh"
+#include "internal.h"
+
+namespace dllm {
+namespace {
+
+
+template <class Epi>
+cudaError_t run_tc(dllm_cache* c, const void* A, int a_rows, int M_host, const int* M_dev, const void* B, int N,
+                   int K, const Epi& epi, cudaStream_t st) {
+  if (!M_dev && M_host <= 0) return cudaSuccess;
+  CUtensorMap ta, tb;
+  if (!make_tmap_2d(&ta, A, K, a_rows, static_cast<uint64_t>(K) * 2, tc::BK, tc::BM, true) ||
+      !make_tmap_2d(&tb, B, K, N, static_cast<uint64_t>(K) * 2, tc::BK, tc::BN, true))
+    return cudaErrorInvalidValue;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(tc::gemm_tc_kernel<Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(tc::SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int m_rows = M_dev ? a_rows : M_host;
+  const int tiles = cdiv(m_rows, tc::BM) * cdiv(N, tc::BN);
+  const int grid = std::max(1, std::min(tiles, c->num_sms));
+  tc::gemm_tc_kernel<Epi><<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ta, tb, M_host, M_dev, a_rows, N, K, epi,
+                                                                    c->err);
+  return cudaGetLastError();
+}
+
+template <int NCH, class Epi>
+cudaError_t run_simt(const void* A, int m_cap, int M_host, const int* M_dev, const void* B, int N, int K,
+                     const Epi& epi, cudaStream_t st) {
+  const int m_rows = M_dev ? m_cap : M_host;
+  if (m_rows <= 0) return cudaSuccess;
+  dim3 grid(cdiv(m_rows, 128), cdiv(N, 32 * NCH));
+  simt::gemm_simt_kernel<float, NCH, Epi><<<grid, 128, 0, st>>>(
+      static_cast<const float*>(A), static_cast<const float*>(B), M_host, M_dev, m_cap, N, K, epi);
+  return cudaGetLastError();
+}
+
+template <typename T, int DH, int NCH>
+EpiQKV<T, DH, NCH> make_qkv(dllm_cache* c, int layer, const int* rows) {
+  EpiQKV<T, DH, NCH> e;
+  const size_t off = static_cast<size_t>(layer) * c->rows * c->d;
+  e.rows = rows;
+  e.rs = c->rs;
+  e.q = static_cast<T*>(c->q) + off;
+  e.k = static_cast<T*>(c->k) + off;
+  e.v = static_cast<T*>(c->v) + off;
+  e.rope = c->rope;
+  e.L = c->cfg.seq_len;
+  e.d = c->d;
+  e.rows_cap = c->rows;
+  e.streaming = c->cfg.sink > 0;
+  e.S = c->cfg.sink;
+  e.W = c->cfg.window;
+  e.max_pos = c->max_pos;
+  return e;
+}
+
+template <int DH>
+cudaError_t qkv_dh(dllm_cache* c, int layer, const void* A, int M_cap, const int* M_dev, const int* rows,
+                   const void* w, cudaStream_t st) {
+  const int d = c->d, N = 3 * d;
+  const int M_host = M_dev ? 0 : M_cap;
+  if (c->cfg.dtype == DLLM_BF16)
+    return run_tc(c, A, M_cap, M_host, M_dev, w, N, d, make_qkv<bf16, DH, 4>(c, layer, rows), st);
+  if (d % 128 == 0) return run_simt<4>(A, M_cap, M_host, M_dev, w, N, d, make_qkv<float, DH, 4>(c, layer, rows), st);
+  if constexpr (DH <= 64)
+    return run_simt<2>(A, M_cap, M_host, M_dev, w, N, d, make_qkv<float, DH, 2>(c, layer, rows), st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int lm_tile_cols(const dllm_cache*) { return 128; }
+
+cudaError_t gemm_qkv(dllm_cache* c, int layer, const void* A, int M_cap, const int* M_dev, const int* rows,
+                     const void* w_qkv, cudaStream_t st) {
+  switch (c->cfg.head_dim) {
+    case 32: return qkv_dh<32>(c, layer, A, M_cap, M_dev, rows, w_qkv, st);
+    case 64: return qkv_dh<64>(c, layer, A, M_cap, M_dev, rows, w_qkv, st);
+    case 128: return qkv_dh<128>(c, layer, A, M_cap, M_dev, rows, w_qkv, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t gemm_resid(dllm_cache* c, const void* A, const void* W, int M, int M_cap, const int* M_dev, int N,
+                       int K, const void* xres, const int* tok, const void* embed, int q_start, int q_len,
+                       void* out, cudaStream_t st) {
+  if (c->cfg.dtype == DLLM_BF16) {
+    EpiResid<bf16, 4> e{static_cast<const bf16*>(xres), static_cast<const bf16*>(embed), tok, q_start, q_len,
+                        c->cfg.seq_len, c->cfg.vocab, static_cast<bf16*>(out), c->err};
+    return run_tc(c, A, M_dev ? M_cap : M, M, M_dev, W, N, K, e, st);
+  }
+  if (N % 128 == 0) {
+    EpiResid<float, 4> e{static_cast<const float*>(xres), static_cast<const float*>(embed), tok, q_start, q_len,
+                         c->cfg.seq_len, c->cfg.vocab, static_cast<float*>(out), c->err};
+    return run_simt<4>(A, M_cap, M, M_dev, W, N, K, e, st);
+  }
+  EpiResid<float, 1> e{static_cast<const float*>(xres), static_cast<const float*>(embed), tok, q_start, q_len,
+                       c->cfg.seq_len, c->cfg.vocab, static_cast<float*>(out), c->err};
+  return run_simt<1>(A, M_cap, M, M_dev, W, N, K, e, st);
+}
+
+cudaError_t gemm_gelu(dllm_cache* c, const void* A, const void* W, int M, int M_cap, const int* M_dev, int N,
+                      int K, const float* rs, void* out, cudaStream_t st) {
+  if (c->cfg.dtype == DLLM_BF16) {
+    EpiGelu<bf16, 4> e{rs, static_cast<bf16*>(out)};
+    return run_tc(c, A, M_dev ? M_cap : M, M, M_dev, W, N, K, e, st);
+  }
+  EpiGelu<float, 1> e{rs, static_cast<float*>(out)};
+  return run_simt<1>(A, M_cap, M, M_dev, W, N, K, e, st);
+}
+
+cudaError_t gemm_lm(dllm_cache* c, const void* A, const void* W, int M, int V, int d, const float* rs,
+                    int mask_id, void* part, int n_tiles, cudaStream_t st) {
+  EpiLM<4> e{rs, mask_id, static_cast<LMPart*>(part), n_tiles};
+  if (c->cfg.dtype == DLLM_BF16) return run_tc(c, A, M, M, nullptr, W, V, d, e, st);
+  return run_simt<4>(A, M, M, nullptr, W, V, d, e, st);
+}
+
+}  // namespace dllm

@@ -1,0 +1,83 @@
+// Host-side internals shared by the translation units of libdllmkv.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "dllm_kv.h"
+
+struct dllm_cache {
+  dllm_cache_cfg cfg;
+  int device = 0;
+  int num_sms = 0;
+  int d = 0;            // n_heads * head_dim
+  int rows = 0;         // cache rows per layer: B*L (dense) or S+W (streaming)
+  int seq_rows = 0;     // B*L for bookkeeping arrays (dense), S+W streaming
+  int max_pos = 0;      // RoPE table rows
+  int Lw = 0;           // 32-position words per sequence
+  size_t elem = 2;      // bytes per element of the cache dtype
+  // state
+  void* q = nullptr;    // [n_layers][rows][d]
+  void* k = nullptr;
+  void* v = nullptr;
+  int* version = nullptr;   // [n_layers][seq_rows]
+  int* tok_w = nullptr;     // [seq_rows]
+  uint8_t* stable = nullptr;
+  int* hist_tok = nullptr;  // [B][blk][K]
+  float* hist_p = nullptr;
+  int* hist_n = nullptr;    // [B][blk]
+  uint32_t* words = nullptr;// [B][Lw] refresh flags
+  float2* rope = nullptr;   // [max_pos][head_dim/2]
+  unsigned* err = nullptr;  // device error word
+  // scratch
+  void* X = nullptr;        // gathered layer inputs [seq_rows][d]
+  float* rs = nullptr;      // RMS scales [seq_rows]
+  void* lm_part = nullptr;  // [B*blk][ceil(V/128)] LMPart
+  float* lm_rs = nullptr;   // [B*blk]
+  int lm_rows_cap = 0, lm_tiles_cap = 0;
+  void* ffn_buf = nullptr;  // [seq_rows][ffn]
+  int ffn_cap = 0;
+};
+
+namespace dllm {
+
+void set_error(const std::string& msg);
+
+// tensor maps (driver entry point resolved once)
+bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                  uint32_t box_inner, uint32_t box_outer, bool bf16);
+
+// gemm_launch.cu -----------------------------------------------------------
+// bf16 or fp32 D = A . B^T with the named epilogue.  M: host rows, or the
+// device count M_dev (then M_cap bounds the grid and A's row extent).
+cudaError_t gemm_qkv(dllm_cache* c, int layer, const void* A, int M_cap, const int* M_dev, const int* rows,
+                     const void* w_qkv, cudaStream_t st);
+cudaError_t gemm_resid(dllm_cache* c, const void* A, const void* W, int M, int M_cap, const int* M_dev, int N,
+                       int K, const void* xres, const int* tok, const void* embed, int q_start, int q_len,
+                       void* out, cudaStream_t st);
+cudaError_t gemm_gelu(dllm_cache* c, const void* A, const void* W, int M, int M_cap, const int* M_dev, int N,
+                      int K, const float* rs, void* out, cudaStream_t st);
+cudaError_t gemm_lm(dllm_cache* c, const void* A, const void* W, int M, int V, int d, const float* rs,
+                    int mask_id, void* part, int n_tiles, cudaStream_t st);
+int lm_tile_cols(const dllm_cache* c);
+
+// attn.cu ------------------------------------------------------------------
+cudaError_t attn_dense(dllm_cache* c, int layer, int q_row0, int q_seq_stride, int q_len, int kv_row0,
+                       int kv_seq_stride, int kv_len, int n_seq, void* out, int out_seq_stride,
+                       cudaStream_t st);
+
+// misc.cu ------------------------------------------------------------------
+cudaError_t launch_gather(dllm_cache* c, int layer, const int* rows, const int* n_rows, int n_host,
+                          const void* x, const int* tok, const void* embed, int t, cudaStream_t st);
+cudaError_t launch_rownorm(dllm_cache* c, const void* h, int M, const int* M_dev, int d, float* rs,
+                           cudaStream_t st);
+cudaError_t launch_lm_merge(const void* part, int M, int n_tiles, int* argmax, float* p1, float* ent,
+                            cudaStream_t st);
+cudaError_t launch_stab(dllm_cache* c, const int* argmax, const float* p1, int* tok, int q_start, int t,
+                        int last, int* rows, int* n_rows, cudaStream_t st);
+cudaError_t launch_refresh_all(dllm_cache* c, int q_start, int* rows, int* n_rows, cudaStream_t st);
+cudaError_t launch_reset(dllm_cache* c, cudaStream_t st);
+
+}  // namespace dllm

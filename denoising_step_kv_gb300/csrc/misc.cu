@@ -1,0 +1,343 @@
+// Row gather + RMS scale, LM-head tile merge, the Stable-Window-Decoding
+// update with refresh-set construction, and state reset.
+#include <algorithm>
+
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "internal.h"
+
+namespace dllm {
+namespace {
+
+constexpr int NEVER = -(1 << 30);   // version of a never-written entry
+
+template <typename T> struct Vec;
+template <> struct Vec<bf16> { static constexpr int N = 8; };
+template <> struct Vec<float> { static constexpr int N = 4; };
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// One warp per refreshed row: validate the row and its token, copy the layer
+// input into the compact buffer X (layer-0 embedding rows; a caller-given
+// input is used in place), compute the RMSNorm scale, and stamp the row's
+// version and token-at-write.
+template <typename T>
+__global__ void __launch_bounds__(256) gather_kernel(const int* __restrict__ rows, const int* __restrict__ n_rows,
+                                                     int n_host, const T* __restrict__ x, const int* __restrict__ tok,
+                                                     const T* __restrict__ embed, T* __restrict__ X,
+                                                     float* __restrict__ rs, int* __restrict__ tok_w,
+                                                     int* __restrict__ version, int t, int d, int rows_cap,
+                                                     int max_pos, int streaming, int vocab, float eps, int x_cap,
+                                                     unsigned* err) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 8 + warp;
+  int n = n_rows ? *n_rows : n_host;
+  if (n > x_cap) {          // more rows than the compact buffers hold
+    if (i == 0 && lane == 0) set_err(err, DLLM_ERR_ROW);
+    n = x_cap;
+  }
+  if (i >= n) return;
+  const int row = rows ? rows[i] : i;
+  const bool row_ok = streaming ? (row >= 0 && row < max_pos) : (row >= 0 && row < rows_cap);
+  if (!row_ok) {
+    if (lane == 0) {
+      set_err(err, DLLM_ERR_ROW);
+      rs[i] = -1.f;
+    }
+    return;
+  }
+  const T* src;
+  int token = -1;
+  if (x) {
+    src = x + static_cast<size_t>(i) * d;
+  } else {
+    token = tok[row];
+    if (token < 0 || token >= vocab) {
+      if (lane == 0) {
+        set_err(err, DLLM_ERR_TOKEN);
+        rs[i] = -1.f;
+      }
+      return;
+    }
+    src = embed + static_cast<size_t>(token) * d;
+  }
+  constexpr int VN = Vec<T>::N;
+  float ss = 0.f;
+  for (int c = lane * VN; c < d; c += 32 * VN) {
+    float v[VN];
+    load_row(src + c, v, VN);
+#pragma unroll
+    for (int j = 0; j < VN; ++j) ss = fmaf(v[j], v[j], ss);
+    if (!x) store_row(X + static_cast<size_t>(i) * d + c, v, VN);
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) {
+    rs[i] = rsqrtf(ss / static_cast<float>(d) + eps);
+    if (!streaming) {
+      if (version) version[row] = t;
+      if (tok_w && token >= 0) tok_w[row] = token;
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) rownorm_kernel(const T* __restrict__ h, int M_host, const int* M_dev, int d,
+                                                      float eps, float* __restrict__ rs) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 8 + warp;
+  const int M = M_dev ? *M_dev : M_host;
+  if (i >= M) return;
+  constexpr int VN = Vec<T>::N;
+  float ss = 0.f;
+  for (int c = lane * VN; c < d; c += 32 * VN) {
+    float v[VN];
+    load_row(h + static_cast<size_t>(i) * d + c, v, VN);
+#pragma unroll
+    for (int j = 0; j < VN; ++j) ss = fmaf(v[j], v[j], ss);
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) rs[i] = rsqrtf(ss / static_cast<float>(d) + eps);
+}
+
+// One warp per row: merge the per-tile statistics (tiles in increasing vocab
+// order per lane, then across lanes with the lower index winning ties).
+__global__ void __launch_bounds__(256) lm_merge_kernel(const LMPart* __restrict__ part, int M, int n_tiles,
+                                                       int* __restrict__ argmax, float* __restrict__ p1,
+                                                       float* __restrict__ ent) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 8 + warp;
+  if (i >= M) return;
+  float m = -INFINITY, s = 0.f, a = 0.f;
+  int idx = 0x7fffffff;
+  for (int tt = lane; tt < n_tiles; tt += 32) {
+    const LMPart p = part[static_cast<size_t>(i) * n_tiles + tt];
+    lm_merge(m, s, a, idx, p.m, p.s, p.a, p.idx);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    const float a2 = __shfl_xor_sync(0xffffffffu, a, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    lm_merge(m, s, a, idx, m2, s2, a2, i2);
+  }
+  if (lane == 0) {
+    argmax[i] = idx;
+    p1[i] = 1.f / s;
+    ent[i] = logf(s) - a / s;
+  }
+}
+
+// Stable-Window-Decoding update of the active block of sequence blockIdx.x,
+// then one flag bit per position for the next step's refresh set.
+__global__ void __launch_bounds__(1024) swd_kernel(
+    const int* __restrict__ argmax, const float* __restrict__ p1, int* __restrict__ tok,
+    uint8_t* __restrict__ stable, int* __restrict__ hist_tok, float* __restrict__ hist_p, int* __restrict__ hist_n,
+    const int* __restrict__ tok_w, const int* __restrict__ version, uint32_t* __restrict__ words, int L, int Lw,
+    int seq_rows, int n_layers, int blk, int K, float tau, int R, int q0, int t, int last, int expiry,
+    int refresh_active) {
+  __shared__ uint8_t s_unst[64];
+  const int b = blockIdx.x;
+  const int nac = min(blk, L - q0);
+  if (threadIdx.x < nac) {
+    const int j = threadIdx.x;
+    const int r = b * L + q0 + j;
+    const int h = b * blk + j;
+    bool st = stable[r] != 0;
+    const int a = argmax[h];
+    if (!st) {
+      int n = hist_n[h];
+      hist_tok[h * K + n % K] = a;
+      hist_p[h * K + n % K] = p1[h];
+      ++n;
+      hist_n[h] = n;
+      if (n >= K) {
+        bool same = true;
+        float s = 0.f;
+        for (int k = 0; k < K; ++k) {        // oldest -> newest
+          const int slot = (n - K + k) % K;
+          same = same && hist_tok[h * K + slot] == a;
+          s = s + hist_p[h * K + slot];
+        }
+        const float mean = s / static_cast<float>(K);
+        if (same && mean > tau) {
+          st = true;
+          stable[r] = 1;
+          tok[r] = a;
+        }
+      }
+    }
+    if (last) {
+      if (!st) tok[r] = a;
+      hist_n[h] = 0;
+    }
+    s_unst[j] = st ? 0 : 1;
+  }
+  __syncthreads();
+  for (int base = 0; base < L; base += blockDim.x) {
+    const int p = base + threadIdx.x;
+    bool f = false;
+    if (p < L) {
+      const int r = b * L + p;
+      if (last) {
+        f = true;
+      } else {
+        const int lo = max(p - R, q0), hi = min(p + R, q0 + nac - 1);
+        for (int u = lo; u <= hi; ++u) f = f || s_unst[u - q0];
+        if (refresh_active && p >= q0 && p < q0 + nac) f = true;
+        f = f || tok[r] != tok_w[r];
+        if (expiry >= 0)
+          for (int l = 0; l < n_layers; ++l) f = f || (t + 1) - version[l * seq_rows + r] > expiry;
+      }
+    }
+    const uint32_t word = __ballot_sync(0xffffffffu, f);
+    const int w = (base + (threadIdx.x & ~31)) >> 5;
+    if ((threadIdx.x & 31) == 0 && w < Lw) words[b * Lw + w] = word;
+  }
+}
+
+__global__ void __launch_bounds__(1024) fill_words_kernel(uint32_t* words, int B, int L, int Lw) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < B * Lw; i += gridDim.x * blockDim.x) {
+    const int w = i % Lw;
+    const int valid = min(32, L - w * 32);
+    words[i] = valid >= 32 ? 0xffffffffu : ((1u << valid) - 1u);
+  }
+}
+
+// Compact the flag words into ascending row ids b * L + pos (block-wide
+// exclusive scan of the per-word popcounts, one word per thread per pass).
+__global__ void __launch_bounds__(1024) compact_kernel(const uint32_t* __restrict__ words, int nw, int L, int Lw,
+                                                       int* __restrict__ rows, int* __restrict__ n_rows) {
+  __shared__ int s_warp[32];
+  __shared__ int s_base;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_base = 0;
+  __syncthreads();
+  for (int base = 0; base < nw; base += blockDim.x) {
+    const int w = base + tid;
+    uint32_t word = w < nw ? words[w] : 0u;
+    const int cnt = __popc(word);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int x = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      s_warp[lane] = x;   // inclusive prefix of warp totals
+    }
+    __syncthreads();
+    int off = s_base + incl - cnt + (warp > 0 ? s_warp[warp - 1] : 0);
+    if (w < nw) {
+      const int rb = (w / Lw) * L + (w % Lw) * 32;
+      while (word) {
+        const int bit = __ffs(word) - 1;
+        word &= word - 1u;
+        rows[off++] = rb + bit;
+      }
+    }
+    __syncthreads();
+    if (tid == 0) s_base += s_warp[(blockDim.x >> 5) - 1];
+    __syncthreads();
+  }
+  if (tid == 0) *n_rows = s_base;
+}
+
+__global__ void reset_kernel(int* version, int n_version, int* tok_w, uint8_t* stable, int n_rows, int* hist_n,
+                             int n_hist, unsigned* err) {
+  const int i0 = blockIdx.x * blockDim.x + threadIdx.x, step = gridDim.x * blockDim.x;
+  for (int i = i0; i < n_version; i += step) version[i] = NEVER;
+  for (int i = i0; i < n_rows; i += step) {
+    tok_w[i] = -1;
+    stable[i] = 0;
+  }
+  for (int i = i0; i < n_hist; i += step) hist_n[i] = 0;
+  if (i0 == 0) *err = 0u;
+}
+
+}  // namespace
+
+cudaError_t launch_gather(dllm_cache* c, int layer, const int* rows, const int* n_rows, int n_host, const void* x,
+                          const int* tok, const void* embed, int t, cudaStream_t st) {
+  const bool dense = c->cfg.sink == 0;
+  const int cap = rows ? c->seq_rows : n_host;    // rows of the compact buffers
+  if (cap <= 0) return cudaSuccess;
+  int* version = dense ? c->version + static_cast<size_t>(layer) * c->seq_rows : nullptr;
+  int* tok_w = (dense && layer == 0 && !x) ? c->tok_w : nullptr;
+  const dim3 grid(cdiv(cap, 8));
+  if (c->cfg.dtype == DLLM_BF16)
+    gather_kernel<bf16><<<grid, 256, 0, st>>>(rows, rows ? n_rows : nullptr, n_host, static_cast<const bf16*>(x),
+                                               tok, static_cast<const bf16*>(embed), static_cast<bf16*>(c->X), c->rs,
+                                               tok_w, version, t, c->d, c->rows, c->max_pos, !dense, c->cfg.vocab,
+                                               c->cfg.rms_eps, c->seq_rows, c->err);
+  else
+    gather_kernel<float><<<grid, 256, 0, st>>>(rows, rows ? n_rows : nullptr, n_host, static_cast<const float*>(x),
+                                                tok, static_cast<const float*>(embed), static_cast<float*>(c->X),
+                                                c->rs, tok_w, version, t, c->d, c->rows, c->max_pos, !dense,
+                                                c->cfg.vocab, c->cfg.rms_eps, c->seq_rows, c->err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rownorm(dllm_cache* c, const void* h, int M, const int* M_dev, int d, float* rs,
+                           cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  if (c->cfg.dtype == DLLM_BF16)
+    rownorm_kernel<bf16><<<cdiv(M, 8), 256, 0, st>>>(static_cast<const bf16*>(h), M, M_dev, d, c->cfg.rms_eps, rs);
+  else
+    rownorm_kernel<float><<<cdiv(M, 8), 256, 0, st>>>(static_cast<const float*>(h), M, M_dev, d, c->cfg.rms_eps,
+                                                       rs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lm_merge(const void* part, int M, int n_tiles, int* argmax, float* p1, float* ent,
+                            cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  lm_merge_kernel<<<cdiv(M, 8), 256, 0, st>>>(static_cast<const LMPart*>(part), M, n_tiles, argmax, p1, ent);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stab(dllm_cache* c, const int* argmax, const float* p1, int* tok, int q_start, int t, int last,
+                        int* rows, int* n_rows, cudaStream_t st) {
+  const dllm_cache_cfg& g = c->cfg;
+  swd_kernel<<<g.batch, 1024, 0, st>>>(argmax, p1, tok, c->stable, c->hist_tok, c->hist_p, c->hist_n, c->tok_w,
+                                       c->version, c->words, g.seq_len, c->Lw, c->seq_rows, g.n_layers, g.block_len,
+                                       g.swd_K, g.swd_tau, g.swd_R, q_start, t, last, g.expiry, g.refresh_active);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  compact_kernel<<<1, 1024, 0, st>>>(c->words, g.batch * c->Lw, g.seq_len, c->Lw, rows, n_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_refresh_all(dllm_cache* c, int q_start, int* rows, int* n_rows, cudaStream_t st) {
+  (void)q_start;
+  const dllm_cache_cfg& g = c->cfg;
+  fill_words_kernel<<<std::min(cdiv(g.batch * c->Lw, 1024), 64), 1024, 0, st>>>(c->words, g.batch, g.seq_len,
+                                                                                   c->Lw);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  compact_kernel<<<1, 1024, 0, st>>>(c->words, g.batch * c->Lw, g.seq_len, c->Lw, rows, n_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reset(dllm_cache* c, cudaStream_t st) {
+  const dllm_cache_cfg& g = c->cfg;
+  const int nv = g.n_layers * c->seq_rows;
+  const int nh = g.batch * g.block_len;
+  reset_kernel<<<std::max(1, std::min(cdiv(std::max(nv, c->seq_rows), 256), 1024)), 256, 0, st>>>(
+      c->version, nv, c->tok_w, c->stable, c->seq_rows, c->hist_n, nh, c->err);
+  return cudaGetLastError();
+}
+
+}  // namespace dllm

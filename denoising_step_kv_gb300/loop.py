@@ -1,0 +1,132 @@
+"""Step-loop driver of the cached denoising step on one GPU.
+
+A generation runs every SAR block for Tb denoising steps on one CUDA stream.
+One step of a single-layer denoiser is:
+
+    kv_refresh   rows of the refresh set -> versioned Q/K/V cache
+    block_attn   active block's queries over the whole cached sequence
+    attn_out     h = x + O W_o^T
+    lmhead_conf  argmax, top-1 probability, entropy of the active rows
+    stab_update  SWD update, commits, next step's refresh set
+
+The refresh-set size stays on the device, so no step synchronises with the
+host and a whole generation can be captured as one CUDA graph.
+"""
+import numpy as np
+import torch
+
+from . import _lib as K
+
+
+def to_device(a, device="cuda"):
+    """Generated array -> device tensor (uint16 bf16 bit patterns -> bfloat16)."""
+    if isinstance(a, list):
+        return [to_device(x, device) for x in a]
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+class DenseGenerator:
+    """Single-layer cached denoiser (dense positional cache)."""
+
+    def __init__(self, w, weights, device="cuda"):
+        assert not w.streaming and w.n_layers == 1 and not w.ffn
+        self.w = w
+        self.W = weights
+        B, L, d, blk = w.batch, w.seq_len, w.d_model, w.block_len
+        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        self.cache = K.dllm_cache_init(K.make_cfg(w))
+        i32 = dict(dtype=torch.int32, device=device)
+        self.tok = torch.zeros(B, L, **i32)
+        self.rows = torch.zeros(B * L, **i32)
+        self.n_rows = torch.zeros(1, **i32)
+        self.o = torch.zeros(B * blk, d, dtype=dt, device=device)
+        self.h = torch.zeros(B * blk, d, dtype=dt, device=device)
+        self.argmax = torch.zeros(B * blk, **i32)
+        self.p1 = torch.zeros(B * blk, dtype=torch.float32, device=device)
+        self.ent = torch.zeros(B * blk, dtype=torch.float32, device=device)
+        self.tok_in = torch.zeros(B, L, **i32)
+        self.graph = None
+        self.lm_events = None
+
+    def close(self):
+        if self.cache is not None:
+            K.dllm_cache_free(self.cache)
+            self.cache = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- one step -------------------------------------------------------------
+    def step(self, t, q0, s, stream=None, lm_event_pair=None):
+        w, c, W = self.w, self.cache, self.W
+        blk = w.block_len
+        if t == 0:
+            K.refresh_all(c, q0, self.rows, self.n_rows, stream)
+        K.kv_refresh(c, 0, None, self.tok, W["embed"], W["w_qkv"][0], self.rows, self.n_rows, t, stream)
+        K.block_attn(c, 0, q0, blk, self.o, stream)
+        K.attn_out(c, self.o, W["w_o"][0], None, self.tok, W["embed"], q0, blk, None, self.h, stream)
+        if lm_event_pair is not None:
+            lm_event_pair[0].record(stream)
+        K.lmhead_conf(c, self.h, W["w_lm"], w.batch * blk, w.vocab, w.d_model, w.mask_id, self.argmax,
+                      self.p1, self.ent, stream)
+        if lm_event_pair is not None:
+            lm_event_pair[1].record(stream)
+        K.stab_update(c, self.argmax, self.p1, self.tok, q0, t, s == w.steps_per_block - 1, self.rows,
+                      self.n_rows, stream)
+
+    def schedule(self):
+        """(t, q0, s) of every step of a generation."""
+        w = self.w
+        t = 0
+        for bi in range(w.n_blocks):
+            q0 = w.n_prompt + bi * w.block_len
+            for s in range(w.steps_per_block):
+                yield t, q0, s
+                t += 1
+
+    def run(self, stream=None, on_step=None, n_steps=None, time_lm=False):
+        """Reset the cache, copy tok_in -> tok and run the step loop."""
+        K.dllm_cache_reset(self.cache, stream)
+        self.tok.copy_(self.tok_in)
+        events = []
+        for t, q0, s in self.schedule():
+            if n_steps is not None and t >= n_steps:
+                break
+            pair = None
+            if time_lm:
+                pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                events.append(pair)
+            self.step(t, q0, s, stream, pair)
+            if on_step is not None:
+                on_step(t, q0, s)
+        self.lm_events = events if time_lm else None
+        return self.tok
+
+    def generate(self, tok0):
+        self.tok_in.copy_(tok0)
+        return self.run()
+
+    # -- CUDA graph of a whole generation -------------------------------------------
+    def capture(self, time_lm=False):
+        """Capture run() as one CUDA graph (after one eager warm-up run)."""
+        self.run()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run(time_lm=time_lm)
+        self.graph = g
+        return g
+
+    def replay(self):
+        self.graph.replay()
+        return self.tok
+
+    def lm_times_ms(self):
+        """Durations of the LM-head launches recorded by the last run/replay."""
+        return [a.elapsed_time(b) for a, b in (self.lm_events or [])]

@@ -1,0 +1,245 @@
+/*
+ * dllm_kv.h -- C ABI of one cached denoising step of a masked diffusion LM
+ * on a single GB300 (sm_103a).
+ *
+ * One denoising step runs, in this order, on one CUDA stream:
+ *   kv_refresh   gather the rows of the refresh set, RMSNorm, QKV projection,
+ *                RoPE, scatter into the versioned per-layer cache (version = t);
+ *   block_attn   the active block's queries attend bidirectionally over the
+ *                whole cached sequence (or over the sink + rolling window);
+ *   attn_out     residual stream h = x + O . W_o^T;
+ *   lmhead_conf  per active row: argmax, top-1 probability and entropy of
+ *                softmax(RMSNorm(h) . W_lm^T) with the mask id excluded;
+ *                logits never reach memory;
+ *   stab_update  Stable-Window-Decoding history push, stability test,
+ *                commit, dilation by R, version expiry, and compaction of the
+ *                refresh set of the next step.
+ *
+ * Sources (page title and section):
+ *   "LaCache: Exact Caching and Precision-Adaptive Inference for Diffusion
+ *     Large Language Models", Problem statement, Methodology 1 (LSM) and 3
+ *     (Inference workflow): token-level operators (embedding, normalisation,
+ *     QKV projection, RoPE) of unchanged tokens are reused; a block's first
+ *     step runs a full forward.
+ *   "Stable Window Decoding" page (wmrh.cn/news/51151), 3.1-3.3 and 4.2:
+ *     stability over the last K steps with mean top-1 probability > tau,
+ *     unstable positions dilated by R.
+ *   "Diffusion latent cache with time anchors" page (mhpq.cn/news/1098081),
+ *     2.3 and 3.1: every cache entry carries its write step; an entry with
+ *     t - version > 2 is rejected.
+ *   "Attention Sinks and Where to Cache Them" explainer (wmrh.cn/news/159578),
+ *     2.3 and 3.1-3.3: S sink entries plus a rolling window of W entries, a
+ *     cache of constant size S + W, positions that never roll.
+ *   "I/O-aware KV cache and self-verifying parallel decoding"
+ *     (bjdmk.com.cn/news/5926815), 3.1: per-position entropy.
+ *
+ * Conventions
+ *   Pointers named *_dev or documented as device pointers are CUDA device
+ *   pointers; every call is asynchronous on `stream` (a cudaStream_t, NULL =
+ *   legacy default stream) and never synchronises, except dllm_cache_check
+ *   and dllm_state_copy.  The caller owns every input, output and weight;
+ *   the library owns only what dllm_cache_init allocates.
+ *   Row layout: a dense cache row is r = b * L + pos; every row is d =
+ *   n_heads * head_dim contiguous elements, heads contiguous inside a row.
+ *   bf16 data is passed as 16-bit patterns (uint16), fp32 as float.
+ *   Errors: an invalid argument returns a status != DLLM_OK, launches nothing
+ *   and sets a message readable with dllm_last_error().  Problems found on
+ *   the device (row or token out of range, a wait that timed out) set bits in
+ *   the handle's device error word and skip the item; dllm_cache_check reads
+ *   and clears that word.  No kernel traps.
+ *   Handles are not thread-safe: one host thread per handle at a time.
+ */
+#ifndef DLLM_KV_H
+#define DLLM_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DLLM_OK = 0,
+  DLLM_EINVAL = 1,       /* bad argument: nothing launched */
+  DLLM_ENOMEM = 2,       /* device allocation failed in dllm_cache_init */
+  DLLM_ECUDA = 3,        /* a CUDA runtime call failed */
+  DLLM_EDEVICE = 4,      /* the device error word was set (dllm_cache_check) */
+  DLLM_EUNSUPPORTED = 5  /* shape outside what the kernels implement */
+} dllm_status;
+
+typedef enum { DLLM_F32 = 0, DLLM_BF16 = 1 } dllm_dtype;
+
+/* device error word bits */
+#define DLLM_ERR_ROW      0x1u   /* row index outside [0, rows) */
+#define DLLM_ERR_TOKEN    0x2u   /* token id outside [0, vocab) */
+#define DLLM_ERR_TIMEOUT  0x4u   /* a bounded wait on a barrier gave up */
+#define DLLM_ERR_POS      0x8u   /* position outside the RoPE table */
+
+typedef struct {
+  int n_layers;      /* layers with a cache (1 for a single attention layer) */
+  int batch;         /* B sequences (1 in streaming mode) */
+  int seq_len;       /* L positions of every sequence (dense mode) */
+  int n_heads;       /* H */
+  int head_dim;      /* dh; bf16 needs 64 or 128, fp32 needs 32, 64 or 128 */
+  int dtype;         /* dllm_dtype of weights, caches and activations */
+  int sink;          /* S sink entries; > 0 selects streaming mode */
+  int window;        /* W rolling entries (streaming mode) */
+  int expiry;        /* reject t - version > expiry; < 0 = no expiry */
+  float rope_theta;  /* RoPE base, 10000 */
+  float rms_eps;     /* RMSNorm epsilon, 1e-6 */
+  int swd_K;         /* steps a top-1 token must persist (<= 8) */
+  float swd_tau;     /* mean top-1 probability threshold (strict >) */
+  int swd_R;         /* dilation radius of unstable positions */
+  int block_len;     /* active block length (<= 64) */
+  int mask_id;       /* id of the mask token */
+  int refresh_active;/* 1: the active block always joins the refresh set,
+                        listed first (multi-layer denoiser) */
+  int vocab;         /* V: token ids are checked against it; sizes the
+                        LM-head workspace */
+  int max_pos;       /* RoPE positions (streaming: stream length); 0 = L */
+  int ffn;           /* FFN width F of the multi-layer denoiser (0 = none);
+                        sizes the FFN workspace */
+} dllm_cache_cfg;
+
+/* Opaque handle: per-layer Q/K/V cache, versions, the token each row was
+   computed from, SWD history and stable flags, RoPE table, device error word
+   and the scratch buffers of the kernels. */
+typedef struct dllm_cache dllm_cache;
+
+/* Allocate and zero a cache for `cfg` on the current device.  Validates the
+   shape (EINVAL / EUNSUPPORTED), allocates with cudaMalloc (ENOMEM).
+   *out receives the handle; free it with dllm_cache_free. */
+dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache** out);
+
+/* Free every buffer of the handle (synchronises the device first). */
+dllm_status dllm_cache_free(dllm_cache* c);
+
+/* Reset for a new generation: versions to "never written", token-at-write
+   to -1, stable flags and SWD history to zero, error word to zero. */
+dllm_status dllm_cache_reset(dllm_cache* c, void* stream);
+
+/* Synchronise `stream`, read and clear the device error word into *err_word
+   (may be NULL).  Returns DLLM_EDEVICE if any bit was set. */
+dllm_status dllm_cache_check(dllm_cache* c, void* stream, uint32_t* err_word);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char* dllm_last_error(void);
+
+/* Fields for dllm_state_copy (deterministic replay of a step in tests). */
+typedef enum {
+  DLLM_FIELD_Q = 0, DLLM_FIELD_K = 1, DLLM_FIELD_V = 2, /* [rows][d] of `layer` */
+  DLLM_FIELD_VERSION = 3,   /* int32 [n_layers][B*L] */
+  DLLM_FIELD_TOK_W = 4,     /* int32 [B*L]: token each row was computed from */
+  DLLM_FIELD_STABLE = 5,    /* uint8 [B*L] */
+  DLLM_FIELD_HIST_TOK = 6,  /* int32 [B][block_len][swd_K] ring of top-1 ids */
+  DLLM_FIELD_HIST_P = 7,    /* float [B][block_len][swd_K] ring of top-1 probs */
+  DLLM_FIELD_HIST_N = 8     /* int32 [B][block_len] records pushed this block */
+} dllm_field;
+
+/* Blocking copy of one state field between the handle and HOST memory
+   `host` (to_device = 1: host -> handle).  `bytes` must equal the field's
+   size; *bytes_out (may be NULL) receives it. */
+dllm_status dllm_state_copy(dllm_cache* c, int field, int layer, void* host, size_t bytes,
+                            int to_device, size_t* bytes_out);
+
+/* --- the step --------------------------------------------------------- */
+
+/* Full refresh set of a block's first step ("LaCache", Inference workflow):
+   every row b * L + pos of every sequence, ascending.
+   rows_dev: int32 [B*L] device; n_rows_dev: int32 [1] device. */
+dllm_status refresh_all(dllm_cache* c, int q_start, int32_t* rows_dev, int32_t* n_rows_dev,
+                        void* stream);
+
+/* Rows rows_dev[0 .. *n_rows_dev) (device count, never read by the host)
+   are recomputed for layer `layer` ("LaCache", LSM: RoPECache holds the
+   normalised hidden state after QKV projection and RoPE):
+     x_i = x_dev[i] if x_dev != NULL (compact [n][d] layer input, i.e. the
+           hidden state of row rows_dev[i]), else embed_dev[tok_dev[row]];
+     [q k v] = RMSNorm(x_i) . W_qkv^T, W_qkv [3d][d] row-major;
+     q, k rotated by RoPE at the row's position; stored into the layer's
+     Q/K/V cache row; version[layer][row] = t; for layer 0 the token is
+     recorded as the row's token-at-write.
+   Dense mode: row = b * L + pos.  Streaming mode: row = stream index n,
+   tok_dev is the stream, the entry goes to ring slot n (n < S) or
+   S + (n - S) mod W, and RoPE uses position n.
+   rows_dev == NULL means every dense row 0 .. B*L-1 (n_rows_dev ignored).
+   At most B*L rows (dense) or S + W rows (streaming) per call; a larger
+   device count sets DLLM_ERR_ROW and only the first rows are refreshed.
+   A caller-given x_dev must hold that many rows (only the first *n_rows
+   are used).  Out-of-range rows / tokens set the error word and are
+   skipped. */
+dllm_status kv_refresh(dllm_cache* c, int layer, const void* x_dev, const int32_t* tok_dev,
+                       const void* embed_dev, const void* w_qkv_dev, const int32_t* rows_dev,
+                       const int32_t* n_rows_dev, int t, void* stream);
+
+/* Bidirectional attention of cached queries over the cached sequence
+   ("LaCache", Problem statement: a block's tokens are updated together over
+   the full context; no causal mask):
+   dense: queries are positions [q_start, q_start + q_len) of every sequence,
+     keys/values all L positions; out_dev [B][q_len][d].
+   streaming: the query is stream token n = q_start (q_len = 1), keys/values
+     the min(n + 1, S + W) entries the ring holds; out_dev [1][d].
+   Split-KV with an online-softmax merge; scratch owned by the handle. */
+dllm_status block_attn(dllm_cache* c, int layer, int q_start, int q_len, void* out_dev,
+                       void* stream);
+
+/* Same attention for an explicit query row list (multi-layer denoiser: the
+   rows that pass through the layers): queries q_rows_dev[0 .. *n_q_dev),
+   out_dev [n][d] compact. */
+dllm_status block_attn_rows(dllm_cache* c, int layer, const int32_t* q_rows_dev,
+                            const int32_t* n_q_dev, void* out_dev, void* stream);
+
+/* Residual stream after attention: h_dev[i] = x_i + o_dev[i] . W_o^T for
+   i < M (M = B * q_len rows, row i = sequence i / q_len, position
+   q_start + i % q_len), W_o [d][d] row-major.  x_i = x_res_dev[i] if given,
+   else embed_dev[tok_dev[b * L + q_start + i % q_len]].
+   m_dev (device int32, may be NULL) overrides M with a device count (at most
+   B*L; o_dev, x_res_dev and h_dev then hold B*L rows). */
+dllm_status attn_out(dllm_cache* c, const void* o_dev, const void* w_o_dev, const void* x_res_dev,
+                     const int32_t* tok_dev, const void* embed_dev, int q_start, int q_len,
+                     const int32_t* m_dev, void* h_dev, void* stream);
+
+/* FFN of the multi-layer denoiser: out_dev[i] = h_i + W2 . GELU(W1 .
+   RMSNorm(h_i)), W1 [F][d], W2 [d][F], exact (erf) GELU, the GELU output
+   stored in the cache dtype.  M rows, or *m_dev if m_dev != NULL. */
+dllm_status ffn_gelu(dllm_cache* c, const void* h_dev, const void* w1_dev, const void* w2_dev,
+                     int F, int M, const int32_t* m_dev, void* out_dev, void* stream);
+
+/* Fused LM head + confidence for M rows of h_dev [M][d]:
+     logits = RMSNorm(h_i) . W_lm^T (W_lm [V][d]), logit[mask_id] excluded;
+     argmax_dev[i] = first index of the largest logit,
+     p_top1_dev[i] = its softmax probability,
+     entropy_dev[i] = -sum p ln p.
+   ("Stable Window Decoding" 3.1; "I/O-aware KV cache ..." 3.1.)
+   Per vocab tile the epilogue reduces (max, argmax, sum e^(l-max),
+   sum e^(l-max)(l-max)) from the accumulator; a merge kernel combines the
+   tiles.  Logits are never written.  M <= B * block_len. */
+dllm_status lmhead_conf(dllm_cache* c, const void* h_dev, const void* w_lm_dev, int M, int V,
+                        int d, int mask_id, int32_t* argmax_dev, float* p_top1_dev,
+                        float* entropy_dev, void* stream);
+
+/* SWD update of the active block [q_start, q_start + block_len) of every
+   sequence, then the refresh set of step t + 1 ("Stable Window Decoding"
+   3.1-3.3, 4.2; "Diffusion latent cache with time anchors" 2.3):
+     every active position not yet stable pushes (argmax, p_top1) into its
+     ring of the last K; it becomes stable when K records exist, all K ids are
+     equal and their mean (fp32, oldest to newest, / K) > tau; a position that
+     becomes stable commits tok = argmax; stable positions are skipped.
+     last_step != 0: every still-unstable active position commits its argmax,
+     the history is cleared, and the next refresh set is the full set of the
+     next block (as refresh_all(q_start + block_len)).
+     Otherwise rows = dilate_R(unstable active) U {tok != token-at-write}
+       U {(t + 1) - version > expiry} (U the active block if refresh_active),
+     ascending b * L + pos.
+   argmax_dev / p_top1_dev: [B * block_len] device; tok_dev [B][L] device,
+   updated in place; rows_dev [B * L], n_rows_dev [1] device outputs. */
+dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p_top1_dev,
+                        int32_t* tok_dev, int q_start, int t, int last_step, int32_t* rows_dev,
+                        int32_t* n_rows_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DLLM_KV_H */

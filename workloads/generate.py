@@ -102,3 +102,25 @@ def model(w):
         m["w1"] = [w_ffn1(w, l) for l in range(w.n_layers)]
         m["w2"] = [w_ffn2(w, l) for l in range(w.n_layers)]
     return m
+
+
+# --- seeded inputs for single-kernel tests --------------------------------------------
+def normal(seed, shape, std=1.0, dtype="bf16"):
+    """N(0, std^2) array in the storage encoding of ``dtype`` (bf16 bits or fp32)."""
+    x = np.random.default_rng([seed, 99]).standard_normal(size=shape, dtype=np.float32) * np.float32(std)
+    return f32_to_bf16_bits(x) if dtype == "bf16" else x
+
+
+def integers(seed, lo, hi, shape):
+    """Uniform int32 in [lo, hi)."""
+    return np.random.default_rng([seed, 98]).integers(lo, hi, size=shape).astype(np.int32)
+
+
+def uniform(seed, lo, hi, shape):
+    """Uniform fp32 in [lo, hi)."""
+    return np.random.default_rng([seed, 97]).uniform(lo, hi, size=shape).astype(np.float32)
+
+
+def choice(seed, n, k):
+    """k distinct sorted ints from [0, n)."""
+    return np.sort(np.random.default_rng([seed, 96]).choice(n, size=k, replace=False)).astype(np.int32)
