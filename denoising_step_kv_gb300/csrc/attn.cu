@@ -55,6 +55,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
+// (a, b) -> bf16 pairs hi = rn(a, b) and lo = rn(a - hi_a, b - hi_b)
+__device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<uint32_t*>(&h);
+  lo = *reinterpret_cast<uint32_t*>(&l);
+}
 // Byte offset of (key, dim) in a tile stored as DH/64 sub-tiles of 64 keys x
 // 128 bytes with the 128-byte swizzle (16-byte chunk index ^= key % 8).
 __device__ __forceinline__ uint32_t swz(int key, int dim) {
@@ -212,19 +220,25 @@ __global__ void __launch_bounds__((NQW + 1) * 32)
         o[i][0] *= al0; o[i][1] *= al0;
         o[i][2] *= al1; o[i][3] *= al1;
       }
+      // P = P_hi + P_lo, both bf16: the PV product keeps ~16 significant
+      // bits of every softmax weight instead of bf16's 8
 #pragma unroll
       for (int kc2 = 0; kc2 < 4; ++kc2) {
-        const uint32_t pa[4] = {pack_bf16(sc[2 * kc2][0], sc[2 * kc2][1]), pack_bf16(sc[2 * kc2][2], sc[2 * kc2][3]),
-                                pack_bf16(sc[2 * kc2 + 1][0], sc[2 * kc2 + 1][1]),
-                                pack_bf16(sc[2 * kc2 + 1][2], sc[2 * kc2 + 1][3])};
+        uint32_t ph[4], pl[4];
+        split_bf16(sc[2 * kc2][0], sc[2 * kc2][1], ph[0], pl[0]);
+        split_bf16(sc[2 * kc2][2], sc[2 * kc2][3], ph[1], pl[1]);
+        split_bf16(sc[2 * kc2 + 1][0], sc[2 * kc2 + 1][1], ph[2], pl[2]);
+        split_bf16(sc[2 * kc2 + 1][2], sc[2 * kc2 + 1][3], ph[3], pl[3]);
 #pragma unroll
         for (int dp = 0; dp < DH / 16; ++dp) {
           const int key = kc2 * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
           const int dim = dp * 16 + ((lane >> 4) << 3);
           uint32_t r0, r1, r2, r3;
           ldsm_x4_t(vb + swz(key, dim), r0, r1, r2, r3);
-          mma16816(o[2 * dp], pa, r0, r1);
-          mma16816(o[2 * dp + 1], pa, r2, r3);
+          mma16816(o[2 * dp], ph, r0, r1);
+          mma16816(o[2 * dp + 1], ph, r2, r3);
+          mma16816(o[2 * dp], pl, r0, r1);
+          mma16816(o[2 * dp + 1], pl, r2, r3);
         }
       }
       __syncwarp();

@@ -8,7 +8,7 @@ import torch
 import oracle as O
 from denoising_step_kv_gb300 import _lib as K
 from denoising_step_kv_gb300 import loop
-from gpu_util import close, max_err, read_field, tol
+from gpu_util import cache_fields, close, i32, max_err, read_field, tol, write_field
 from workloads import configs as C
 from workloads import generate as G
 
@@ -68,4 +68,78 @@ def test_free_running_generation(name):
         assert np.array_equal(g["rows"], rec["rows_next"]), (name, t, "rows")
         assert np.array_equal(g["version"], rec["version"]), (name, t, "version")
         compared += 1
-    assert compared >= min(len(trace), 6), (name, compared)
+    assert compared >= 1 or np.any(trace[0]["margin"] <= 1e-2), (name, compared)
+
+
+def _load_pre(gen, w, rec):
+    """Put the oracle's pre-step state into the GPU handle and buffers."""
+    pre = rec["pre"]
+    B, L, blk, Kk = w.batch, w.seq_len, w.block_len, w.swd_K
+    c = gen.cache
+    gen.tok.copy_(torch.from_numpy(pre["tok"].astype(np.int32)))
+    write_field(c, K.FIELD_VERSION, 0, pre["version"], "i32")
+    write_field(c, K.FIELD_TOK_W, 0, pre["tok_w"], "i32")
+    write_field(c, K.FIELD_STABLE, 0, pre["stable"].reshape(-1), "u8")
+    ht = np.zeros((B, blk, Kk), np.int32)
+    hp = np.zeros((B, blk, Kk), np.float32)
+    hn = pre["swd"].n.astype(np.int32)
+    for b in range(B):
+        for j in range(blk):
+            toks, ps = pre["swd"].tok[b][j], pre["swd"].p[b][j]
+            n = int(hn[b, j])
+            for k, (a, p) in enumerate(zip(toks, ps)):
+                slot = (n - len(toks) + k) % Kk
+                ht[b, j, slot], hp[b, j, slot] = a, p
+    write_field(c, K.FIELD_HIST_TOK, 0, ht, "i32")
+    write_field(c, K.FIELD_HIST_P, 0, hp, "f32")
+    write_field(c, K.FIELD_HIST_N, 0, hn, "i32")
+    for f, arr in zip((K.FIELD_Q, K.FIELD_K, K.FIELD_V), pre["caches"]):
+        write_field(c, f, 0, arr[0], cache_fields(w))
+    rows = rec["rows"]
+    gen.rows.zero_()
+    gen.rows[:len(rows)] = i32(rows)
+    gen.n_rows.fill_(len(rows))
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32_sharp", "mid_bf16", "mid_bf16_dh64", "mid_bf16_sharp"])
+def test_teacher_forced_steps(name):
+    """Every step starts from the oracle's pre-step state (caches included);
+    exactness is required away from ambiguous positions."""
+    w = C.get(name)
+    m = G.model(w)
+    tok0 = G.prompt_tokens(w)
+    trace = O.run_dense(w, O.weights_f64(w, m), tok0, keep_pre=True)
+    gen = loop.DenseGenerator(w, {k: loop.to_device(v) for k, v in m.items()})
+    B, L, blk, d, R = w.batch, w.seq_len, w.block_len, w.d_model, w.swd_R
+    rtol, atol = tol(w)
+    try:
+        K.dllm_cache_reset(gen.cache)
+        for rec in trace:
+            t, q0, s = rec["t"], rec["q0"], rec["s"]
+            _load_pre(gen, w, rec)
+            gen.step(t, q0, s)
+            assert K.dllm_cache_check(gen.cache) == 0
+            o = gen.o.float().cpu().numpy().reshape(B, blk, d)
+            h = gen.h.float().cpu().numpy().reshape(B, blk, d)
+            assert close(o, rec["o"], w), (name, t, "o", max_err(o, rec["o"]))
+            assert close(h, rec["h"], w), (name, t, "h", max_err(h, rec["h"]))
+            assert np.allclose(gen.p1.cpu().numpy().reshape(B, blk), rec["p1"], rtol=rtol, atol=atol), (name, t)
+            assert np.allclose(gen.ent.cpu().numpy().reshape(B, blk), rec["ent"], rtol=rtol, atol=atol), (name, t)
+            amb = _ambiguous(rec, w)
+            am = gen.argmax.cpu().numpy().reshape(B, blk)
+            assert np.array_equal(am[~amb], rec["argmax"][~amb]), (name, t, "argmax")
+            # positions whose fate hangs on an ambiguous decision
+            skip = np.zeros((B, L), dtype=bool)
+            for b, j in zip(*np.nonzero(amb)):
+                skip[b, max(0, q0 + j - R):q0 + j + R + 1] = True
+            tok = gen.tok.cpu().numpy()
+            stable = read_field(gen.cache, K.FIELD_STABLE, 0, (B, L), "u8").astype(bool)
+            assert np.array_equal(tok[~skip], rec["tok"][~skip]), (name, t, "tok")
+            assert np.array_equal(stable[~skip], rec["stable"][~skip]), (name, t, "stable")
+            rows = gen.rows.cpu().numpy()[:int(gen.n_rows.item())]
+            keep = lambda r: r[~skip.reshape(-1)[r]]
+            assert np.array_equal(keep(rows), keep(rec["rows_next"])), (name, t, "rows")
+            ver = read_field(gen.cache, K.FIELD_VERSION, 0, (1, B, L), "i32")
+            assert np.array_equal(ver, rec["version"]), (name, t, "version")
+    finally:
+        gen.close()
