@@ -49,7 +49,9 @@ _SIGS = {
     "ffn_gelu": [_VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _VP],
     "lmhead_conf": [_VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP],
     "stab_update": [_VP, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _VP],
+    "dllm_profile_events": [_VP, _I, _VP, _VP],
 }
+PROF_QKV_GEMM, PROF_ATTN, PROF_LM_GEMM = 1, 2, 3
 EXPORTS = list(_SIGS) + ["dllm_last_error"]
 
 _lib = None
@@ -187,3 +189,11 @@ def lmhead_conf(c, h, w_lm, M, V, d, mask_id, argmax, p_top1, entropy, stream=No
 def stab_update(c, argmax, p_top1, tok, q_start, t, last_step, rows, n_rows, stream=None):
     _check("stab_update", lib().stab_update(c, _p(argmax), _p(p_top1), _p(tok), q_start, t,
                                             1 if last_step else 0, _p(rows), _p(n_rows), _s(stream)))
+
+
+def dllm_profile_events(c, kernel, ev_begin, ev_end):
+    """Bracket the next launches of `kernel` with torch.cuda.Event pairs
+    (None, None clears the hook)."""
+    b = None if ev_begin is None else ctypes.c_void_p(ev_begin.cuda_event)
+    e = None if ev_end is None else ctypes.c_void_p(ev_end.cuda_event)
+    _check("dllm_profile_events", lib().dllm_profile_events(c, kernel, b, e))

@@ -59,7 +59,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 void free_all(dllm_cache* c) {
   void* bufs[] = {c->q, c->k, c->v, c->version, c->tok_w, c->stable, c->hist_tok, c->hist_p, c->hist_n, c->words,
-                  c->rope, c->err, c->X, c->rs, c->lm_part, c->lm_rs, c->ffn_buf};
+                  c->rope, c->err, c->ticket, c->X, c->rs, c->lm_part, c->lm_rs, c->ffn_buf};
   for (void* b : bufs)
     if (b) cudaFree(b);
 }
@@ -154,7 +154,7 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
             dalloc(&c->hist_n, static_cast<size_t>(g.batch) * blk * sizeof(int)) &&
             dalloc(&c->words, static_cast<size_t>(g.batch) * c->Lw * sizeof(uint32_t)) &&
             dalloc(&c->rope, static_cast<size_t>(c->max_pos) * (g.head_dim / 2) * sizeof(float2)) &&
-            dalloc(&c->err, sizeof(unsigned)) && dalloc(&c->X, sr * d * c->elem) && dalloc(&c->rs, sr * sizeof(float)) &&
+            dalloc(&c->err, sizeof(unsigned)) && dalloc(&c->ticket, sizeof(unsigned)) && dalloc(&c->X, sr * d * c->elem) && dalloc(&c->rs, sr * sizeof(float)) &&
             dalloc(&c->lm_part, static_cast<size_t>(c->lm_rows_cap) * c->lm_tiles_cap * 16) &&
             dalloc(&c->lm_rs, static_cast<size_t>(c->lm_rows_cap) * sizeof(float)) &&
             dalloc(&c->ffn_buf, sr * static_cast<size_t>(g.ffn) * c->elem);
@@ -186,6 +186,7 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
   cudaMemsetAsync(c->q, 0, nl * rows * d * c->elem, st);
   cudaMemsetAsync(c->k, 0, nl * rows * d * c->elem, st);
   cudaMemsetAsync(c->v, 0, nl * rows * d * c->elem, st);
+  cudaMemsetAsync(c->ticket, 0, sizeof(unsigned), st);
   cudaMemsetAsync(c->hist_tok, 0, static_cast<size_t>(g.batch) * blk * K * sizeof(int), st);
   cudaMemsetAsync(c->hist_p, 0, static_cast<size_t>(g.batch) * blk * K * sizeof(float), st);
   if (launch_reset(c, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess) {
@@ -303,8 +304,11 @@ dllm_status kv_refresh(dllm_cache* c, int layer, const void* x_dev, const int32_
   DLLM_LAUNCH(launch_gather(c, layer, rows_dev, n_rows_dev, n_host, x_dev, tok_dev, embed_dev, t, st),
               "kv_refresh: gather");
   const void* A = x_dev ? x_dev : c->X;
-  DLLM_LAUNCH(gemm_qkv(c, layer, A, c->seq_rows, rows_dev ? n_rows_dev : nullptr, rows_dev, w_qkv_dev, st),
-              "kv_refresh: projection");
+  {
+    ProfScope prof(c, DLLM_PROF_QKV_GEMM, st);
+    DLLM_LAUNCH(gemm_qkv(c, layer, A, c->seq_rows, rows_dev ? n_rows_dev : nullptr, rows_dev, w_qkv_dev, st),
+                "kv_refresh: projection");
+  }
   return DLLM_OK;
 }
 
@@ -319,12 +323,14 @@ dllm_status block_attn(dllm_cache* c, int layer, int q_start, int q_len, void* o
       return fail(DLLM_EINVAL, "block_attn: streaming takes one query 0 <= n < max_pos");
     const int slot = q_start < g.sink ? q_start : g.sink + (q_start - g.sink) % g.window;
     const int kv_len = std::min(q_start + 1, g.sink + g.window);
+    ProfScope prof(c, DLLM_PROF_ATTN, st);
     DLLM_LAUNCH(attn_dense(c, layer, slot, 0, 1, 0, 0, kv_len, 1, out_dev, 0, st), "block_attn");
     return DLLM_OK;
   }
   if (q_start < 0 || q_len < 1 || q_start + q_len > g.seq_len)
     return fail(DLLM_EINVAL, "block_attn: query range outside the sequence");
   if (g.dtype == DLLM_BF16 && q_len > 64) return fail(DLLM_EUNSUPPORTED, "block_attn: q_len > 64");
+  ProfScope prof(c, DLLM_PROF_ATTN, st);
   DLLM_LAUNCH(attn_dense(c, layer, q_start, g.seq_len, q_len, 0, g.seq_len, g.seq_len, g.batch, out_dev, q_len, st),
               "block_attn");
   return DLLM_OK;
@@ -385,7 +391,11 @@ dllm_status lmhead_conf(dllm_cache* c, const void* h_dev, const void* w_lm_dev, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int n_tiles = cdiv(V, 128);
   DLLM_LAUNCH(launch_rownorm(c, h_dev, M, nullptr, d, c->lm_rs, st), "lmhead_conf: norm");
-  DLLM_LAUNCH(gemm_lm(c, h_dev, w_lm_dev, M, V, d, c->lm_rs, mask_id, c->lm_part, n_tiles, st), "lmhead_conf: gemm");
+  {
+    ProfScope prof(c, DLLM_PROF_LM_GEMM, st);
+    DLLM_LAUNCH(gemm_lm(c, h_dev, w_lm_dev, M, V, d, c->lm_rs, mask_id, c->lm_part, n_tiles, st),
+                "lmhead_conf: gemm");
+  }
   DLLM_LAUNCH(launch_lm_merge(c->lm_part, M, n_tiles, argmax_dev, p_top1_dev, entropy_dev, st), "lmhead_conf: merge");
   return DLLM_OK;
 }
@@ -402,6 +412,16 @@ dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p
   DLLM_LAUNCH(launch_stab(c, argmax_dev, p_top1_dev, tok_dev, q_start, t, last_step ? 1 : 0, rows_dev, n_rows_dev,
                           static_cast<cudaStream_t>(stream)),
               "stab_update");
+  return DLLM_OK;
+}
+
+dllm_status dllm_profile_events(dllm_cache* c, int kernel, void* ev_begin, void* ev_end) {
+  DLLM_CHECK_HANDLE(c);
+  if (kernel < DLLM_PROF_QKV_GEMM || kernel > DLLM_PROF_LM_GEMM)
+    return fail(DLLM_EINVAL, "dllm_profile_events: unknown kernel");
+  if (!ev_begin != !ev_end) return fail(DLLM_EINVAL, "dllm_profile_events: give both events or neither");
+  c->prof_begin[kernel] = static_cast<cudaEvent_t>(ev_begin);
+  c->prof_end[kernel] = static_cast<cudaEvent_t>(ev_end);
   return DLLM_OK;
 }
 

@@ -3,11 +3,13 @@
 //
 // bf16: grid (n_split, H, B) launched as clusters of n_split CTAs.  In each
 // CTA a producer warp streams 64-key K and V tiles of its key range with TMA
-// (128-byte swizzle) into a 3-stage mbarrier ring; NQW consumer warps (16
-// queries each) compute S = Q K^T and O += P V with mma.sync m16n8k16 (bf16
-// in, fp32 accumulate) from ldmatrix fragments and keep an online softmax in
-// the log2 domain.  The split partials (m, l, O) are merged across the cluster
-// through distributed shared memory, so no partial ever reaches HBM.
+// (128-byte swizzle) into a 3-stage mbarrier ring; two groups of NQW consumer
+// warps (16 queries per warp) each take one 32-key half of every tile and
+// compute S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in, fp32
+// accumulate) from ldmatrix fragments, keeping an online softmax in the log2
+// domain.  The partials (m, l, O) of both groups of every CTA are merged
+// across the cluster through distributed shared memory, so no partial ever
+// reaches HBM.
 // fp32: one warp per (query, head, sequence), online softmax in fp32.
 #include <algorithm>
 
@@ -29,9 +31,12 @@ struct AttnShape {
   static constexpr int RING = ASTAGES * STAGE;
 };
 
+constexpr int QLD_PAD = 8;   // bf16 padding of a staged Q row (ldmatrix without bank conflicts)
+
 template <int DH, int NQW>
 constexpr size_t attn_smem_bytes() {
-  return 1024 + AttnShape<DH>::RING + 2 * ASTAGES * sizeof(uint64_t) + 16;
+  return 1024 + AttnShape<DH>::RING + 2 * ASTAGES * sizeof(uint64_t) + 16 +
+         static_cast<size_t>(NQW) * 16 * (DH + QLD_PAD) * 2;
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -79,16 +84,32 @@ __device__ __forceinline__ float ld_peer(const float* p, int rank) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
   return v;
 }
-__device__ __forceinline__ uint32_t ld_u32(const bf16* p) { return *reinterpret_cast<const uint32_t*>(p); }
+// PER consecutive floats (16- or 8-byte aligned) from the same offset in the
+// shared memory of cluster CTA `rank`.
+template <int PER>
+__device__ __forceinline__ void ld_peer_vec(const float* p, int rank, float (&v)[PER]) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(p)), "r"(rank));
+  if constexpr (PER == 4) {
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+                 : "r"(ra)
+                 : "memory");
+  } else {
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v[0]), "=f"(v[1]) : "r"(ra) : "memory");
+  }
+}
+
+constexpr int GROUPS = 2;    // consumer warp groups, one per 32-key half of a tile
 
 template <int DH, int NQW>
-__global__ void __launch_bounds__((NQW + 1) * 32)
+__global__ void __launch_bounds__((GROUPS * NQW + 1) * 32, NQW <= 2 ? 2 : 1)
     attn_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const bf16* __restrict__ Q, int ld, int q_row0, int q_seq_stride, int q_len, int kv_row0,
                      int kv_seq_stride, int kv_len, int keys_per_split, float scale_log2, bf16* __restrict__ out,
                      int out_seq_stride, unsigned* err) {
   using S = AttnShape<DH>;
-  constexpr int NT = (NQW + 1) * 32;
+  constexpr int CW = GROUPS * NQW;   // consumer warps; warp CW is the producer
   const int split = blockIdx.x, n_split = gridDim.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -99,11 +120,21 @@ __global__ void __launch_bounds__((NQW + 1) * 32)
   uint64_t* empty = full + ASTAGES;
   int* abort_flag = reinterpret_cast<int*>(empty + ASTAGES);
   volatile int* abort = abort_flag;
+  constexpr int QLD = DH + QLD_PAD;
+  bf16* qs = reinterpret_cast<bf16*>(reinterpret_cast<uint8_t*>(full) + 2 * ASTAGES * sizeof(uint64_t) + 16);
 
+  // stage the queries (16 rows per query warp, zero rows past q_len)
+  for (int e = tid; e < NQW * 16 * (DH / 8); e += (GROUPS * NQW + 1) * 32) {
+    const int r = e / (DH / 8), c = (e % (DH / 8)) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < q_len)
+      v = *reinterpret_cast<const uint4*>(Q + static_cast<size_t>(q_row0 + b * q_seq_stride + r) * ld + h * DH + c);
+    *reinterpret_cast<uint4*>(qs + r * QLD + c) = v;
+  }
   if (tid == 0) {
     for (int s = 0; s < ASTAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NQW);
+      mbar_init(&empty[s], CW);    // every consumer warp releases every stage
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -118,9 +149,10 @@ __global__ void __launch_bounds__((NQW + 1) * 32)
   float o[DH / 8][4];
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
   const int g = lane >> 2, t4 = lane & 3;
-  const int qi0 = warp * 16 + g, qi1 = qi0 + 8;
+  const int grp = warp / NQW, qw = warp % NQW;
+  const int qi0 = qw * 16 + g, qi1 = qi0 + 8;
 
-  if (warp == NQW) {
+  if (warp == CW) {
     if (lane == 0) {
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
@@ -146,18 +178,11 @@ __global__ void __launch_bounds__((NQW + 1) * 32)
   } else {
 #pragma unroll
     for (int i = 0; i < DH / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    // Q fragments (A operand, rows qi0 / qi1) straight from the cache
-    uint32_t qa[DH / 16][4];
-    const bool v0 = qi0 < q_len, v1 = qi1 < q_len;
-    const bf16* q0p = Q + static_cast<size_t>(q_row0 + b * q_seq_stride + (v0 ? qi0 : 0)) * ld + h * DH;
-    const bf16* q1p = Q + static_cast<size_t>(q_row0 + b * q_seq_stride + (v1 ? qi1 : 0)) * ld + h * DH;
-#pragma unroll
-    for (int kc = 0; kc < DH / 16; ++kc) {
-      qa[kc][0] = v0 ? ld_u32(q0p + kc * 16 + 2 * t4) : 0u;
-      qa[kc][1] = v1 ? ld_u32(q1p + kc * 16 + 2 * t4) : 0u;
-      qa[kc][2] = v0 ? ld_u32(q0p + kc * 16 + 8 + 2 * t4) : 0u;
-      qa[kc][3] = v1 ? ld_u32(q1p + kc * 16 + 8 + 2 * t4) : 0u;
-    }
+    // ldmatrix row address of this lane in the warp's staged Q tile
+    const uint32_t qrow = smem_u32(qs + (qw * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * QLD + (lane >> 4) * 8);
+    // every consumer warp takes every tile, in order (so each wait targets the
+    // stage's next phase); group grp covers keys [grp * HK, grp * HK + HK)
+    constexpr int HK = KT / GROUPS, NT = HK / 8;
     for (int it = 0; it < n_tiles; ++it) {
       const int s = it % ASTAGES;
       const uint32_t ph = (it / ASTAGES) & 1;
@@ -166,25 +191,27 @@ __global__ void __launch_bounds__((NQW + 1) * 32)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const uint32_t kb = smem_u32(ring + s * S::STAGE), vb = kb + S::TILE;
-      float sc[8][4];
+      float sc[NT][4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+      for (int i = 0; i < NT; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
 #pragma unroll
       for (int kc = 0; kc < DH / 16; ++kc) {
+        uint32_t qa[4];
+        ldsm_x4(qrow + kc * 32, qa[0], qa[1], qa[2], qa[3]);
 #pragma unroll
-        for (int np = 0; np < 4; ++np) {
-          const int key = np * 16 + ((lane >> 4) << 3) + (lane & 7);
+        for (int np = 0; np < NT / 2; ++np) {
+          const int key = grp * HK + np * 16 + ((lane >> 4) << 3) + (lane & 7);
           const int dim = kc * 16 + (((lane >> 3) & 1) << 3);
           uint32_t r0, r1, r2, r3;
           ldsm_x4(kb + swz(key, dim), r0, r1, r2, r3);
-          mma16816(sc[2 * np], qa[kc], r0, r1);
-          mma16816(sc[2 * np + 1], qa[kc], r2, r3);
+          mma16816(sc[2 * np], qa, r0, r1);
+          mma16816(sc[2 * np + 1], qa, r2, r3);
         }
       }
-      const int key0 = k_begin + it * KT;
+      const int key0 = k_begin + it * KT + grp * HK;
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int kidx = key0 + nt * 8 + 2 * t4 + (c & 1);
@@ -203,7 +230,7 @@ __global__ void __launch_bounds__((NQW + 1) * 32)
       const float al0 = exp2f(mrow[0] - ref0), al1 = exp2f(mrow[1] - ref1);
       float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < NT; ++nt) {
         sc[nt][0] = exp2f(sc[nt][0] - ref0);
         sc[nt][1] = exp2f(sc[nt][1] - ref0);
         sc[nt][2] = exp2f(sc[nt][2] - ref1);
@@ -221,24 +248,26 @@ __global__ void __launch_bounds__((NQW + 1) * 32)
         o[i][2] *= al1; o[i][3] *= al1;
       }
       // P = P_hi + P_lo, both bf16: the PV product keeps ~16 significant
-      // bits of every softmax weight instead of bf16's 8
+      // bits of every softmax weight instead of bf16's 8 (hi pass, then lo
+      // pass, so no accumulator is hit twice back to back)
 #pragma unroll
-      for (int kc2 = 0; kc2 < 4; ++kc2) {
-        uint32_t ph[4], pl[4];
-        split_bf16(sc[2 * kc2][0], sc[2 * kc2][1], ph[0], pl[0]);
-        split_bf16(sc[2 * kc2][2], sc[2 * kc2][3], ph[1], pl[1]);
-        split_bf16(sc[2 * kc2 + 1][0], sc[2 * kc2 + 1][1], ph[2], pl[2]);
-        split_bf16(sc[2 * kc2 + 1][2], sc[2 * kc2 + 1][3], ph[3], pl[3]);
+      for (int kc2 = 0; kc2 < NT / 2; ++kc2) {
+        uint32_t pp[2][4];
+        split_bf16(sc[2 * kc2][0], sc[2 * kc2][1], pp[0][0], pp[1][0]);
+        split_bf16(sc[2 * kc2][2], sc[2 * kc2][3], pp[0][1], pp[1][1]);
+        split_bf16(sc[2 * kc2 + 1][0], sc[2 * kc2 + 1][1], pp[0][2], pp[1][2]);
+        split_bf16(sc[2 * kc2 + 1][2], sc[2 * kc2 + 1][3], pp[0][3], pp[1][3]);
 #pragma unroll
-        for (int dp = 0; dp < DH / 16; ++dp) {
-          const int key = kc2 * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
-          const int dim = dp * 16 + ((lane >> 4) << 3);
-          uint32_t r0, r1, r2, r3;
-          ldsm_x4_t(vb + swz(key, dim), r0, r1, r2, r3);
-          mma16816(o[2 * dp], ph, r0, r1);
-          mma16816(o[2 * dp + 1], ph, r2, r3);
-          mma16816(o[2 * dp], pl, r0, r1);
-          mma16816(o[2 * dp + 1], pl, r2, r3);
+        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+          for (int dp = 0; dp < DH / 16; ++dp) {
+            const int key = grp * HK + kc2 * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
+            const int dim = dp * 16 + ((lane >> 4) << 3);
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_t(vb + swz(key, dim), r0, r1, r2, r3);
+            mma16816(o[2 * dp], pp[part], r0, r1);
+            mma16816(o[2 * dp + 1], pp[part], r2, r3);
+          }
         }
       }
       __syncwarp();
@@ -253,40 +282,67 @@ __global__ void __launch_bounds__((NQW + 1) * 32)
 
   // ---- split merge across the cluster (distributed shared memory)
   __syncthreads();
-  float* po = reinterpret_cast<float*>(ring);      // [NQW*16][DH] unnormalised O
-  float* pml = po + NQW * 16 * DH;                 // [NQW*16][2] (m, l), log2 domain
-  if (warp < NQW) {
+  constexpr int QP = NQW * 16;                     // padded queries per CTA
+  float* po = reinterpret_cast<float*>(ring);      // [GROUPS][QP][DH] unnormalised O
+  float* pml = po + GROUPS * QP * DH;              // [GROUPS][QP][2] (m, l), log2 domain
+  if (warp < CW) {
+    float* pg = po + grp * QP * DH;
+    float* mg = pml + grp * QP * 2;
 #pragma unroll
     for (int dt = 0; dt < DH / 8; ++dt) {
       const int col = dt * 8 + 2 * t4;
-      po[qi0 * DH + col] = o[dt][0];
-      po[qi0 * DH + col + 1] = o[dt][1];
-      po[qi1 * DH + col] = o[dt][2];
-      po[qi1 * DH + col + 1] = o[dt][3];
+      pg[qi0 * DH + col] = o[dt][0];
+      pg[qi0 * DH + col + 1] = o[dt][1];
+      pg[qi1 * DH + col] = o[dt][2];
+      pg[qi1 * DH + col + 1] = o[dt][3];
     }
     if (t4 == 0) {
-      pml[qi0 * 2] = mrow[0];
-      pml[qi0 * 2 + 1] = lrow[0];
-      pml[qi1 * 2] = mrow[1];
-      pml[qi1 * 2 + 1] = lrow[1];
+      mg[qi0 * 2] = mrow[0];
+      mg[qi0 * 2 + 1] = lrow[0];
+      mg[qi1 * 2] = mrow[1];
+      mg[qi1 * 2 + 1] = lrow[1];
     }
   }
   cluster_sync_all();
+  // CTA `split` finishes queries [split * qpc, split * qpc + qpc): one warp per
+  // query; lane p < 2 n_split fetches partial p = (CTA p / 2, group p % 2)'s
+  // (m, l), then every lane gathers its DH/32 output columns from all
+  // partials with vector loads.
+  constexpr int NW = CW + 1, PER = DH / 32;
   const int qpc = cdiv(q_len, n_split);
-  for (int idx = tid; idx < qpc * DH; idx += NT) {
-    const int q = split * qpc + idx / DH, e = idx % DH;
-    if (q >= q_len) continue;
-    float M = -INFINITY;
-    for (int r = 0; r < n_split; ++r) M = fmaxf(M, ld_peer(pml + q * 2, r));
-    float num = 0.f, den = 0.f;
-    for (int r = 0; r < n_split; ++r) {
-      const float m = ld_peer(pml + q * 2, r);
-      if (m == -INFINITY) continue;
-      const float w = exp2f(m - M);
-      den += w * ld_peer(pml + q * 2 + 1, r);
-      num += w * ld_peer(po + q * DH + e, r);
+  const int n_part = GROUPS * n_split;
+  for (int wq = warp; wq < qpc; wq += NW) {
+    const int q = split * qpc + wq;
+    if (q >= q_len) break;
+    float m_r = -INFINITY, l_r = 0.f;
+    if (lane < n_part) {
+      const float* mg = pml + (lane % GROUPS) * QP * 2 + q * 2;
+      m_r = ld_peer(mg, lane / GROUPS);
+      l_r = ld_peer(mg + 1, lane / GROUPS);
     }
-    out[static_cast<size_t>(b * out_seq_stride + q) * ld + h * DH + e] = __float2bfloat16_rn(num / den);
+    float M = m_r;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float wr = (m_r == -INFINITY) ? 0.f : exp2f(m_r - M);
+    float den = wr * l_r;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    float acc[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+    for (int p = 0; p < n_part; ++p) {
+      const float wgt = __shfl_sync(0xffffffffu, wr, p);
+      if (wgt == 0.f) continue;
+      float v[PER];
+      ld_peer_vec<PER>(po + (p % GROUPS) * QP * DH + q * DH + lane * PER, p / GROUPS, v);
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] = fmaf(wgt, v[i], acc[i]);
+    }
+    const float inv = 1.f / den;
+    bf16* op = out + static_cast<size_t>(b * out_seq_stride + q) * ld + h * DH + lane * PER;
+#pragma unroll
+    for (int i = 0; i < PER; i += 2)
+      *reinterpret_cast<__nv_bfloat162*>(op + i) = __floats2bfloat162_rn(acc[i] * inv, acc[i + 1] * inv);
   }
   cluster_sync_all();
 }
@@ -332,22 +388,22 @@ cudaError_t launch_bf16(dllm_cache* c, const CUtensorMap& tk, const CUtensorMap&
                         bf16* out, int out_seq_stride, cudaStream_t st) {
   const int H = c->cfg.n_heads;
   const int tiles = cdiv(kv_len, KT);
-  int n_split = std::min(8, std::max(1, cdiv(3 * c->num_sms, n_seq * H)));
-  n_split = std::min(n_split, tiles);
+  // one wave at two CTAs per SM, every CTA with >= 2 tiles
+  int n_split = std::min(8, std::max(1, (2 * c->num_sms) / (n_seq * H)));
+  n_split = std::max(1, std::min(n_split, tiles / 2));
   const int per = cdiv(tiles, n_split);
   n_split = cdiv(tiles, per);
   const int keys_per_split = per * KT;
   constexpr size_t smem = attn_smem_bytes<DH, NQW>();
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bf16_kernel<DH, NQW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = set_smem(attn_bf16_kernel<DH, NQW>, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_split, H, n_seq);
-  cfg.blockDim = dim3((NQW + 1) * 32);
+  cfg.blockDim = dim3((GROUPS * NQW + 1) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attrs[1];

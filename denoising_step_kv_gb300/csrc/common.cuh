@@ -14,6 +14,17 @@ using bf16 = __nv_bfloat16;
 
 __host__ __device__ __forceinline__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
 
+// Opt a kernel into `bytes` of dynamic shared memory and the largest shared
+// memory carveout, so that two such CTAs can share an SM when they fit.
+template <class F>
+inline cudaError_t set_smem(F* fn, size_t bytes) {
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
+  return e;
+}
+
 // ---------------------------------------------------------------- storage
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }

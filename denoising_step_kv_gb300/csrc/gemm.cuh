@@ -22,7 +22,7 @@ namespace dllm {
 // number of times whatever its row.
 
 namespace tc {
-constexpr int BM = 128, BN = 128, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 128, BK = 64, MAX_STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -30,25 +30,29 @@ constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 
 struct Bars {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t done;
   uint32_t tmem;
   int abort;
 };
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + sizeof(Bars);
+// Persistent kernel: 4 stages (one CTA per SM) for compute-bound shapes, 3
+// stages (two CTAs per SM, twice the weight bytes in flight) for streaming.
+template <int STAGES>
+constexpr size_t smem_bytes() { return 1024 + STAGES * STAGE_BYTES + sizeof(Bars); }
 
 struct TmemLoader {
   uint32_t taddr;
   __device__ __forceinline__ void operator()(int col, float (&v)[32]) const { tmem_ld32(taddr + col, v); }
 };
 
-template <class Epi>
+template <class Epi, int STAGES>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   int M_host, const int* __restrict__ M_dev, int M_cap, int N, int K, Epi epi, unsigned* err) {
+                   int M_host, const int* __restrict__ M_dev, int M_cap, int M_min, int N, int K, Epi epi,
+                   unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -59,7 +63,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = M_dev ? min(*M_dev, M_cap) : M_host;   // never past A's rows
   const int nM = (M + BM - 1) / BM, nN = (N + BN - 1) / BN, nK = (K + BK - 1) / BK;
-  const int tiles = M > 0 ? nM * nN : 0;
+  // M below M_min belongs to the split-K kernel launched beside this one
+  const int tiles = (M > 0 && M >= M_min) ? nM * nN : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -173,6 +178,184 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// Split-K over a cluster of SPLITK CTAs, one output tile per cluster: CTA
+// rank r accumulates k-blocks [r * kpc, (r + 1) * kpc) into its TMEM, copies
+// the fp32 partial tile to its shared memory, and after a cluster barrier
+// finishes rows [r * 128/SPLITK, (r + 1) * 128/SPLITK) by summing the
+// partials of all ranks (in rank order) through distributed shared memory.
+// Used when few output tiles would leave most SMs without weight bytes to
+// stream.  The grid covers M_cap rows; clusters past the device count exit.
+constexpr int SK_STAGES = 3;     // two CTAs per SM
+constexpr int RED_LD = BN + 4;   // padded fp32 row of the partial tile
+struct SkBars {
+  uint64_t full[SK_STAGES];
+  uint64_t empty[SK_STAGES];
+  uint64_t tfull;
+  uint32_t tmem;
+  int abort;
+};
+constexpr size_t SK_SMEM = 1024 + SK_STAGES * STAGE_BYTES + sizeof(SkBars);
+static_assert(BM * RED_LD * 4 <= SK_STAGES * STAGE_BYTES, "partial tile must fit in the stage ring");
+
+struct LocalRowLoader {
+  const float* row;
+  __device__ __forceinline__ void operator()(int col, float (&v)[32]) const {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(row + col + j);
+      v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
+    }
+  }
+};
+
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// A CTA overwrites only its own slice of rows with their sums; no other CTA
+// reads those rows, and each thread reads its element before writing it.
+__device__ __forceinline__ void partial_sum_store(float* dst, float4 v) { *reinterpret_cast<float4*>(dst) = v; }
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+template <class Epi, int SPLITK>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       int M_host, const int* __restrict__ M_dev, int M_cap, int M_max, int N, int K, Epi epi,
+                       unsigned* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + SK_STAGES * A_BYTES;
+  SkBars* bars = reinterpret_cast<SkBars*>(smem + SK_STAGES * STAGE_BYTES);
+  float* red = reinterpret_cast<float*>(smem);      // [BM][RED_LD], after the mainloop
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int M = M_dev ? min(*M_dev, M_cap) : M_host;
+  const int nN = (N + BN - 1) / BN, nK = (K + BK - 1) / BK;
+  const int tile = blockIdx.x / SPLITK;
+  const int rank = static_cast<int>(cluster_rank());
+  const int mb = tile / nN, nb = tile % nN;
+  // the same decision in every CTA of the cluster: skip the tile entirely
+  if (M > M_max || mb * BM >= M) return;
+  const int kpc = (nK + SPLITK - 1) / SPLITK;
+  const int kb0 = rank * kpc, kb1 = min(nK, kb0 + kpc);
+  const bool has_k = kb1 > kb0;   // an empty K range contributes zeros
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SK_STAGES; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->tfull, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&bars->tmem, BN);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  volatile int* abort = &bars->abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      uint32_t issued = 0, par = 0;
+      for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
+        const int stage = i % SK_STAGES;
+        const uint32_t phase = (i / SK_STAGES) & 1u;
+        if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort, err)) break;
+        mbar_expect_tx(&bars->full[stage], STAGE_BYTES);
+        tma_load_2d(sa + stage * A_BYTES, &tmA, kb * BK, mb * BM, &bars->full[stage]);
+        tma_load_2d(sb + stage * B_BYTES, &tmB, kb * BK, nb * BN, &bars->full[stage]);
+        issued |= 1u << stage;
+        par = (par & ~(1u << stage)) | (phase << stage);
+      }
+      if (*abort)
+        for (int s = 0; s < SK_STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait(&bars->full[s], (par >> s) & 1u, nullptr, err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(BM, BN);
+      for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
+        const int stage = i % SK_STAGES;
+        const uint32_t phase = (i / SK_STAGES) & 1u;
+        if (!mbar_wait(&bars->full[stage], phase, abort, err)) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sa + stage * A_BYTES), b0 = smem_u32(sb + stage * B_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          tc_mma_bf16(tmem, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc, (i | k) != 0 ? 1u : 0u);
+        tc_commit(&bars->empty[stage]);
+      }
+      // completes once every MMA above is done (also when none was issued)
+      tc_commit(&bars->tfull);
+    }
+  } else {
+    // partial accumulator -> shared memory (all MMAs done: the ring is free)
+    const int q = warp & 3;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(&bars->tfull, 0, abort, err) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    tc_fence_after();
+    const int r = q * 32 + lane;
+    float v[32];
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v);
+      float* dst = red + r * RED_LD + c * 32;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(dst + j) = (ok && has_k) ? make_float4(v[j], v[j + 1], v[j + 2], v[j + 3])
+                                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  tc_fence_before();
+  cluster_barrier();
+  // rows [rank * RPC, (rank + 1) * RPC) of the tile: every thread sums float4
+  // column groups over the cluster's partials (rank order) into this CTA's own
+  // copy of those rows, which no other CTA reads
+  constexpr int RPC = BM / SPLITK, G4 = BN / 4;
+  const int row0 = rank * RPC;
+  for (int e = threadIdx.x; e < RPC * G4; e += THREADS) {
+    const int r = row0 + e / G4, c = (e % G4) * 4;
+    const uint32_t la = smem_u32(red + r * RED_LD + c);
+    float4 part[SPLITK];            // all remote loads in flight, then sum in rank order
+#pragma unroll
+    for (int p = 0; p < SPLITK; ++p) {
+      uint32_t ra;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(p));
+      asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(part[p].x), "=f"(part[p].y), "=f"(part[p].z), "=f"(part[p].w)
+                   : "r"(ra)
+                   : "memory");
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int p = 0; p < SPLITK; ++p) {
+      acc.x += part[p].x; acc.y += part[p].y; acc.z += part[p].z; acc.w += part[p].w;
+    }
+    partial_sum_store(red + r * RED_LD + c, acc);
+  }
+  __syncthreads();
+  if (threadIdx.x < RPC) {
+    const int r = row0 + threadIdx.x;
+    LocalRowLoader ld{red + r * RED_LD};
+    epi.run(mb * BM + r, nb * BN, M, N, ld);
+  }
+  cluster_barrier();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, BN);
   }
 }
 }  // namespace tc

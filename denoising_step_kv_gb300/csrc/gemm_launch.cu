@@ -9,6 +9,61 @@ namespace dllm {
 namespace {
 
 
+// Rows at or below which a projection streams its weights (split-K path).
+constexpr int SMALL_M = 512;
+
+template <class Epi, int STAGES>
+cudaError_t launch_persistent(dllm_cache* c, const CUtensorMap& ta, const CUtensorMap& tb, int a_rows, int M_host,
+                              const int* M_dev, int M_min, int N, int K, const Epi& epi, cudaStream_t st) {
+  constexpr size_t smem = tc::smem_bytes<STAGES>();
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(tc::gemm_tc_kernel<Epi, STAGES>, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int m_rows = M_dev ? a_rows : M_host;
+  const int tiles = cdiv(m_rows, tc::BM) * cdiv(N, tc::BN);
+  const int per_sm = STAGES <= 3 ? 2 : 1;
+  const int grid = std::max(1, std::min(tiles, per_sm * c->num_sms));
+  tc::gemm_tc_kernel<Epi, STAGES><<<grid, tc::THREADS, smem, st>>>(ta, tb, M_host, M_dev, a_rows, M_min, N, K, epi,
+                                                                   c->err);
+  return cudaGetLastError();
+}
+
+template <class Epi, int S>
+cudaError_t launch_splitk(dllm_cache* c, const CUtensorMap& ta, const CUtensorMap& tb, int a_rows, int M_host,
+                          const int* M_dev, int M_max, int N, int K, const Epi& epi, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(tc::gemm_splitk_kernel<Epi, S>, tc::SK_SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int m_rows = std::min(M_dev ? a_rows : M_host, M_max);
+  const int tiles = cdiv(m_rows, tc::BM) * cdiv(N, tc::BN);
+  if (tiles <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles * S);
+  cfg.blockDim = dim3(tc::THREADS);
+  cfg.dynamicSmemBytes = tc::SK_SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = S;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc::gemm_splitk_kernel<Epi, S>, ta, tb, M_host, M_dev, a_rows, M_max, N, K, epi,
+                            c->err);
+}
+
+// bf16 D = A . B^T with epilogue `epi`.  M is M_host, or the device count
+// M_dev (at most a_rows).  Small M streams the weights: a split-K cluster
+// kernel spreads them over enough CTAs to fill the GPU.  Large M is
+// tensor-bound: the persistent kernel.  With a device count both are
+// launched and each one skips the other's range.
 template <class Epi>
 cudaError_t run_tc(dllm_cache* c, const void* A, int a_rows, int M_host, const int* M_dev, const void* B, int N,
                    int K, const Epi& epi, cudaStream_t st) {
@@ -17,19 +72,28 @@ cudaError_t run_tc(dllm_cache* c, const void* A, int a_rows, int M_host, const i
   if (!make_tmap_2d(&ta, A, K, a_rows, static_cast<uint64_t>(K) * 2, tc::BK, tc::BM, true) ||
       !make_tmap_2d(&tb, B, K, N, static_cast<uint64_t>(K) * 2, tc::BK, tc::BN, true))
     return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(tc::gemm_tc_kernel<Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(tc::SMEM_BYTES));
+  const int nN = cdiv(N, tc::BN);
+  const int small_rows = std::min(M_dev ? a_rows : M_host, SMALL_M);
+  const int small_tiles = cdiv(small_rows, tc::BM) * nN;
+  const bool want_small = M_dev ? true : (M_host <= SMALL_M && small_tiles < c->num_sms);
+  const bool want_large = M_dev ? a_rows > SMALL_M : !want_small;
+  cudaError_t e = cudaSuccess;
+  if (want_small) {
+    const int ratio = cdiv(c->num_sms, std::max(1, small_tiles));
+    if (M_dev) e = launch_splitk<Epi, 2>(c, ta, tb, a_rows, M_host, M_dev, SMALL_M, N, K, epi, st);
+    else if (ratio >= 8) e = launch_splitk<Epi, 8>(c, ta, tb, a_rows, M_host, M_dev, SMALL_M, N, K, epi, st);
+    else if (ratio >= 4) e = launch_splitk<Epi, 4>(c, ta, tb, a_rows, M_host, M_dev, SMALL_M, N, K, epi, st);
+    else if (ratio >= 2) e = launch_splitk<Epi, 2>(c, ta, tb, a_rows, M_host, M_dev, SMALL_M, N, K, epi, st);
+    else e = launch_persistent<Epi, 3>(c, ta, tb, a_rows, M_host, M_dev, 0, N, K, epi, st);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
-  const int m_rows = M_dev ? a_rows : M_host;
-  const int tiles = cdiv(m_rows, tc::BM) * cdiv(N, tc::BN);
-  const int grid = std::max(1, std::min(tiles, c->num_sms));
-  tc::gemm_tc_kernel<Epi><<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ta, tb, M_host, M_dev, a_rows, N, K, epi,
-                                                                    c->err);
-  return cudaGetLastError();
+  if (want_large) {
+    const int M_min = M_dev ? SMALL_M + 1 : 0;
+    const int m_rows = M_dev ? a_rows : M_host;
+    if (m_rows <= 256) return launch_persistent<Epi, 3>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
+    return launch_persistent<Epi, 4>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
+  }
+  return e;
 }
 
 template <int NCH, class Epi>

@@ -31,6 +31,7 @@ struct dllm_cache {
   uint32_t* words = nullptr;// [B][Lw] refresh flags
   float2* rope = nullptr;   // [max_pos][head_dim/2]
   unsigned* err = nullptr;  // device error word
+  unsigned* ticket = nullptr; // arrival counter of the SWD kernel's blocks
   // scratch
   void* X = nullptr;        // gathered layer inputs [seq_rows][d]
   float* rs = nullptr;      // RMS scales [seq_rows]
@@ -39,11 +40,36 @@ struct dllm_cache {
   int lm_rows_cap = 0, lm_tiles_cap = 0;
   void* ffn_buf = nullptr;  // [seq_rows][ffn]
   int ffn_cap = 0;
+  // measurement hook: events bracketing a kernel (index = dllm_prof_kernel)
+  cudaEvent_t prof_begin[4] = {nullptr, nullptr, nullptr, nullptr};
+  cudaEvent_t prof_end[4] = {nullptr, nullptr, nullptr, nullptr};
 };
 
 namespace dllm {
 
 void set_error(const std::string& msg);
+
+// Record the measurement hook's events around one launch.  Under stream
+// capture a plain event record only orders streams; the external flag makes
+// it an event-record node that the graph timestamps on every replay.
+inline void record_event(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(st, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, st);
+}
+struct ProfScope {
+  cudaEvent_t end;
+  cudaStream_t st;
+  ProfScope(dllm_cache* c, int k, cudaStream_t s) : end(c->prof_end[k]), st(s) {
+    if (c->prof_begin[k]) record_event(c->prof_begin[k], st);
+  }
+  ~ProfScope() {
+    if (end) record_event(end, st);
+  }
+};
 
 // tensor maps (driver entry point resolved once)
 bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,

@@ -65,14 +65,20 @@ __global__ void __launch_bounds__(256) gather_kernel(const int* __restrict__ row
     }
     src = embed + static_cast<size_t>(token) * d;
   }
-  constexpr int VN = Vec<T>::N;
+  constexpr int VN = Vec<T>::N, U = 8;     // U vectors per lane in flight
   float ss = 0.f;
-  for (int c = lane * VN; c < d; c += 32 * VN) {
-    float v[VN];
-    load_row(src + c, v, VN);
+  for (int c0 = lane * VN; c0 < d; c0 += 32 * VN * U) {
+    float v[U][VN];
 #pragma unroll
-    for (int j = 0; j < VN; ++j) ss = fmaf(v[j], v[j], ss);
-    if (!x) store_row(X + static_cast<size_t>(i) * d + c, v, VN);
+    for (int u = 0; u < U; ++u)
+      if (c0 + u * 32 * VN < d) load_row(src + c0 + u * 32 * VN, v[u], VN);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (c0 + u * 32 * VN >= d) break;
+#pragma unroll
+      for (int j = 0; j < VN; ++j) ss = fmaf(v[u][j], v[u][j], ss);
+      if (!x) store_row(X + static_cast<size_t>(i) * d + c0 + u * 32 * VN, v[u], VN);
+    }
   }
   ss = warp_sum(ss);
   if (lane == 0) {
@@ -91,29 +97,38 @@ __global__ void __launch_bounds__(256) rownorm_kernel(const T* __restrict__ h, i
   const int i = blockIdx.x * 8 + warp;
   const int M = M_dev ? *M_dev : M_host;
   if (i >= M) return;
-  constexpr int VN = Vec<T>::N;
+  constexpr int VN = Vec<T>::N, U = 8;
+  const T* row = h + static_cast<size_t>(i) * d;
   float ss = 0.f;
-  for (int c = lane * VN; c < d; c += 32 * VN) {
-    float v[VN];
-    load_row(h + static_cast<size_t>(i) * d + c, v, VN);
+  for (int c0 = lane * VN; c0 < d; c0 += 32 * VN * U) {
+    float v[U][VN];
 #pragma unroll
-    for (int j = 0; j < VN; ++j) ss = fmaf(v[j], v[j], ss);
+    for (int u = 0; u < U; ++u)
+      if (c0 + u * 32 * VN < d) load_row(row + c0 + u * 32 * VN, v[u], VN);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (c0 + u * 32 * VN >= d) break;
+#pragma unroll
+      for (int j = 0; j < VN; ++j) ss = fmaf(v[u][j], v[u][j], ss);
+    }
   }
   ss = warp_sum(ss);
   if (lane == 0) rs[i] = rsqrtf(ss / static_cast<float>(d) + eps);
 }
 
-// One warp per row: merge the per-tile statistics (tiles in increasing vocab
-// order per lane, then across lanes with the lower index winning ties).
-__global__ void __launch_bounds__(256) lm_merge_kernel(const LMPart* __restrict__ part, int M, int n_tiles,
-                                                       int* __restrict__ argmax, float* __restrict__ p1,
-                                                       float* __restrict__ ent) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i = blockIdx.x * 8 + warp;
+// One 128-thread CTA per row: every thread merges its tiles in increasing
+// vocab order, then a tree merge across threads (ties: lower index wins).
+constexpr int MERGE_THREADS = 128;
+__global__ void __launch_bounds__(MERGE_THREADS) lm_merge_kernel(const LMPart* __restrict__ part, int M,
+                                                                 int n_tiles, int* __restrict__ argmax,
+                                                                 float* __restrict__ p1, float* __restrict__ ent) {
+  __shared__ float s_m[MERGE_THREADS / 32], s_s[MERGE_THREADS / 32], s_a[MERGE_THREADS / 32];
+  __shared__ int s_i[MERGE_THREADS / 32];
+  const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (i >= M) return;
   float m = -INFINITY, s = 0.f, a = 0.f;
   int idx = 0x7fffffff;
-  for (int tt = lane; tt < n_tiles; tt += 32) {
+  for (int tt = tid; tt < n_tiles; tt += MERGE_THREADS) {
     const LMPart p = part[static_cast<size_t>(i) * n_tiles + tt];
     lm_merge(m, s, a, idx, p.m, p.s, p.a, p.idx);
   }
@@ -126,11 +141,19 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const LMPart* __restrict_
     lm_merge(m, s, a, idx, m2, s2, a2, i2);
   }
   if (lane == 0) {
+    s_m[warp] = m; s_s[warp] = s; s_a[warp] = a; s_i[warp] = idx;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < MERGE_THREADS / 32; ++w) lm_merge(m, s, a, idx, s_m[w], s_s[w], s_a[w], s_i[w]);
     argmax[i] = idx;
     p1[i] = 1.f / s;
     ent[i] = logf(s) - a / s;
   }
 }
+
+__device__ void compact_words(const uint32_t* __restrict__ words, int nw, int L, int Lw, int* __restrict__ rows,
+                              int* __restrict__ n_rows);
 
 // Stable-Window-Decoding update of the active block of sequence blockIdx.x,
 // then one flag bit per position for the next step's refresh set.
@@ -139,8 +162,9 @@ __global__ void __launch_bounds__(1024) swd_kernel(
     uint8_t* __restrict__ stable, int* __restrict__ hist_tok, float* __restrict__ hist_p, int* __restrict__ hist_n,
     const int* __restrict__ tok_w, const int* __restrict__ version, uint32_t* __restrict__ words, int L, int Lw,
     int seq_rows, int n_layers, int blk, int K, float tau, int R, int q0, int t, int last, int expiry,
-    int refresh_active) {
+    int refresh_active, unsigned* __restrict__ ticket, int* __restrict__ rows, int* __restrict__ n_rows) {
   __shared__ uint8_t s_unst[64];
+  __shared__ int s_last;
   const int b = blockIdx.x;
   const int nac = min(blk, L - q0);
   if (threadIdx.x < nac) {
@@ -198,23 +222,25 @@ __global__ void __launch_bounds__(1024) swd_kernel(
     const int w = (base + (threadIdx.x & ~31)) >> 5;
     if ((threadIdx.x & 31) == 0 && w < Lw) words[b * Lw + w] = word;
   }
-}
-
-__global__ void __launch_bounds__(1024) fill_words_kernel(uint32_t* words, int B, int L, int Lw) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < B * Lw; i += gridDim.x * blockDim.x) {
-    const int w = i % Lw;
-    const int valid = min(32, L - w * 32);
-    words[i] = valid >= 32 ? 0xffffffffu : ((1u << valid) - 1u);
-  }
+  // the last sequence block to finish compacts every sequence's flags
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  compact_words(words, gridDim.x * Lw, L, Lw, rows, n_rows);
+  if (threadIdx.x == 0) *ticket = 0u;
 }
 
 // Compact the flag words into ascending row ids b * L + pos (block-wide
 // exclusive scan of the per-word popcounts, one word per thread per pass).
-__global__ void __launch_bounds__(1024) compact_kernel(const uint32_t* __restrict__ words, int nw, int L, int Lw,
-                                                       int* __restrict__ rows, int* __restrict__ n_rows) {
+// Run by one whole block of blockDim.x (a multiple of 32, <= 1024) threads.
+__device__ void compact_words(const uint32_t* __restrict__ words, int nw, int L, int Lw, int* __restrict__ rows,
+                              int* __restrict__ n_rows) {
   __shared__ int s_warp[32];
   __shared__ int s_base;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   if (tid == 0) s_base = 0;
   __syncthreads();
   for (int base = 0; base < nw; base += blockDim.x) {
@@ -230,7 +256,7 @@ __global__ void __launch_bounds__(1024) compact_kernel(const uint32_t* __restric
     if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-      int x = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
+      int x = lane < nwarps ? s_warp[lane] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -249,10 +275,16 @@ __global__ void __launch_bounds__(1024) compact_kernel(const uint32_t* __restric
       }
     }
     __syncthreads();
-    if (tid == 0) s_base += s_warp[(blockDim.x >> 5) - 1];
+    if (tid == 0) s_base += s_warp[nwarps - 1];
     __syncthreads();
   }
   if (tid == 0) *n_rows = s_base;
+}
+
+// Every refresh row 0 .. n-1 (the block-start full refresh).
+__global__ void __launch_bounds__(256) all_rows_kernel(int* __restrict__ rows, int* __restrict__ n_rows, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) rows[i] = i;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *n_rows = n;
 }
 
 __global__ void reset_kernel(int* version, int n_version, int* tok_w, uint8_t* stable, int n_rows, int* hist_n,
@@ -304,7 +336,7 @@ cudaError_t launch_rownorm(dllm_cache* c, const void* h, int M, const int* M_dev
 cudaError_t launch_lm_merge(const void* part, int M, int n_tiles, int* argmax, float* p1, float* ent,
                             cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
-  lm_merge_kernel<<<cdiv(M, 8), 256, 0, st>>>(static_cast<const LMPart*>(part), M, n_tiles, argmax, p1, ent);
+  lm_merge_kernel<<<M, MERGE_THREADS, 0, st>>>(static_cast<const LMPart*>(part), M, n_tiles, argmax, p1, ent);
   return cudaGetLastError();
 }
 
@@ -313,21 +345,15 @@ cudaError_t launch_stab(dllm_cache* c, const int* argmax, const float* p1, int* 
   const dllm_cache_cfg& g = c->cfg;
   swd_kernel<<<g.batch, 1024, 0, st>>>(argmax, p1, tok, c->stable, c->hist_tok, c->hist_p, c->hist_n, c->tok_w,
                                        c->version, c->words, g.seq_len, c->Lw, c->seq_rows, g.n_layers, g.block_len,
-                                       g.swd_K, g.swd_tau, g.swd_R, q_start, t, last, g.expiry, g.refresh_active);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  compact_kernel<<<1, 1024, 0, st>>>(c->words, g.batch * c->Lw, g.seq_len, c->Lw, rows, n_rows);
+                                       g.swd_K, g.swd_tau, g.swd_R, q_start, t, last, g.expiry, g.refresh_active,
+                                       c->ticket, rows, n_rows);
   return cudaGetLastError();
 }
 
 cudaError_t launch_refresh_all(dllm_cache* c, int q_start, int* rows, int* n_rows, cudaStream_t st) {
   (void)q_start;
-  const dllm_cache_cfg& g = c->cfg;
-  fill_words_kernel<<<std::min(cdiv(g.batch * c->Lw, 1024), 64), 1024, 0, st>>>(c->words, g.batch, g.seq_len,
-                                                                                   c->Lw);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  compact_kernel<<<1, 1024, 0, st>>>(c->words, g.batch * c->Lw, g.seq_len, c->Lw, rows, n_rows);
+  const int n = c->seq_rows;
+  all_rows_kernel<<<std::min(cdiv(n, 256), 256), 256, 0, st>>>(rows, n_rows, n);
   return cudaGetLastError();
 }
 

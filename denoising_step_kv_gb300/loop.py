@@ -49,7 +49,7 @@ class DenseGenerator:
         self.ent = torch.zeros(B * blk, dtype=torch.float32, device=device)
         self.tok_in = torch.zeros(B, L, **i32)
         self.graph = None
-        self.lm_events = None
+        self.prof = {}          # kernel id -> [(begin, end) per step] of the last run
 
     def close(self):
         if self.cache is not None:
@@ -63,7 +63,7 @@ class DenseGenerator:
             pass
 
     # -- one step -------------------------------------------------------------
-    def step(self, t, q0, s, stream=None, lm_event_pair=None):
+    def step(self, t, q0, s, stream=None):
         w, c, W = self.w, self.cache, self.W
         blk = w.block_len
         if t == 0:
@@ -71,12 +71,8 @@ class DenseGenerator:
         K.kv_refresh(c, 0, None, self.tok, W["embed"], W["w_qkv"][0], self.rows, self.n_rows, t, stream)
         K.block_attn(c, 0, q0, blk, self.o, stream)
         K.attn_out(c, self.o, W["w_o"][0], None, self.tok, W["embed"], q0, blk, None, self.h, stream)
-        if lm_event_pair is not None:
-            lm_event_pair[0].record(stream)
         K.lmhead_conf(c, self.h, W["w_lm"], w.batch * blk, w.vocab, w.d_model, w.mask_id, self.argmax,
                       self.p1, self.ent, stream)
-        if lm_event_pair is not None:
-            lm_event_pair[1].record(stream)
         K.stab_update(c, self.argmax, self.p1, self.tok, q0, t, s == w.steps_per_block - 1, self.rows,
                       self.n_rows, stream)
 
@@ -90,22 +86,38 @@ class DenseGenerator:
                 yield t, q0, s
                 t += 1
 
-    def run(self, stream=None, on_step=None, n_steps=None, time_lm=False):
-        """Reset the cache, copy tok_in -> tok and run the step loop."""
+    def make_prof_events(self, kernels):
+        """One (begin, end) CUDA event pair per step for each kernel id
+        (_lib.PROF_*), created now (a torch event exists once recorded)."""
+        ev = {k: [] for k in kernels}
+        for k in kernels:
+            for _ in range(self.w.n_steps):
+                pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                pair[0].record()
+                pair[1].record()
+                ev[k].append(pair)
+        return ev
+
+    def run(self, stream=None, on_step=None, n_steps=None, prof=None):
+        """Reset the cache, copy tok_in -> tok and run the step loop.
+
+        prof: {kernel id: [(begin, end) per step]} from make_prof_events; the
+        library records the pair around that kernel's launch in every step.
+        """
         K.dllm_cache_reset(self.cache, stream)
         self.tok.copy_(self.tok_in)
-        events = []
+        prof = prof or {}
+        self.prof = prof
         for t, q0, s in self.schedule():
             if n_steps is not None and t >= n_steps:
                 break
-            pair = None
-            if time_lm:
-                pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                events.append(pair)
-            self.step(t, q0, s, stream, pair)
+            for k, pairs in prof.items():
+                K.dllm_profile_events(self.cache, k, *pairs[t])
+            self.step(t, q0, s, stream)
             if on_step is not None:
                 on_step(t, q0, s)
-        self.lm_events = events if time_lm else None
+        for k in prof:
+            K.dllm_profile_events(self.cache, k, None, None)
         return self.tok
 
     def generate(self, tok0):
@@ -113,13 +125,13 @@ class DenseGenerator:
         return self.run()
 
     # -- CUDA graph of a whole generation -------------------------------------------
-    def capture(self, time_lm=False):
+    def capture(self, prof=None):
         """Capture run() as one CUDA graph (after one eager warm-up run)."""
         self.run()
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.run(time_lm=time_lm)
+            self.run(prof=prof)
         self.graph = g
         return g
 
@@ -127,6 +139,6 @@ class DenseGenerator:
         self.graph.replay()
         return self.tok
 
-    def lm_times_ms(self):
-        """Durations of the LM-head launches recorded by the last run/replay."""
-        return [a.elapsed_time(b) for a, b in (self.lm_events or [])]
+    def kernel_times_ms(self, kernel):
+        """Per-step durations of `kernel` recorded by the last run/replay."""
+        return [a.elapsed_time(b) for a, b in self.prof.get(kernel, [])]

@@ -238,6 +238,22 @@ dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p
                         int32_t* tok_dev, int q_start, int t, int last_step, int32_t* rows_dev,
                         int32_t* n_rows_dev, void* stream);
 
+/* --- measurement ------------------------------------------------------ */
+
+/* Kernels that dllm_profile_events can bracket. */
+typedef enum {
+  DLLM_PROF_QKV_GEMM = 1,   /* projection GEMM of kv_refresh */
+  DLLM_PROF_ATTN = 2,       /* attention kernel of block_attn */
+  DLLM_PROF_LM_GEMM = 3     /* fused LM-head GEMM of lmhead_conf */
+} dllm_prof_kernel;
+
+/* Record the CUDA events ev_begin / ev_end (cudaEvent_t, created by the
+   caller with timing enabled) on the call's stream immediately before and
+   after the next launches of `kernel`, until changed; NULL events clear the
+   hook.  Under stream capture the records become graph nodes, so a captured
+   generation can time one kernel per step. */
+dllm_status dllm_profile_events(dllm_cache* c, int kernel, void* ev_begin, void* ev_end);
+
 #ifdef __cplusplus
 }
 #endif

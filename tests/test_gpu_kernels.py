@@ -133,6 +133,36 @@ def test_block_attn(name, q_start, q_len):
         K.dllm_cache_free(c)
 
 
+@pytest.mark.parametrize("name,q_len", [("8b_shaped", 32), ("bf16_d2048", 32), ("bf16_d2048", 16)])
+def test_block_attn_many_tiles(name, q_len):
+    """Full-size key ranges: every CTA streams many K/V tiles through the
+    3-stage ring (8B-shaped: one split, 64 tiles per CTA), so every stage
+    barrier goes through many phases; sampled (sequence, head) pairs are
+    checked against the oracle."""
+    w = C.get(name)
+    B, L, H, dh, d = w.batch, w.seq_len, w.n_heads, w.head_dim, w.d_model
+    q0 = w.n_prompt
+    c = _fresh(w)
+    try:
+        fields = {}
+        for f, seed in ((K.FIELD_Q, 51), (K.FIELD_K, 52), (K.FIELD_V, 53)):
+            a = G.normal(seed, (B * L, d), 0.5, "bf16")
+            fields[f] = O.bf16_bits_to_f64(a).reshape(B, L, H, dh)
+            K.dllm_state_copy(c, f, 0, torch.from_numpy(a.view(np.int16)), True)
+        out = torch.zeros(B * q_len, d, dtype=torch.bfloat16, device="cuda")
+        for _ in range(3):                       # repeated launches reuse the same code path
+            K.block_attn(c, 0, q0, q_len, out, None)
+        assert K.dllm_cache_check(c) == 0
+        got = out.float().cpu().numpy().astype(np.float64).reshape(B, q_len, H, dh)
+        for b, h in [(0, 0), (B - 1, H - 1), (B // 2, H // 3)]:
+            want = O.round_store(O.attention(fields[K.FIELD_Q][b, q0:q0 + q_len, h:h + 1],
+                                             fields[K.FIELD_K][b, :, h:h + 1], fields[K.FIELD_V][b, :, h:h + 1]),
+                                 "bf16")
+            assert close(got[b, :, h:h + 1], want, w), (name, b, h, max_err(got[b, :, h:h + 1], want))
+    finally:
+        K.dllm_cache_free(c)
+
+
 @pytest.mark.parametrize("name", CFGS)
 def test_attn_out(name):
     w, m, W, D = _setup(name)
