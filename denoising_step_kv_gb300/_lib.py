@@ -50,6 +50,7 @@ _SIGS = {
     "lmhead_conf": [_VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP],
     "stab_update": [_VP, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _VP],
     "dllm_profile_events": [_VP, _I, _VP, _VP],
+    "lmhead_conf_noalloc": [_VP, _VP, _I, _I, _I, _I, _I, ctypes.c_float, _VP, _VP, _VP, _VP],
 }
 PROF_QKV_GEMM, PROF_ATTN, PROF_LM_GEMM = 1, 2, 3
 EXPORTS = list(_SIGS) + ["dllm_last_error"]
@@ -197,3 +198,11 @@ def dllm_profile_events(c, kernel, ev_begin, ev_end):
     b = None if ev_begin is None else ctypes.c_void_p(ev_begin.cuda_event)
     e = None if ev_end is None else ctypes.c_void_p(ev_end.cuda_event)
     _check("dllm_profile_events", lib().dllm_profile_events(c, kernel, b, e))
+
+
+def lmhead_conf_noalloc(h, w_lm, M, V, d, dtype, mask_id, rms_eps, argmax, p_top1, entropy, stream=None):
+    """lmhead_conf without a handle or any device allocation (scratch in a
+    static device array; M <= 256, V <= 131072; overlapping calls race)."""
+    _check("lmhead_conf_noalloc", lib().lmhead_conf_noalloc(_p(h), _p(w_lm), M, V, d, dtype, mask_id,
+                                                            ctypes.c_float(rms_eps), _p(argmax), _p(p_top1),
+                                                            _p(entropy), _s(stream)))

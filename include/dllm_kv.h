@@ -238,6 +238,28 @@ dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p
                         int32_t* tok_dev, int q_start, int t, int last_step, int32_t* rows_dev,
                         int32_t* n_rows_dev, void* stream);
 
+/* --- without device allocation ---------------------------------------- */
+
+/* lmhead_conf for callers that cannot call cudaMalloc: the same computation
+   and kernels, no handle, and no allocation by the library.  (This entry
+   point has no counterpart in the pages; it serves hosts such as a serving
+   engine whose memory planner owns every device byte, code that must not hit
+   cudaMalloc's implicit device synchronisation, or a caller that has no
+   dllm_cache handle.)  The caller passes inputs and outputs as for
+   lmhead_conf, plus the storage dtype and the RMSNorm epsilon.
+   Scratch lives in one static device array of 4 MiB + 1.25 KiB that every GPU
+   which loads the library keeps until the process exits; it bounds a call to
+   M <= 256 rows and V <= 131072 (larger sizes return DLLM_EINVAL).  The first
+   call on a device resolves the array's address on that device (the device
+   must be current); make that first call before any stream capture.  Every
+   call shares the array and leaves its contents behind: calls whose kernels
+   overlap on the GPU (different streams, or several host threads) race.
+   The call allocates nothing: no cudaMalloc, cudaFree, or allocating library
+   routine. */
+dllm_status lmhead_conf_noalloc(const void* h_dev, const void* w_lm_dev, int M, int V, int d, int dtype,
+                                int mask_id, float rms_eps, int32_t* argmax_dev, float* p_top1_dev,
+                                float* entropy_dev, void* stream);
+
 /* --- measurement ------------------------------------------------------ */
 
 /* Kernels that dllm_profile_events can bracket. */
