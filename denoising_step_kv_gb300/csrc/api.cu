@@ -140,14 +140,18 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
   c->max_pos = g.max_pos > 0 ? g.max_pos : g.seq_len;
   if (!streaming && c->max_pos < g.seq_len) c->max_pos = g.seq_len;
   c->Lw = streaming ? 1 : cdiv(g.seq_len, 32);
-  const size_t nl = g.n_layers, rows = c->rows, sr = c->seq_rows;
+  const size_t nl = g.n_layers, sr = c->seq_rows;
+  c->kv.H = g.n_heads;
+  c->kv.Lp = cdiv(streaming ? g.sink + g.window : g.seq_len, 64) * 64;
+  c->kv.row_bytes = static_cast<int>(g.head_dim * c->elem);
+  c->kv_layer_bytes = c->kv.layer_bytes(streaming ? 1 : g.batch);
   const int blk = streaming ? 1 : g.block_len;
   const int K = streaming ? 1 : g.swd_K;
   c->lm_rows_cap = g.batch * blk;
   c->lm_tiles_cap = cdiv(g.vocab, 128);
   c->ffn_cap = g.ffn;
-  bool ok = dalloc(&c->q, nl * rows * d * c->elem) && dalloc(&c->k, nl * rows * d * c->elem) &&
-            dalloc(&c->v, nl * rows * d * c->elem) && dalloc(&c->version, nl * sr * sizeof(int)) &&
+  bool ok = dalloc(&c->q, nl * c->kv_layer_bytes) && dalloc(&c->k, nl * c->kv_layer_bytes) &&
+            dalloc(&c->v, nl * c->kv_layer_bytes) && dalloc(&c->version, nl * sr * sizeof(int)) &&
             dalloc(&c->tok_w, sr * sizeof(int)) && dalloc(&c->stable, sr) &&
             dalloc(&c->hist_tok, static_cast<size_t>(g.batch) * blk * K * sizeof(int)) &&
             dalloc(&c->hist_p, static_cast<size_t>(g.batch) * blk * K * sizeof(float)) &&
@@ -183,9 +187,9 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
     }
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaMemsetAsync(c->q, 0, nl * rows * d * c->elem, st);
-  cudaMemsetAsync(c->k, 0, nl * rows * d * c->elem, st);
-  cudaMemsetAsync(c->v, 0, nl * rows * d * c->elem, st);
+  cudaMemsetAsync(c->q, 0, nl * c->kv_layer_bytes, st);
+  cudaMemsetAsync(c->k, 0, nl * c->kv_layer_bytes, st);
+  cudaMemsetAsync(c->v, 0, nl * c->kv_layer_bytes, st);
   cudaMemsetAsync(c->ticket, 0, sizeof(unsigned), st);
   cudaMemsetAsync(c->hist_tok, 0, static_cast<size_t>(g.batch) * blk * K * sizeof(int), st);
   cudaMemsetAsync(c->hist_p, 0, static_cast<size_t>(g.batch) * blk * K * sizeof(float), st);
@@ -243,7 +247,7 @@ dllm_status dllm_state_copy(dllm_cache* c, int field, int layer, void* host, siz
   const size_t blk = g.sink > 0 ? 1 : g.block_len, K = g.sink > 0 ? 1 : g.swd_K;
   if (field <= DLLM_FIELD_V) {
     if (layer < 0 || layer >= g.n_layers) return fail(DLLM_EINVAL, "dllm_state_copy: bad layer");
-    size = static_cast<size_t>(c->rows) * c->d * c->elem;
+    size = c->kv_layer_bytes;
     void* base = field == DLLM_FIELD_Q ? c->q : field == DLLM_FIELD_K ? c->k : c->v;
     ptr = static_cast<char*>(base) + static_cast<size_t>(layer) * size;
   } else if (field == DLLM_FIELD_VERSION) {
@@ -324,15 +328,14 @@ dllm_status block_attn(dllm_cache* c, int layer, int q_start, int q_len, void* o
     const int slot = q_start < g.sink ? q_start : g.sink + (q_start - g.sink) % g.window;
     const int kv_len = std::min(q_start + 1, g.sink + g.window);
     ProfScope prof(c, DLLM_PROF_ATTN, st);
-    DLLM_LAUNCH(attn_dense(c, layer, slot, 0, 1, 0, 0, kv_len, 1, out_dev, 0, st), "block_attn");
+    DLLM_LAUNCH(attn_dense(c, layer, slot, 1, kv_len, 1, out_dev, st), "block_attn");
     return DLLM_OK;
   }
   if (q_start < 0 || q_len < 1 || q_start + q_len > g.seq_len)
     return fail(DLLM_EINVAL, "block_attn: query range outside the sequence");
   if (g.dtype == DLLM_BF16 && q_len > 64) return fail(DLLM_EUNSUPPORTED, "block_attn: q_len > 64");
   ProfScope prof(c, DLLM_PROF_ATTN, st);
-  DLLM_LAUNCH(attn_dense(c, layer, q_start, g.seq_len, q_len, 0, g.seq_len, g.seq_len, g.batch, out_dev, q_len, st),
-              "block_attn");
+  DLLM_LAUNCH(attn_dense(c, layer, q_start, q_len, g.seq_len, g.batch, out_dev, st), "block_attn");
   return DLLM_OK;
 }
 

@@ -10,41 +10,59 @@ __host__ __device__ __forceinline__ int ring_slot(int n, int S, int W) {
   return n < S ? n : S + (n - S) % W;
 }
 
+// Store 32 consecutive values of head h, dims [e0, e0 + 32), of cache row
+// (b, pos) into the tiled KV layout (see KvLayout), 16 bytes at a time.
+template <typename T>
+__device__ __forceinline__ void store_kv32(uint8_t* base, const KvLayout& kv, int b, int h, int pos, int e0,
+                                           const float* v) {
+  constexpr int PER = 16 / sizeof(T);          // values per 16-byte chunk
+  const int c0 = e0 / PER;
+#pragma unroll
+  for (int q = 0; q < 32 / PER; ++q) store_row(reinterpret_cast<T*>(base + kv.chunk_off(b, h, pos, c0 + q)),
+                                               v + q * PER, PER);
+}
+
 // QKV projection: accumulator row m (compact refresh index) times the row's
 // RMSNorm scale, RoPE on the q and k parts (rotate-half pairs (i, i + DH/2)
-// with a cos/sin table), stored into the layer's Q/K/V cache row.
+// with a cos/sin table), stored into the layer's tiled Q/K/V cache.
 template <typename T, int DH, int NCH>
 struct EpiQKV {
   const int* rows;      // compact index -> row id (nullptr: identity)
   const float* rs;      // per compact row: RMS scale (< 0: skip the row)
-  T* q;
-  T* k;
-  T* v;                 // layer base pointers, rows of d elements
+  uint8_t* q;
+  uint8_t* k;
+  uint8_t* v;           // layer base pointers (tiled layout)
+  KvLayout kv;
   const float2* rope;   // [max_pos][DH/2] (cos, sin)
   int L, d, rows_cap, streaming, S, W, max_pos;
 
   template <class LD>
   __device__ __forceinline__ void run(int m, int n0, int M, int N, const LD& ld) const {
     bool ok = m < M;
-    int dst = 0, pos = 0;
+    int b = 0, slot = 0, pos = 0;
     float sc = 0.f;
     if (ok) {
       const int row = rows ? rows[m] : m;
       if (streaming) {
         ok = row >= 0 && row < max_pos;
         pos = row;
-        dst = ok ? ring_slot(row, S, W) : 0;
+        slot = ok ? ring_slot(row, S, W) : 0;
       } else {
         ok = row >= 0 && row < rows_cap;
-        pos = ok ? row % L : 0;
-        dst = row;
+        b = ok ? row / L : 0;
+        pos = ok ? row - b * L : 0;
+        slot = pos;
       }
       sc = ok ? rs[m] : -1.f;
       ok = ok && sc > 0.f;
     }
-    const int part = n0 / d, c0 = n0 - part * d;
-    T* out = (part == 0 ? q : part == 1 ? k : v) + static_cast<size_t>(dst) * d + c0;
-    float a[32], b[32];
+    const int part = n0 / d, c0 = n0 - part * d;   // c0: first column inside q, k or v
+    uint8_t* base = part == 0 ? q : part == 1 ? k : v;
+    auto put = [&](int col, const float* vals) {    // col: column inside the part
+      const int h = col / DH;
+      store_kv32<T>(base, kv, b, h, slot, col - h * DH, vals);
+    };
+    float a[32], bb[32];
     if (part == 2) {
 #pragma unroll 1
       for (int c = 0; c < NCH; ++c) {
@@ -52,7 +70,7 @@ struct EpiQKV {
         if (ok) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) a[j] *= sc;
-          store_row(out + c * 32, a, 32);
+          put(c0 + c * 32, a);
         }
       }
     } else if (DH >= 64) {
@@ -64,18 +82,18 @@ struct EpiQKV {
         for (int hc = 0; hc < HALF_CH; ++hc) {
           const int c1 = hd * DH + hc * 32, c2 = c1 + DH / 2;
           ld(c1, a);
-          ld(c2, b);
+          ld(c2, bb);
           if (ok) {
             const float2* rp = rope + static_cast<size_t>(pos) * (DH / 2) + hc * 32;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const float2 cs = rp[j];
-              const float x1 = a[j] * sc, x2 = b[j] * sc;
+              const float x1 = a[j] * sc, x2 = bb[j] * sc;
               a[j] = x1 * cs.x - x2 * cs.y;
-              b[j] = x2 * cs.x + x1 * cs.y;
+              bb[j] = x2 * cs.x + x1 * cs.y;
             }
-            store_row(out + c1, a, 32);
-            store_row(out + c2, b, 32);
+            put(c0 + c1, a);
+            put(c0 + c2, bb);
           }
         }
       }
@@ -92,7 +110,7 @@ struct EpiQKV {
             a[j] = x1 * cs.x - x2 * cs.y;
             a[j + 16] = x2 * cs.x + x1 * cs.y;
           }
-          store_row(out + c * 32, a, 32);
+          put(c0 + c * 32, a);
         }
       }
     }

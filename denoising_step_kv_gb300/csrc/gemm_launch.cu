@@ -110,12 +110,13 @@ cudaError_t run_simt(const void* A, int m_cap, int M_host, const int* M_dev, con
 template <typename T, int DH, int NCH>
 EpiQKV<T, DH, NCH> make_qkv(dllm_cache* c, int layer, const int* rows) {
   EpiQKV<T, DH, NCH> e;
-  const size_t off = static_cast<size_t>(layer) * c->rows * c->d;
+  const size_t off = static_cast<size_t>(layer) * c->kv_layer_bytes;
   e.rows = rows;
   e.rs = c->rs;
-  e.q = static_cast<T*>(c->q) + off;
-  e.k = static_cast<T*>(c->k) + off;
-  e.v = static_cast<T*>(c->v) + off;
+  e.q = static_cast<uint8_t*>(c->q) + off;
+  e.k = static_cast<uint8_t*>(c->k) + off;
+  e.v = static_cast<uint8_t*>(c->v) + off;
+  e.kv = c->kv;
   e.rope = c->rope;
   e.L = c->cfg.seq_len;
   e.d = c->d;

@@ -7,6 +7,7 @@
 #include <string>
 
 #include "dllm_kv.h"
+#include "kv_layout.h"
 
 struct dllm_cache {
   dllm_cache_cfg cfg;
@@ -18,8 +19,10 @@ struct dllm_cache {
   int max_pos = 0;      // RoPE table rows
   int Lw = 0;           // 32-position words per sequence
   size_t elem = 2;      // bytes per element of the cache dtype
+  dllm::KvLayout kv{};  // tiled layout of every layer's Q/K/V cache
+  size_t kv_layer_bytes = 0;
   // state
-  void* q = nullptr;    // [n_layers][rows][d]
+  void* q = nullptr;    // [n_layers] x tiled layout (kv), B (or 1) sequences
   void* k = nullptr;
   void* v = nullptr;
   int* version = nullptr;   // [n_layers][seq_rows]
@@ -90,8 +93,10 @@ cudaError_t gemm_lm(dllm_cache* c, const void* A, const void* W, int M, int V, i
 int lm_tile_cols(const dllm_cache* c);
 
 // attn.cu ------------------------------------------------------------------
-cudaError_t attn_dense(dllm_cache* c, int layer, int q_row0, int q_seq_stride, int q_len, int kv_row0,
-                       int kv_seq_stride, int kv_len, int n_seq, void* out, int out_seq_stride,
+// Queries: positions [q_pos0, q_pos0 + q_len) (ring slot in streaming mode)
+// of each of n_seq sequences; keys/values: positions [0, kv_len).  out:
+// [n_seq][q_len][d] in the cache dtype.
+cudaError_t attn_dense(dllm_cache* c, int layer, int q_pos0, int q_len, int kv_len, int n_seq, void* out,
                        cudaStream_t st);
 
 // misc.cu ------------------------------------------------------------------

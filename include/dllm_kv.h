@@ -128,7 +128,13 @@ const char* dllm_last_error(void);
 
 /* Fields for dllm_state_copy (deterministic replay of a step in tests). */
 typedef enum {
-  DLLM_FIELD_Q = 0, DLLM_FIELD_K = 1, DLLM_FIELD_V = 2, /* [rows][d] of `layer` */
+  /* Q, K, V of `layer`, in the cache's tiled layout: for each sequence b
+     (1 in streaming mode) and head h, Lp rows (L, or S + W, rounded up to
+     64) in tiles of 64; a tile holds head_dim * elem / 128 sub-tiles of 64
+     rows x 128 bytes, and the 16-byte chunk c of row r of a sub-tile sits at
+     chunk c ^ (r % 8).  Row pos of (b, h) is in tile (b * H + h) * Lp/64 +
+     pos / 64.  Streaming mode indexes rows by ring slot. */
+  DLLM_FIELD_Q = 0, DLLM_FIELD_K = 1, DLLM_FIELD_V = 2,
   DLLM_FIELD_VERSION = 3,   /* int32 [n_layers][B*L] */
   DLLM_FIELD_TOK_W = 4,     /* int32 [B*L]: token each row was computed from */
   DLLM_FIELD_STABLE = 5,    /* uint8 [B*L] */

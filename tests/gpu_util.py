@@ -59,3 +59,46 @@ def close(a, b, w):
 
 def max_err(a, b):
     return float(np.max(np.abs(np.asarray(a) - np.asarray(b)))) if np.size(a) else 0.0
+
+
+def kv_index(B, L, H, DH, esize):
+    """Element index, in a layer's tiled Q/K/V cache, of the logical element
+    [b, pos, h, e] (the layout include/dllm_kv.h documents for the Q/K/V
+    fields: per (sequence, head) block of Lp rows, 64-row tiles of 128-byte
+    sub-tile rows, 16-byte chunk c of row r at chunk c ^ (r % 8))."""
+    Lp = -(-L // 64) * 64
+    row_bytes = DH * esize
+    b = np.arange(B)[:, None, None, None]
+    pos = np.arange(L)[None, :, None, None]
+    h = np.arange(H)[None, None, :, None]
+    e = np.arange(DH)[None, None, None, :]
+    per = 16 // esize
+    chunk, within = e // per, (e % per) * esize
+    sub, cc, r = chunk >> 3, chunk & 7, pos & 63
+    off = ((b * H + h) * Lp + (pos & ~63)) * row_bytes + sub * 8192 + r * 128 + ((cc ^ (r & 7)) << 4) + within
+    return off // esize
+
+
+def _kv_shape(w):
+    if w.streaming:
+        return 1, w.sink + w.window
+    return w.batch, w.seq_len
+
+
+def read_kv(c, field, layer, w):
+    """Q/K/V cache of a layer as [B, L, H, dh] float64 (streaming: [1, S+W, H, dh])."""
+    B, L = _kv_shape(w)
+    esize = 2 if w.dtype == "bf16" else 4
+    n = K.state_size(c, field, layer) // esize
+    flat = read_field(c, field, layer, (n,), "bf16" if w.dtype == "bf16" else "f32")
+    return flat[kv_index(B, L, w.n_heads, w.head_dim, esize)]
+
+
+def write_kv(c, field, layer, w, arr):
+    """Write a [B, L, H, dh] array into a layer's tiled Q/K/V cache (zeros elsewhere)."""
+    B, L = _kv_shape(w)
+    esize = 2 if w.dtype == "bf16" else 4
+    n = K.state_size(c, field, layer) // esize
+    flat = np.zeros(n, dtype=np.float64)
+    flat[kv_index(B, L, w.n_heads, w.head_dim, esize)] = np.asarray(arr, dtype=np.float64).reshape(B, L, w.n_heads, w.head_dim)
+    write_field(c, field, layer, flat, "bf16" if w.dtype == "bf16" else "f32")

@@ -11,7 +11,7 @@ import torch
 import oracle as O
 from denoising_step_kv_gb300 import _lib as K
 from denoising_step_kv_gb300.loop import to_device
-from gpu_util import cache_fields, close, i32, max_err, read_field, tol, write_field
+from gpu_util import cache_fields, close, i32, max_err, read_field, read_kv, tol, write_field, write_kv
 from workloads import configs as C
 from workloads import generate as G
 
@@ -42,7 +42,7 @@ def test_kv_refresh_all_rows(name):
         assert K.dllm_cache_check(c) == 0
         q, k, v = O.project_qkv(W["embed"][tok.reshape(-1)], W["w_qkv"][0], np.tile(np.arange(L), B), H, w.dtype)
         for f, want in ((K.FIELD_Q, q), (K.FIELD_K, k), (K.FIELD_V, v)):
-            got = read_field(c, f, 0, (B * L, H, dh), cache_fields(w))
+            got = read_kv(c, f, 0, w).reshape(B * L, H, dh)
             assert close(got, want, w), (name, f, max_err(got, want))
         ver = read_field(c, K.FIELD_VERSION, 0, (B * L,), "i32")
         tw = read_field(c, K.FIELD_TOK_W, 0, (B * L,), "i32")
@@ -67,7 +67,7 @@ def test_kv_refresh_ragged_rows(name):
         q, k, v = O.project_qkv(W["embed"][tok.reshape(-1)[rows]], W["w_qkv"][0], rows % L, H, w.dtype)
         untouched = np.setdiff1d(np.arange(B * L), rows)
         for f, want in ((K.FIELD_Q, q), (K.FIELD_K, k), (K.FIELD_V, v)):
-            got = read_field(c, f, 0, (B * L, H, dh), cache_fields(w))
+            got = read_kv(c, f, 0, w).reshape(B * L, H, dh)
             assert close(got[rows], want, w), (name, f, max_err(got[rows], want))
             assert np.all(got[untouched] == 0)
         ver = read_field(c, K.FIELD_VERSION, 0, (B * L,), "i32")
@@ -120,7 +120,7 @@ def test_block_attn(name, q_start, q_len):
     c = _fresh(w)
     try:
         for f, a in ((K.FIELD_Q, q), (K.FIELD_K, k), (K.FIELD_V, v)):
-            write_field(c, f, 0, a, st)
+            write_kv(c, f, 0, w, a)
         dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
         out = torch.zeros(B * q_len, d, dtype=dt, device="cuda")
         K.block_attn(c, 0, q_start, q_len, out, None)
@@ -148,7 +148,7 @@ def test_block_attn_many_tiles(name, q_len):
         for f, seed in ((K.FIELD_Q, 51), (K.FIELD_K, 52), (K.FIELD_V, 53)):
             a = G.normal(seed, (B * L, d), 0.5, "bf16")
             fields[f] = O.bf16_bits_to_f64(a).reshape(B, L, H, dh)
-            K.dllm_state_copy(c, f, 0, torch.from_numpy(a.view(np.int16)), True)
+            write_kv(c, f, 0, w, fields[f])
         out = torch.zeros(B * q_len, d, dtype=torch.bfloat16, device="cuda")
         for _ in range(3):                       # repeated launches reuse the same code path
             K.block_attn(c, 0, q0, q_len, out, None)

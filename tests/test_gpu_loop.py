@@ -8,7 +8,7 @@ import torch
 import oracle as O
 from denoising_step_kv_gb300 import _lib as K
 from denoising_step_kv_gb300 import loop
-from gpu_util import cache_fields, close, i32, max_err, read_field, tol, write_field
+from gpu_util import cache_fields, close, i32, max_err, read_field, tol, write_field, write_kv
 from workloads import configs as C
 from workloads import generate as G
 
@@ -94,7 +94,7 @@ def _load_pre(gen, w, rec):
     write_field(c, K.FIELD_HIST_P, 0, hp, "f32")
     write_field(c, K.FIELD_HIST_N, 0, hn, "i32")
     for f, arr in zip((K.FIELD_Q, K.FIELD_K, K.FIELD_V), pre["caches"]):
-        write_field(c, f, 0, arr[0], cache_fields(w))
+        write_kv(c, f, 0, w, arr[0])
     rows = rec["rows"]
     gen.rows.zero_()
     gen.rows[:len(rows)] = i32(rows)
