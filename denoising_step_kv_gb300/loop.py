@@ -142,3 +142,61 @@ class DenseGenerator:
     def kernel_times_ms(self, kernel):
         """Per-step durations of `kernel` recorded by the last run/replay."""
         return [a.elapsed_time(b) for a, b in self.prof.get(kernel, [])]
+
+
+class StreamGenerator:
+    """Attention-sink stream through one layer (batch 1).
+
+    Token n's step: its Q/K/V row joins the sink + rolling cache at ring slot
+    n (sinks keep slots 0..S-1, later tokens cycle through the W rolling
+    slots, RoPE at the absolute stream index), then its query attends over
+    the min(n + 1, S + W) entries the cache holds.  O_n lands in out[n].
+    """
+
+    def __init__(self, w, weights, device="cuda"):
+        assert w.streaming and w.n_layers == 1
+        self.w = w
+        self.W = weights
+        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        self.cache = K.dllm_cache_init(K.make_cfg(w))
+        i32 = dict(dtype=torch.int32, device=device)
+        self.pos = torch.arange(w.stream_len, **i32)      # row list: token n is row n
+        self.one = torch.ones(1, **i32)
+        self.tok = torch.zeros(w.stream_len, **i32)
+        self.out = torch.zeros(w.stream_len, w.d_model, dtype=dt, device=device)
+        self.graph = None
+
+    def close(self):
+        if self.cache is not None:
+            K.dllm_cache_free(self.cache)
+            self.cache = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def step(self, n, stream=None):
+        c, W = self.cache, self.W
+        K.kv_refresh(c, 0, None, self.tok, W["embed"], W["w_qkv"][0], self.pos[n:n + 1], self.one, n, stream)
+        K.block_attn(c, 0, n, 1, self.out[n:n + 1], stream)
+
+    def run(self, n_tokens=None, stream=None):
+        K.dllm_cache_reset(self.cache, stream)
+        for n in range(self.w.stream_len if n_tokens is None else n_tokens):
+            self.step(n, stream)
+        return self.out
+
+    def capture(self, n_tokens=None):
+        self.run(n_tokens)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run(n_tokens)
+        self.graph = g
+        return g
+
+    def replay(self):
+        self.graph.replay()
+        return self.out

@@ -114,6 +114,12 @@ MID_SINK = Workload(
     block_len=1, steps_per_block=1, d_model=256, n_heads=2, head_dim=128,
     vocab=1000, seed=13, sink=4, window=92, stream_len=300)
 
+# fp32 stream through a ring of 2 sinks + 13 rolling slots (wraps 3 times)
+TINY_SINK_F32 = Workload(
+    name="tiny_sink_f32", dtype="f32", n_layers=1, batch=1, seq_len=0, n_prompt=0,
+    block_len=1, steps_per_block=1, d_model=64, n_heads=2, head_dim=32,
+    vocab=256, seed=15, sink=2, window=13, stream_len=50)
+
 MID_MULTI = Workload(
     name="mid_multi", dtype="bf16", n_layers=3, batch=2, seq_len=160, n_prompt=128,
     block_len=16, steps_per_block=6, d_model=256, n_heads=4, head_dim=64,
@@ -121,7 +127,7 @@ MID_MULTI = Workload(
     refresh_active=1)
 
 ALL = dict(NAMED)
-for _w in (MID_BF16, MID_BF16_DH64, TINY_FP32_SHARP, MID_BF16_SHARP, MID_SINK, MID_MULTI):
+for _w in (MID_BF16, MID_BF16_DH64, TINY_FP32_SHARP, MID_BF16_SHARP, MID_SINK, TINY_SINK_F32, MID_MULTI):
     ALL[_w.name] = _w
 
 
