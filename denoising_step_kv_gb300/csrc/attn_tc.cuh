@@ -118,10 +118,6 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ float ld_peer_f(const float* p, int rank) {
   uint32_t ra;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(p)), "r"(rank));
@@ -462,7 +458,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
   tc_fence_before();
-  cluster_sync();
+  cluster_barrier();
   // CTA `split` finishes queries [split * qpc, split * qpc + qpc):
   //   1. one thread per query reads every split's (m, l) and keeps the weights
   //   2. every thread gathers float4 column groups of O from all splits
@@ -507,7 +503,7 @@ __global__ void __launch_bounds__(192, 1)
     *reinterpret_cast<__nv_bfloat162*>(op) = __floats2bfloat162_rn(a0, a1);
     *reinterpret_cast<__nv_bfloat162*>(op + 2) = __floats2bfloat162_rn(a2, a3);
   }
-  cluster_sync();
+  cluster_barrier();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, S::TMEM_COLS);

@@ -25,7 +25,7 @@ __device__ __forceinline__ void store_kv32(uint8_t* base, const KvLayout& kv, in
 // QKV projection: accumulator row m (compact refresh index) times the row's
 // RMSNorm scale, RoPE on the q and k parts (rotate-half pairs (i, i + DH/2)
 // with a cos/sin table), stored into the layer's tiled Q/K/V cache.
-template <typename T, int DH, int NCH>
+template <typename T, int DH>
 struct EpiQKV {
   const int* rows;      // compact index -> row id (nullptr: identity)
   const float* rs;      // per compact row: RMS scale (< 0: skip the row)
@@ -37,7 +37,7 @@ struct EpiQKV {
   int L, d, rows_cap, streaming, S, W, max_pos;
 
   template <class LD>
-  __device__ __forceinline__ void run(int m, int n0, int M, int N, const LD& ld) const {
+  __device__ __forceinline__ void run(int m, int n0, int nch, int M, int N, const LD& ld) const {
     bool ok = m < M;
     int b = 0, slot = 0, pos = 0;
     float sc = 0.f;
@@ -65,7 +65,7 @@ struct EpiQKV {
     float a[32], bb[32];
     if (part == 2) {
 #pragma unroll 1
-      for (int c = 0; c < NCH; ++c) {
+      for (int c = 0; c < nch; ++c) {
         ld(c * 32, a);
         if (ok) {
 #pragma unroll
@@ -75,9 +75,9 @@ struct EpiQKV {
       }
     } else if (DH >= 64) {
       constexpr int HALF_CH = DH / 64;        // 32-column chunks in half a head
-      constexpr int HEADS = NCH * 32 / DH;    // heads in the tile
+      const int heads = nch * 32 / DH;        // heads in the tile
 #pragma unroll 1
-      for (int hd = 0; hd < HEADS; ++hd) {
+      for (int hd = 0; hd < heads; ++hd) {
 #pragma unroll 1
         for (int hc = 0; hc < HALF_CH; ++hc) {
           const int c1 = hd * DH + hc * 32, c2 = c1 + DH / 2;
@@ -99,7 +99,7 @@ struct EpiQKV {
       }
     } else {   // DH == 32: both halves of a head sit in one 32-column chunk
 #pragma unroll 1
-      for (int c = 0; c < NCH; ++c) {
+      for (int c = 0; c < nch; ++c) {
         ld(c * 32, a);
         if (ok) {
           const float2* rp = rope + static_cast<size_t>(pos) * 16;
@@ -119,7 +119,7 @@ struct EpiQKV {
 
 // out[m] = resid_m + acc[m]: resid_m = xres[m], or the embedding of the
 // token at position q_start + m % q_len of sequence m / q_len.
-template <typename T, int NCH>
+template <typename T>
 struct EpiResid {
   const T* xres;
   const T* embed;
@@ -129,7 +129,7 @@ struct EpiResid {
   unsigned* err;
 
   template <class LD>
-  __device__ __forceinline__ void run(int m, int n0, int M, int N, const LD& ld) const {
+  __device__ __forceinline__ void run(int m, int n0, int nch, int M, int N, const LD& ld) const {
     bool ok = m < M;
     const T* rrow = nullptr;
     if (ok) {
@@ -148,7 +148,7 @@ struct EpiResid {
     }
     float a[32], r[32];
 #pragma unroll 1
-    for (int c = 0; c < NCH; ++c) {
+    for (int c = 0; c < nch; ++c) {
       ld(c * 32, a);
       const int n = n0 + c * 32;
       if (ok && n < N) {
@@ -162,18 +162,18 @@ struct EpiResid {
 };
 
 // out[m] = GELU(rs[m] * acc[m]) with the exact (erf) GELU.
-template <typename T, int NCH>
+template <typename T>
 struct EpiGelu {
   const float* rs;
   T* out;
 
   template <class LD>
-  __device__ __forceinline__ void run(int m, int n0, int M, int N, const LD& ld) const {
+  __device__ __forceinline__ void run(int m, int n0, int nch, int M, int N, const LD& ld) const {
     const bool ok = m < M;
     const float sc = ok ? rs[m] : 0.f;
     float a[32];
 #pragma unroll 1
-    for (int c = 0; c < NCH; ++c) {
+    for (int c = 0; c < nch; ++c) {
       ld(c * 32, a);
       const int n = n0 + c * 32;
       if (ok && n < N) {
@@ -211,7 +211,6 @@ __device__ __forceinline__ void lm_merge(float& m, float& s, float& a, int& idx,
   m = mx; s = s_new; a = a_new;
 }
 
-template <int NCH>
 struct EpiLM {
   const float* rs;   // RMSNorm scale of each row of h
   int mask_id;
@@ -219,14 +218,14 @@ struct EpiLM {
   int n_tiles;
 
   template <class LD>
-  __device__ __forceinline__ void run(int m, int n0, int M, int N, const LD& ld) const {
+  __device__ __forceinline__ void run(int m, int n0, int nch, int M, int N, const LD& ld) const {
     const bool ok = m < M;
     const float sc = ok ? rs[m] : 0.f;
     float mx = -INFINITY, S = 0.f, A = 0.f;
     int idx = -1;
     float v[32];
 #pragma unroll 1
-    for (int c = 0; c < NCH; ++c) {
+    for (int c = 0; c < nch; ++c) {
       ld(c * 32, v);
       const int nb = n0 + c * 32;
       float cm = -INFINITY;
@@ -252,7 +251,7 @@ struct EpiLM {
       }
       lm_merge(mx, S, A, idx, cm, cs, ca, ci);
     }
-    if (ok) part[static_cast<size_t>(m) * n_tiles + n0 / (32 * NCH)] = LMPart{mx, S, A, idx};
+    if (ok) part[static_cast<size_t>(m) * n_tiles + n0 / (32 * nch)] = LMPart{mx, S, A, idx};
   }
 };
 

@@ -15,9 +15,10 @@
 namespace dllm {
 
 // Epilogue interface:
-//   template <class LD> __device__ void run(int m, int n0, int M, int N, const LD& ld) const;
+//   template <class LD> __device__ void run(int m, int n0, int nch, int M, int N, const LD& ld) const;
 // m: output row (may be >= M: then store nothing), n0: first column of the
-// tile; ld(col, v) fills v[0..31] with accumulator columns n0+col .. n0+col+31.
+// tile, nch: the tile's width in 32-column chunks; ld(col, v) fills v[0..31]
+// with accumulator columns n0+col .. n0+col+31.
 // On the tensor-core path ld is warp-collective: every lane calls it the same
 // number of times whatever its row.
 
@@ -163,7 +164,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int mb = tile % nM, nb = tile / nM;
       const int m = mb * BM + q * 32 + lane;
       TmemLoader ld{tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN)};
-      epi.run(m, nb * BN, M, N, ld);
+      epi.run(m, nb * BN, BN / 32, M, N, ld);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->tempty[acc]);
@@ -178,6 +179,163 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// Pair kernel for large M: persistent clusters of two CTAs; cluster tile p
+// covers rows [256 mp, 256 mp + 256) x columns [256 nb, 256 nb + 256), CTA
+// rank r the 128-row half 2 mp + r.  Each CTA loads its own 128 x 64 A tile
+// and one 128-row half of the 256 x 64 B tile, multicast into both CTAs, so a
+// CTA fetches 32 KB per k-block for 512 tensor cycles (M=128, N=256, K=64)
+// instead of 32 KB per 256 cycles with 128 x 128 tiles.  A stage is reloaded
+// only once both CTAs' MMAs have read it: every MMA commit arrives on the
+// empty barrier of both CTAs (count 2).  Accumulators: 2 x 256 TMEM columns.
+constexpr int PBN = 256;
+constexpr int PB_BYTES = PBN * BK * 2;             // two 16 KB halves
+constexpr int PSTAGE_BYTES = A_BYTES + PB_BYTES;   // 48 KB
+constexpr uint32_t PTMEM_COLS = 2 * PBN;
+template <int STAGES>
+constexpr size_t pair_smem_bytes() { return 1024 + STAGES * PSTAGE_BYTES + sizeof(Bars); }
+
+template <class Epi, int STAGES>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     int M_host, const int* __restrict__ M_dev, int M_cap, int M_min, int N, int K, Epi epi,
+                     unsigned* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + STAGES * A_BYTES;
+  Bars* bars = reinterpret_cast<Bars*>(smem + STAGES * PSTAGE_BYTES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_rank());
+  const int M = M_dev ? min(*M_dev, M_cap) : M_host;
+  const int nM = (M + BM - 1) / BM, nMP = (nM + 1) / 2, nN = (N + PBN - 1) / PBN, nK = (K + BK - 1) / BK;
+  // the same in both CTAs of a cluster: both run the same tiles and k-blocks
+  const int tiles = (M > 0 && M >= M_min) ? nMP * nN : 0;
+  const int cl = blockIdx.x >> 1, n_cl = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 2);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bars->tfull[a], 1);
+      mbar_init(&bars->tempty[a], 4);
+    }
+    mbar_init(&bars->done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&bars->tmem, PTMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier();       // the peer's barriers exist before any multicast lands
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  volatile int* abort = &bars->abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, par = 0;
+      for (int tile = cl; tile < tiles && !*abort; tile += n_cl) {
+        const int mp = tile % nMP, nb = tile / nMP;
+        // a half past the last row tile loads the last valid one again (its
+        // rows are >= M, the epilogue stores nothing for them)
+        const int mb_ld = min(2 * mp + rank, nM - 1);
+        for (int kb = 0; kb < nK; ++kb) {
+          if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort, err)) break;
+          mbar_expect_tx(&bars->full[stage], PSTAGE_BYTES);
+          tma_load_2d(sa + stage * A_BYTES, &tmA, kb * BK, mb_ld * BM, &bars->full[stage]);
+          tma_load_2d_mc(sb + stage * PB_BYTES + rank * B_BYTES, &tmB, kb * BK, nb * PBN + rank * BN,
+                         &bars->full[stage], 0x3);
+          issued |= 1u << stage;
+          par = (par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*abort) {
+        for (int s = 0; s < STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait(&bars->full[s], (par >> s) & 1u, nullptr, err);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(BM, PBN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      for (int tile = cl; tile < tiles && !*abort; tile += n_cl) {
+        if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1u, abort, err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * PBN);
+        bool ok = true;
+        for (int kb = 0; kb < nK; ++kb) {
+          if (!mbar_wait(&bars->full[stage], phase, abort, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sa + stage * A_BYTES), b0 = smem_u32(sb + stage * PB_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma_bf16(d_tmem, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc,
+                        (kb | k) != 0 ? 1u : 0u);
+          tc_commit_mc(&bars->empty[stage], 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&bars->tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // all MMAs (and the empty-barrier arrivals they owe the peer) complete
+      // before the cluster barrier below
+      tc_commit(&bars->done);
+      mbar_wait(&bars->done, 0, nullptr, err);
+    }
+  } else {
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = cl; tile < tiles; tile += n_cl) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&bars->tfull[acc], acc_phase, abort, err) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const int mp = tile % nMP, nb = tile / nMP;
+      const int m = (2 * mp + rank) * BM + q * 32 + lane;
+      TmemLoader ld{tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * PBN)};
+      epi.run(m, nb * PBN, PBN / 32, M, N, ld);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier();       // no multicast copy or commit still targets this CTA
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, PTMEM_COLS);
   }
 }
 
@@ -211,17 +369,9 @@ struct LocalRowLoader {
   }
 };
 
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 // A CTA overwrites only its own slice of rows with their sums; no other CTA
 // reads those rows, and each thread reads its element before writing it.
 __device__ __forceinline__ void partial_sum_store(float* dst, float4 v) { *reinterpret_cast<float4*>(dst) = v; }
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
 
 template <class Epi, int SPLITK>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -350,7 +500,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x < RPC) {
     const int r = row0 + threadIdx.x;
     LocalRowLoader ld{red + r * RED_LD};
-    epi.run(mb * BM + r, nb * BN, M, N, ld);
+    epi.run(mb * BM + r, nb * BN, BN / 32, M, N, ld);
   }
   cluster_barrier();
   if (warp == 1) {
@@ -391,7 +541,7 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(const T* __restrict__ A,
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   const int n0 = blockIdx.y * 32 * NCH;
   DotLoader<T> ld{A, B, m, n0, M, N, K};
-  epi.run(m, n0, M, N, ld);
+  epi.run(m, n0, NCH, M, N, ld);
 }
 }  // namespace simt
 

@@ -31,6 +31,35 @@ cudaError_t launch_persistent(dllm_cache* c, const CUtensorMap& ta, const CUtens
   return cudaGetLastError();
 }
 
+template <class Epi, int STAGES>
+cudaError_t launch_pair(dllm_cache* c, const CUtensorMap& ta, const CUtensorMap& tb, int a_rows, int M_host,
+                        const int* M_dev, int M_min, int N, int K, const Epi& epi, cudaStream_t st) {
+  constexpr size_t smem = tc::pair_smem_bytes<STAGES>();
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(tc::gemm_pair_kernel<Epi, STAGES>, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int m_rows = M_dev ? a_rows : M_host;
+  const int pairs = cdiv(cdiv(m_rows, tc::BM), 2) * cdiv(N, tc::PBN);
+  const int clusters = std::max(1, std::min(pairs, c->num_sms / 2));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(tc::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc::gemm_pair_kernel<Epi, STAGES>, ta, tb, M_host, M_dev, a_rows, M_min, N, K,
+                            epi, c->err);
+}
+
 template <class Epi, int S>
 cudaError_t launch_splitk(dllm_cache* c, const CUtensorMap& ta, const CUtensorMap& tb, int a_rows, int M_host,
                           const int* M_dev, int M_max, int N, int K, const Epi& epi, cudaStream_t st) {
@@ -62,11 +91,12 @@ cudaError_t launch_splitk(dllm_cache* c, const CUtensorMap& ta, const CUtensorMa
 // bf16 D = A . B^T with epilogue `epi`.  M is M_host, or the device count
 // M_dev (at most a_rows).  Small M streams the weights: a split-K cluster
 // kernel spreads them over enough CTAs to fill the GPU.  Large M is
-// tensor-bound: the persistent kernel.  With a device count both are
-// launched and each one skips the other's range.
+// tensor-bound: the multicast pair kernel (256-wide tiles; `wide_ok` says the
+// epilogue accepts them), else the persistent kernel.  With a device count
+// both sizes are launched and each one skips the other's range.
 template <class Epi>
 cudaError_t run_tc(dllm_cache* c, const void* A, int a_rows, int M_host, const int* M_dev, const void* B, int N,
-                   int K, const Epi& epi, cudaStream_t st) {
+                   int K, const Epi& epi, cudaStream_t st, bool wide_ok = true) {
   if (!M_dev && M_host <= 0) return cudaSuccess;
   CUtensorMap ta, tb;
   if (!make_tmap_2d(&ta, A, K, a_rows, static_cast<uint64_t>(K) * 2, tc::BK, tc::BM, true) ||
@@ -91,6 +121,8 @@ cudaError_t run_tc(dllm_cache* c, const void* A, int a_rows, int M_host, const i
     const int M_min = M_dev ? SMALL_M + 1 : 0;
     const int m_rows = M_dev ? a_rows : M_host;
     if (m_rows <= 256) return launch_persistent<Epi, 3>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
+    if (wide_ok && N % tc::PBN == 0)
+      return launch_pair<Epi, 4>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
     return launch_persistent<Epi, 4>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
   }
   return e;
@@ -107,9 +139,9 @@ cudaError_t run_simt(const void* A, int m_cap, int M_host, const int* M_dev, con
   return cudaGetLastError();
 }
 
-template <typename T, int DH, int NCH>
-EpiQKV<T, DH, NCH> make_qkv(dllm_cache* c, int layer, const int* rows) {
-  EpiQKV<T, DH, NCH> e;
+template <typename T, int DH>
+EpiQKV<T, DH> make_qkv(dllm_cache* c, int layer, const int* rows) {
+  EpiQKV<T, DH> e;
   const size_t off = static_cast<size_t>(layer) * c->kv_layer_bytes;
   e.rows = rows;
   e.rs = c->rs;
@@ -134,10 +166,11 @@ cudaError_t qkv_dh(dllm_cache* c, int layer, const void* A, int M_cap, const int
   const int d = c->d, N = 3 * d;
   const int M_host = M_dev ? 0 : M_cap;
   if (c->cfg.dtype == DLLM_BF16)
-    return run_tc(c, A, M_cap, M_host, M_dev, w, N, d, make_qkv<bf16, DH, 4>(c, layer, rows), st);
-  if (d % 128 == 0) return run_simt<4>(A, M_cap, M_host, M_dev, w, N, d, make_qkv<float, DH, 4>(c, layer, rows), st);
+    return run_tc(c, A, M_cap, M_host, M_dev, w, N, d, make_qkv<bf16, DH>(c, layer, rows), st,
+                  d % tc::PBN == 0);   // a 256-wide tile stays inside q, k or v
+  if (d % 128 == 0) return run_simt<4>(A, M_cap, M_host, M_dev, w, N, d, make_qkv<float, DH>(c, layer, rows), st);
   if constexpr (DH <= 64)
-    return run_simt<2>(A, M_cap, M_host, M_dev, w, N, d, make_qkv<float, DH, 2>(c, layer, rows), st);
+    return run_simt<2>(A, M_cap, M_host, M_dev, w, N, d, make_qkv<float, DH>(c, layer, rows), st);
   return cudaErrorInvalidValue;
 }
 
@@ -159,16 +192,16 @@ cudaError_t gemm_resid(dllm_cache* c, const void* A, const void* W, int M, int M
                        int K, const void* xres, const int* tok, const void* embed, int q_start, int q_len,
                        void* out, cudaStream_t st) {
   if (c->cfg.dtype == DLLM_BF16) {
-    EpiResid<bf16, 4> e{static_cast<const bf16*>(xres), static_cast<const bf16*>(embed), tok, q_start, q_len,
+    EpiResid<bf16> e{static_cast<const bf16*>(xres), static_cast<const bf16*>(embed), tok, q_start, q_len,
                         c->cfg.seq_len, c->cfg.vocab, static_cast<bf16*>(out), c->err};
     return run_tc(c, A, M_dev ? M_cap : M, M, M_dev, W, N, K, e, st);
   }
   if (N % 128 == 0) {
-    EpiResid<float, 4> e{static_cast<const float*>(xres), static_cast<const float*>(embed), tok, q_start, q_len,
+    EpiResid<float> e{static_cast<const float*>(xres), static_cast<const float*>(embed), tok, q_start, q_len,
                          c->cfg.seq_len, c->cfg.vocab, static_cast<float*>(out), c->err};
     return run_simt<4>(A, M_cap, M, M_dev, W, N, K, e, st);
   }
-  EpiResid<float, 1> e{static_cast<const float*>(xres), static_cast<const float*>(embed), tok, q_start, q_len,
+  EpiResid<float> e{static_cast<const float*>(xres), static_cast<const float*>(embed), tok, q_start, q_len,
                        c->cfg.seq_len, c->cfg.vocab, static_cast<float*>(out), c->err};
   return run_simt<1>(A, M_cap, M, M_dev, W, N, K, e, st);
 }
@@ -176,16 +209,16 @@ cudaError_t gemm_resid(dllm_cache* c, const void* A, const void* W, int M, int M
 cudaError_t gemm_gelu(dllm_cache* c, const void* A, const void* W, int M, int M_cap, const int* M_dev, int N,
                       int K, const float* rs, void* out, cudaStream_t st) {
   if (c->cfg.dtype == DLLM_BF16) {
-    EpiGelu<bf16, 4> e{rs, static_cast<bf16*>(out)};
+    EpiGelu<bf16> e{rs, static_cast<bf16*>(out)};
     return run_tc(c, A, M_dev ? M_cap : M, M, M_dev, W, N, K, e, st);
   }
-  EpiGelu<float, 1> e{rs, static_cast<float*>(out)};
+  EpiGelu<float> e{rs, static_cast<float*>(out)};
   return run_simt<1>(A, M_cap, M, M_dev, W, N, K, e, st);
 }
 
 cudaError_t gemm_lm(dllm_cache* c, const void* A, const void* W, int M, int V, int d, const float* rs,
                     int mask_id, void* part, int n_tiles, cudaStream_t st) {
-  EpiLM<4> e{rs, mask_id, static_cast<LMPart*>(part), n_tiles};
+  EpiLM e{rs, mask_id, static_cast<LMPart*>(part), n_tiles};
   if (c->cfg.dtype == DLLM_BF16) return run_tc(c, A, M, M, nullptr, W, V, d, e, st);
   return run_simt<4>(A, M, M, nullptr, W, V, d, e, st);
 }

@@ -76,6 +76,36 @@ def test_kv_refresh_ragged_rows(name):
         K.dllm_cache_free(c)
 
 
+@pytest.mark.parametrize("name", ["big_rows", "big_rows_dh64"])
+@pytest.mark.parametrize("n", [None, 700, 530, 513, 200])
+def test_kv_refresh_large_m(name, n):
+    """Row counts above the weight-streaming range: the host count (every
+    row) and device counts on both sides of the 512-row switch."""
+    w, m, W, D = _setup(name)
+    B, L, H, dh = w.batch, w.seq_len, w.n_heads, w.head_dim
+    tok = G.integers(5, 1, w.vocab, (B, L))
+    if n is not None and n > B * L:
+        pytest.skip("more rows than the cache holds")
+    rows = np.arange(B * L) if n is None else G.choice(6 + (n or 0), B * L, n)
+    c = _fresh(w)
+    try:
+        if n is None:
+            K.kv_refresh(c, 0, None, i32(tok), D["embed"], D["w_qkv"][0], None, None, 4)
+        else:
+            rows_d = torch.zeros(B * L, dtype=torch.int32, device="cuda")
+            rows_d[:n] = i32(rows)
+            K.kv_refresh(c, 0, None, i32(tok), D["embed"], D["w_qkv"][0], rows_d, i32([n]), 4)
+        assert K.dllm_cache_check(c) == 0
+        q, k, v = O.project_qkv(W["embed"][tok.reshape(-1)[rows]], W["w_qkv"][0], rows % L, H, w.dtype)
+        untouched = np.setdiff1d(np.arange(B * L), rows)
+        for f, want in ((K.FIELD_Q, q), (K.FIELD_K, k), (K.FIELD_V, v)):
+            got = read_kv(c, f, 0, w).reshape(B * L, H, dh)
+            assert close(got[rows], want, w), (name, n, f, max_err(got[rows], want))
+            assert np.all(got[untouched] == 0)
+    finally:
+        K.dllm_cache_free(c)
+
+
 def test_kv_refresh_empty_and_bad_rows():
     w, m, W, D = _setup("mid_bf16")
     B, L = w.batch, w.seq_len

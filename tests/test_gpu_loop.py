@@ -26,7 +26,8 @@ def _ambiguous(rec, w):
     return amb
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "tiny_fp32_sharp", "mid_bf16", "mid_bf16_dh64", "mid_bf16_sharp"])
+@pytest.mark.parametrize("name", ["tiny_fp32", "tiny_fp32_sharp", "mid_bf16", "mid_bf16_dh64", "mid_bf16_sharp",
+                                  "big_rows"])
 def test_free_running_generation(name):
     w = C.get(name)
     m = G.model(w)
