@@ -45,6 +45,7 @@ _SIGS = {
     "kv_refresh": [_VP, _I, _VP, _VP, _VP, _VP, _VP, _VP, _I, _VP],
     "block_attn": [_VP, _I, _I, _I, _VP, _VP],
     "block_attn_rows": [_VP, _I, _VP, _VP, _VP, _VP],
+    "active_rows": [_VP, _VP, _VP, _VP, _I, _I, _VP, _VP],
     "attn_out": [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _VP],
     "ffn_gelu": [_VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _VP],
     "lmhead_conf": [_VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP],
@@ -171,6 +172,10 @@ def block_attn(c, layer, q_start, q_len, out, stream=None):
 
 def block_attn_rows(c, layer, q_rows, n_q, out, stream=None):
     _check("block_attn_rows", lib().block_attn_rows(c, layer, _p(q_rows), _p(n_q), _p(out), _s(stream)))
+
+
+def active_rows(c, src, rows, n_rows, q_start, q_len, dst, stream=None):
+    _check("active_rows", lib().active_rows(c, _p(src), _p(rows), _p(n_rows), q_start, q_len, _p(dst), _s(stream)))
 
 
 def attn_out(c, o, w_o, x_res, tok, embed, q_start, q_len, m_dev, h, stream=None):

@@ -157,7 +157,7 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
             dalloc(&c->hist_p, static_cast<size_t>(g.batch) * blk * K * sizeof(float)) &&
             dalloc(&c->hist_n, static_cast<size_t>(g.batch) * blk * sizeof(int)) &&
             dalloc(&c->words, static_cast<size_t>(g.batch) * c->Lw * sizeof(uint32_t)) &&
-            dalloc(&c->rope, static_cast<size_t>(c->max_pos) * (g.head_dim / 2) * sizeof(float2)) &&
+            dalloc(&c->rope, static_cast<size_t>(g.head_dim / 2) * sizeof(float2)) &&
             dalloc(&c->err, sizeof(unsigned)) && dalloc(&c->ticket, sizeof(unsigned)) && dalloc(&c->X, sr * d * c->elem) && dalloc(&c->rs, sr * sizeof(float)) &&
             dalloc(&c->lm_part, static_cast<size_t>(c->lm_rows_cap) * c->lm_tiles_cap * 16) &&
             dalloc(&c->lm_rs, static_cast<size_t>(c->lm_rows_cap) * sizeof(float)) &&
@@ -168,22 +168,20 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
     cudaGetLastError();
     return fail(DLLM_ENOMEM, "dllm_cache_init: cudaMalloc failed");
   }
-  // RoPE table: cos/sin of pos * theta^(-2i/dh), computed in double on the host
+  // RoPE frequencies theta^(-2i/dh), computed in double on the host and kept
+  // as a float pair (hi, lo) so that kernels form pos * f to ~1e-10 relative
   {
     const int half = g.head_dim / 2;
-    std::vector<float2> tab(static_cast<size_t>(c->max_pos) * half);
+    std::vector<float2> tab(half);
     for (int i = 0; i < half; ++i) {
       const double inv = std::pow(static_cast<double>(g.rope_theta), -2.0 * i / g.head_dim);
-      for (int p = 0; p < c->max_pos; ++p) {
-        const double a = p * inv;
-        tab[static_cast<size_t>(p) * half + i] = make_float2(static_cast<float>(std::cos(a)),
-                                                             static_cast<float>(std::sin(a)));
-      }
+      const float hi = static_cast<float>(inv);
+      tab[i] = make_float2(hi, static_cast<float>(inv - static_cast<double>(hi)));
     }
     if (cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess) {
       free_all(c);
       delete c;
-      return fail(DLLM_ECUDA, "dllm_cache_init: RoPE table upload failed");
+      return fail(DLLM_ECUDA, "dllm_cache_init: RoPE frequency upload failed");
     }
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -342,8 +340,32 @@ dllm_status block_attn(dllm_cache* c, int layer, int q_start, int q_len, void* o
 dllm_status block_attn_rows(dllm_cache* c, int layer, const int32_t* q_rows_dev, const int32_t* n_q_dev,
                             void* out_dev, void* stream) {
   DLLM_CHECK_HANDLE(c);
-  (void)layer; (void)q_rows_dev; (void)n_q_dev; (void)out_dev; (void)stream;
-  return fail(DLLM_EUNSUPPORTED, "block_attn_rows: not built yet");
+  const dllm_cache_cfg& g = c->cfg;
+  if (layer < 0 || layer >= g.n_layers) return fail(DLLM_EINVAL, "block_attn_rows: layer out of range");
+  if (!q_rows_dev || !n_q_dev || !out_dev) return fail(DLLM_EINVAL, "block_attn_rows: null pointer");
+  if (g.sink > 0) return fail(DLLM_EINVAL, "block_attn_rows: dense cache only");
+  if (g.dtype != DLLM_BF16) return fail(DLLM_EUNSUPPORTED, "block_attn_rows: bf16 caches only");
+  if (g.batch > 256) return fail(DLLM_EUNSUPPORTED, "block_attn_rows: batch above 256");
+  if (!aligned16(out_dev)) return fail(DLLM_EINVAL, "block_attn_rows: out must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ProfScope prof(c, DLLM_PROF_ATTN, st);
+  DLLM_LAUNCH(attn_rows_dense(c, layer, q_rows_dev, n_q_dev, out_dev, st), "block_attn_rows");
+  return DLLM_OK;
+}
+
+dllm_status active_rows(dllm_cache* c, const void* src_dev, const int32_t* rows_dev, const int32_t* n_rows_dev,
+                        int q_start, int q_len, void* dst_dev, void* stream) {
+  DLLM_CHECK_HANDLE(c);
+  const dllm_cache_cfg& g = c->cfg;
+  if (!src_dev || !rows_dev || !n_rows_dev || !dst_dev) return fail(DLLM_EINVAL, "active_rows: null pointer");
+  if (g.sink > 0) return fail(DLLM_EINVAL, "active_rows: dense cache only");
+  if (q_start < 0 || q_len < 1 || q_start + q_len > g.seq_len)
+    return fail(DLLM_EINVAL, "active_rows: query range outside the sequence");
+  if (!aligned16(src_dev) || !aligned16(dst_dev)) return fail(DLLM_EINVAL, "active_rows: pointers not 16-byte aligned");
+  DLLM_LAUNCH(launch_active_rows(c, src_dev, rows_dev, n_rows_dev, q_start, q_len, dst_dev,
+                                 static_cast<cudaStream_t>(stream)),
+              "active_rows");
+  return DLLM_OK;
 }
 
 dllm_status attn_out(dllm_cache* c, const void* o_dev, const void* w_o_dev, const void* x_res_dev,
@@ -352,6 +374,10 @@ dllm_status attn_out(dllm_cache* c, const void* o_dev, const void* w_o_dev, cons
   DLLM_CHECK_HANDLE(c);
   const dllm_cache_cfg& g = c->cfg;
   if (!o_dev || !w_o_dev || !h_dev) return fail(DLLM_EINVAL, "attn_out: null o, w_o or h");
+  // with a device row count and no x_res, the residual rows are the compact
+  // layer-0 input the last kv_refresh gathered (embeddings of its rows)
+  const bool from_gather = !x_res_dev && m_dev;
+  if (from_gather) x_res_dev = c->X;
   if (!x_res_dev && (!tok_dev || !embed_dev)) return fail(DLLM_EINVAL, "attn_out: need x_res, or tok and embed");
   if (!x_res_dev && (q_len < 1 || q_start < 0 || q_start + q_len > g.seq_len))
     return fail(DLLM_EINVAL, "attn_out: query range outside the sequence");

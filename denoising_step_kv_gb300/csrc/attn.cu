@@ -5,6 +5,7 @@
 #include <algorithm>
 
 #include "attn_tc.cuh"
+#include "attn_rows.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -93,6 +94,35 @@ cudaError_t launch_tc(dllm_cache* c, const uint8_t* Ql, const uint8_t* Kl, const
 }
 
 }  // namespace
+
+template <int DH>
+cudaError_t launch_rows(dllm_cache* c, const uint8_t* Ql, const uint8_t* Kl, const uint8_t* Vl, const int* rows,
+                        const int* n_rows, bf16* out, cudaStream_t st) {
+  using S = attn_rows::Shape<DH>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(attn_rows::attn_rows_kernel<DH>, S::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(DH));
+  attn_rows::attn_rows_kernel<DH><<<c->num_sms, 192, S::SMEM, st>>>(
+      Ql, Kl, Vl, c->kv, c->cfg.seq_len, c->cfg.batch, c->cfg.n_heads, rows, n_rows, c->seq_rows, scale_log2, out,
+      c->err);
+  return cudaGetLastError();
+}
+
+cudaError_t attn_rows_dense(dllm_cache* c, int layer, const int* rows, const int* n_rows, void* out,
+                            cudaStream_t st) {
+  const size_t off = static_cast<size_t>(layer) * c->kv_layer_bytes;
+  const uint8_t* Ql = static_cast<const uint8_t*>(c->q) + off;
+  const uint8_t* Kl = static_cast<const uint8_t*>(c->k) + off;
+  const uint8_t* Vl = static_cast<const uint8_t*>(c->v) + off;
+  bf16* o = static_cast<bf16*>(out);
+  if (c->cfg.head_dim == 128) return launch_rows<128>(c, Ql, Kl, Vl, rows, n_rows, o, st);
+  if (c->cfg.head_dim == 64) return launch_rows<64>(c, Ql, Kl, Vl, rows, n_rows, o, st);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t attn_dense(dllm_cache* c, int layer, int q_pos0, int q_len, int kv_len, int n_seq, void* out,
                        cudaStream_t st) {

@@ -1,0 +1,365 @@
+// Cached attention for queries given as a sorted list of flat rows b * L + pos
+// (every row that passes through the layer stack of a multi-layer step):
+// each query attends over all L cached positions of its own sequence.
+//
+// Persistent kernel, one CTA per SM.  A work item is (sequence b, query tile
+// of up to 128 of its rows, head h); items are numbered in (b, tile) order,
+// heads fastest, and CTA i takes items i, i + gridDim.x, ...  The per-sequence
+// row ranges come from a binary search of the sorted list at kernel start.
+// Within an item the pipeline is the one of attn_tc_kernel with one query per
+// MMA row (no replicas, no key splits): lanes 0/1 of warp 0 stream K/V tiles
+// (one bulk copy each), one thread of warp 1 issues S = Q K^T and
+// O += P_hi V + P_lo V on tcgen05, warps 2-5 run the online softmax (one
+// query per thread) and, after the last tile, normalise O and store it.  The
+// barrier phases run on a tile counter shared by all items of the CTA.
+#pragma once
+#include "attn_tc.cuh"
+
+namespace dllm {
+namespace attn_rows {
+
+using attn_tc::KT;
+using attn_tc::LAZY;
+constexpr int KS = 3, VS = 4, QROWS = 128, MAX_SEQ = 256;
+
+template <int DH>
+struct Shape {
+  static constexpr int Q_BYTES = QROWS * DH * 2;
+  static constexpr int KV_TILE = KT * DH * 2;
+  static constexpr int P_BYTES = QROWS * KT * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_P = OFF_Q + Q_BYTES;        // [2 buffers][hi, lo]
+  static constexpr int OFF_K = OFF_P + 4 * P_BYTES;
+  static constexpr int OFF_V = OFF_K + KS * KV_TILE;
+  static constexpr int OFF_SEQ = OFF_V + VS * KV_TILE;  // [MAX_SEQ + 1] first item, [MAX_SEQ + 1] first row
+  static constexpr int OFF_BAR = OFF_SEQ + (2 * MAX_SEQ + 2) * 4;
+  static constexpr int SMEM = 1024 + OFF_BAR + 256;
+  static constexpr uint32_t TMEM_COLS = 256;           // S: 2 x 64 columns, O: DH columns
+  static constexpr uint32_t S_COL = 0, O_COL = 128;
+};
+
+struct Bars {
+  uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
+  uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
+  uint64_t q_ready, done;
+  uint32_t tmem;
+  int abort;
+};
+
+// rows [0, n) sorted ascending; out [n][ld] bf16 (ld = H * DH).
+template <int DH>
+__global__ void __launch_bounds__(192, 1)
+    attn_rows_kernel(const uint8_t* __restrict__ Ql, const uint8_t* __restrict__ Kl,
+                     const uint8_t* __restrict__ Vl, KvLayout kv, int L, int n_seq, int n_heads,
+                     const int* __restrict__ rows, const int* __restrict__ n_rows, int rows_cap, float scale_log2,
+                     bf16* __restrict__ out, unsigned* err) {
+  using S = Shape<DH>;
+  using attn_tc::sw128_off;
+  using attn_tc::pack2;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  Bars* bars = reinterpret_cast<Bars*>(sm + S::OFF_BAR);
+  int* first_item = reinterpret_cast<int*>(sm + S::OFF_SEQ);   // [n_seq + 1], in (b, tile) units
+  int* row_start = first_item + MAX_SEQ + 1;                     // [n_seq + 1]
+  volatile int* abort = &bars->abort;
+  const int n = min(*n_rows, rows_cap);
+  const int n_tiles = cdiv(L, KT);
+
+  if (tid == 0) {
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_empty[i], 4);
+      mbar_init(&bars->p_full[i], 4);
+      mbar_init(&bars->pv_done[i], 1);
+    }
+    mbar_init(&bars->q_ready, 4);
+    mbar_init(&bars->done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  // per-sequence row ranges: rows of sequence b are [start_b, start_{b+1})
+  for (int b = tid; b <= n_seq; b += 192) {
+    int lo = 0, hi = n;   // first index with rows[i] >= b * L
+    const long long key = static_cast<long long>(b) * L;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (rows[mid] < key) lo = mid + 1; else hi = mid;
+    }
+    row_start[b] = lo;    // rows past the last sequence (out of range) are left out
+    first_item[b] = lo;   // overwritten below with tile prefix sums
+  }
+  if (warp == 1) tmem_alloc(&bars->tmem, S::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {   // row starts -> prefix sums of query tiles per sequence
+    int acc = 0;
+    for (int b = 0; b < n_seq; ++b) {
+      const int cnt = row_start[b + 1] - row_start[b];
+      first_item[b] = acc;
+      acc += cdiv(cnt, QROWS);
+    }
+    first_item[n_seq] = acc;
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  const int n_items = first_item[n_seq] * n_heads;
+  // item -> (b, query tile, head)
+  auto decode = [&](int item, int& b, int& qt, int& h) {
+    h = item % n_heads;
+    const int bt = item / n_heads;
+    int lo = 0, hi = n_seq - 1;   // last b with first_item[b] <= bt
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (first_item[mid] <= bt) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    qt = bt - first_item[b];
+  };
+
+  if (warp == 0) {
+    if (lane < 2) {
+      const uint8_t* src = lane == 0 ? Kl : Vl;
+      const int slots = lane == 0 ? KS : VS;
+      uint64_t* fullb = lane == 0 ? bars->k_full : bars->v_full;
+      uint64_t* emptyb = lane == 0 ? bars->k_empty : bars->v_empty;
+      uint8_t* ring = sm + (lane == 0 ? S::OFF_K : S::OFF_V);
+      uint32_t issued = 0, par = 0;
+      int J = 0;   // tile counter over all items of this CTA
+      for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
+        int b, qt, h;
+        decode(item, b, qt, h);
+        for (int j = 0; j < n_tiles; ++j, ++J) {
+          const int s = J % slots;
+          const uint32_t ph = (J / slots) & 1u;
+          if (!mbar_wait(&emptyb[s], ph ^ 1u, abort, err)) break;
+          mbar_expect_tx(&fullb[s], S::KV_TILE);
+          bulk_load(ring + s * S::KV_TILE, src + kv.tile_off(b, h, j * KT), S::KV_TILE, &fullb[s]);
+          issued |= 1u << s;
+          par = (par & ~(1u << s)) | (ph << s);
+        }
+      }
+      if (*abort)
+        for (int s = 0; s < slots; ++s)
+          if (issued & (1u << s)) mbar_wait(&fullb[s], (par >> s) & 1u, nullptr, err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16(QROWS, KT);
+      const uint32_t id_pv = attn_tc::idesc_bf16_bmn(QROWS, 64);
+      const uint32_t q_base = smem_u32(sm + S::OFF_Q);
+      // P_J V_J; `first`: the first tile of an item (overwrites O)
+      auto pv = [&](int J, bool first) -> bool {
+        const int pb = J & 1, vs = J % VS;
+        if (!mbar_wait(&bars->p_full[pb], (J >> 1) & 1u, abort, err)) return false;
+        if (!mbar_wait(&bars->v_full[vs], (J / VS) & 1u, abort, err)) return false;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(sm + S::OFF_V + vs * S::KV_TILE);
+#pragma unroll
+        for (int half = 0; half < DH / 64; ++half) {
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t pbase = smem_u32(sm + S::OFF_P + (pb * 2 + part) * S::P_BYTES);
+#pragma unroll
+            for (int k = 0; k < KT / 16; ++k)
+              tc_mma_bf16(tmem + S::O_COL + half * 64, sdesc_sw128(pbase + k * 32),
+                          attn_tc::sdesc_sw128_mn(vb + half * KT * 128 + k * 2048), id_pv,
+                          (!first || part > 0 || k > 0) ? 1u : 0u);
+          }
+        }
+        tc_commit(&bars->pv_done[pb]);
+        tc_commit(&bars->v_empty[vs]);
+        return true;
+      };
+      bool ok = true;
+      int J = 0, it = 0;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+        ok = mbar_wait(&bars->q_ready, it & 1u, abort, err);
+        const int J0 = J;
+        for (int j = 0; j < n_tiles && ok; ++j, ++J) {
+          const int ks = J % KS, sb = J & 1;
+          if (!mbar_wait(&bars->k_full[ks], (J / KS) & 1u, abort, err)) { ok = false; break; }
+          if (!mbar_wait(&bars->s_empty[sb], ((J >> 1) & 1u) ^ 1u, abort, err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kb = smem_u32(sm + S::OFF_K + ks * S::KV_TILE);
+#pragma unroll
+          for (int kc = 0; kc < DH / 16; ++kc)
+            tc_mma_bf16(tmem + S::S_COL + sb * KT, sdesc_sw128(q_base + (kc >> 2) * (QROWS * 128) + (kc & 3) * 32),
+                        sdesc_sw128(kb + (kc >> 2) * (KT * 128) + (kc & 3) * 32), id_s, kc > 0 ? 1u : 0u);
+          tc_commit(&bars->s_full[sb]);
+          tc_commit(&bars->k_empty[ks]);
+          if (j > 0) ok = pv(J - 1, J - 1 == J0);
+        }
+        if (ok && !*abort) ok = pv(J - 1, J - 1 == J0);
+      }
+      tc_commit(&bars->done);
+      mbar_wait(&bars->done, 0, nullptr, err);
+    }
+  } else {
+    const int wq = warp & 3, m = wq * 32 + lane;   // this thread's query row (TMEM lane)
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const int st = tid - 64;                        // 128 staging threads
+    // P rows of queries past the tile's count keep their zeros
+    for (int e = st; e < 4 * S::P_BYTES / 16; e += 128)
+      *reinterpret_cast<uint4*>(sm + S::OFF_P + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+    int J = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      int b, qt, h;
+      decode(item, b, qt, h);
+      const int r0 = row_start[b] + qt * QROWS;
+      const int r_end = row_start[b + 1];
+      const int nq = min(QROWS, r_end - r0);
+      // ---- stage Q of rows r0 .. r0 + nq (zero past nq); the previous item's
+      // S MMAs are done (its last P V has completed before we got here)
+      for (int e = st; e < QROWS * (DH / 8); e += 128) {
+        const int q = e / (DH / 8), c = e % (DH / 8);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (q < nq) {
+          const int row = rows[r0 + q];
+          v = *reinterpret_cast<const uint4*>(Ql + kv.chunk_off(b, h, row - b * L, c));
+        }
+        *reinterpret_cast<uint4*>(sm + S::OFF_Q + (c >> 3) * (QROWS * 128) + sw128_off(q, c & 7)) = v;
+      }
+      attn_tc::fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->q_ready);
+
+      const bool valid = m < nq;
+      float m_ref = -INFINITY, l_sum = 0.f;
+      const int J0 = J;
+      for (int j = 0; j < n_tiles; ++j, ++J) {
+        const int sb = J & 1;
+        int w_ok = 1;
+        if (lane == 0) w_ok = mbar_wait(&bars->s_full[sb], (J >> 1) & 1u, abort, err) ? 1 : 0;
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) { ok = false; break; }
+        tc_fence_after();
+        float sv[KT];
+        {
+          float t0[32], t1[32];
+          const uint32_t col = tmem + lane_off + S::S_COL + sb * KT;
+          tmem_ld32(col, t0);
+          tmem_ld32(col + 32, t1);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            sv[i] = t0[i];
+            sv[i + 32] = t1[i];
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_empty[sb]);
+        const int key0 = j * KT;
+        float mt = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < KT; ++i) {
+          sv[i] = (valid && key0 + i < L) ? sv[i] * scale_log2 : -INFINITY;
+          mt = fmaxf(mt, sv[i]);
+        }
+        float alpha = 1.f;
+        bool moved = false;
+        if (mt > m_ref + LAZY || (m_ref == -INFINITY && mt != -INFINITY)) {
+          alpha = m_ref == -INFINITY ? 0.f : exp2f(m_ref - mt);
+          m_ref = mt;
+          moved = j > 0 && alpha != 1.f;
+        }
+        float ls = 0.f;
+#pragma unroll
+        for (int i = 0; i < KT; ++i) {
+          sv[i] = m_ref == -INFINITY ? 0.f : exp2f(sv[i] - m_ref);
+          ls += sv[i];
+        }
+        l_sum = l_sum * alpha + ls;
+        if (__any_sync(0xffffffffu, moved)) {   // rescale O after the previous P V
+          int ok2 = 1;
+          if (lane == 0) ok2 = mbar_wait(&bars->pv_done[(J - 1) & 1], ((J - 1) >> 1) & 1u, abort, err) ? 1 : 0;
+          ok2 = __shfl_sync(0xffffffffu, ok2, 0);
+          if (!ok2) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < DH / 32; ++c) {
+            float o[32];
+            tmem_ld32(tmem + lane_off + S::O_COL + c * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            attn_tc::tmem_st32(tmem + lane_off + S::O_COL + c * 32, o);
+          }
+        }
+        // P buffer sb was last read by P V of tile J - 2
+        if (J >= 2) {
+          int ok3 = 1;
+          if (lane == 0) ok3 = mbar_wait(&bars->pv_done[sb], ((J - 2) >> 1) & 1u, abort, err) ? 1 : 0;
+          ok3 = __shfl_sync(0xffffffffu, ok3, 0);
+          if (!ok3) { ok = false; break; }
+        }
+        if (valid) {
+          uint8_t* ph = sm + S::OFF_P + (sb * 2) * S::P_BYTES;
+          uint8_t* pl = ph + S::P_BYTES;
+#pragma unroll
+          for (int c = 0; c < KT / 8; ++c) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float a = sv[c * 8 + 2 * i], bb = sv[c * 8 + 2 * i + 1];
+              const __nv_bfloat162 hb = __floats2bfloat162_rn(a, bb);
+              const float2 hf = __bfloat1622float2(hb);
+              hi[i] = *reinterpret_cast<const uint32_t*>(&hb);
+              lo[i] = pack2(a - hf.x, bb - hf.y);
+            }
+            const uint32_t off = sw128_off(m, c);
+            *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(pl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+        }
+        attn_tc::fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full[sb]);
+      }
+      if (!ok) break;
+      // ---- the item's last P V done: O / l for this thread's query
+      {
+        int w_ok = 1;
+        if (lane == 0) w_ok = mbar_wait(&bars->pv_done[(J - 1) & 1], ((J - 1) >> 1) & 1u, abort, err) ? 1 : 0;
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) { ok = false; break; }
+        tc_fence_after();
+        const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+        bf16* orow = out + static_cast<size_t>(r0 + m) * (n_heads * DH) + h * DH;
+#pragma unroll 1
+        for (int c = 0; c < DH / 32; ++c) {
+          float o[32];
+          tmem_ld32(tmem + lane_off + S::O_COL + c * 32, o);
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= inv;
+            store_row(orow + c * 32, o, 32);
+          }
+        }
+        (void)J0;
+        tc_fence_before();   // O reads ordered before the next item's first P V
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, S::TMEM_COLS);
+  }
+}
+
+}  // namespace attn_rows
+}  // namespace dllm

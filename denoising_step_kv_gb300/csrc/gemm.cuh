@@ -1,12 +1,15 @@
-// D = A . B^T for K-major A [M][K] and B [N][K], finished by an epilogue
-// functor that receives one accumulator row at a time.
+// D = A . B^T for K-major A [M][K] (rows) and B [N][K] (weights), finished
+// by an epilogue functor that receives one output row of a tile at a time.
 //
-// bf16: persistent tcgen05 kernel.  Warp 0 issues TMA loads of 128x64 A and B
-// tiles (128-byte swizzle) into a STAGES-deep ring; one thread of warp 1
-// issues tcgen05.mma (M=128, N=128, K=16) into one of two TMEM accumulators
-// (2 x 128 columns) and commits to mbarriers; warps 2-5 read the finished
-// accumulator with tcgen05.ld (warp w owns TMEM lanes 32*(w%4) ...) and run
-// the epilogue while the next tile accumulates into the other buffer.
+// bf16, three tcgen05 kernels (TMA loads with 128-byte swizzle into an
+// mbarrier ring, one thread issuing the MMAs, fp32 accumulators in TMEM):
+//   gemm_tc_kernel      persistent, 128 x 128 tiles, two TMEM accumulators so
+//                       the epilogue of one tile overlaps the next tile's MMAs;
+//   gemm_pair_kernel    the same with clusters of two CTAs on 128 x 256 tiles
+//                       that share (multicast) the weight tile - large M;
+//   gemm_skinny_kernel  weights as the MMA's A operand, the few rows as its B
+//                       operand, K split over a cluster - M <= 256, weight
+//                       streaming.
 // fp32: a SIMT kernel whose "loader" computes 32 dot products on demand, used
 // only by the fp32 workload (tensor cores have no fp32 path within 1e-5).
 #pragma once
@@ -339,67 +342,89 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// Split-K over a cluster of SPLITK CTAs, one output tile per cluster: CTA
-// rank r accumulates k-blocks [r * kpc, (r + 1) * kpc) into its TMEM, copies
-// the fp32 partial tile to its shared memory, and after a cluster barrier
-// finishes rows [r * 128/SPLITK, (r + 1) * 128/SPLITK) by summing the
-// partials of all ranks (in rank order) through distributed shared memory.
-// Used when few output tiles would leave most SMs without weight bytes to
-// stream.  The grid covers M_cap rows; clusters past the device count exit.
-constexpr int SK_STAGES = 3;     // two CTAs per SM
-constexpr int RED_LD = BN + 4;   // padded fp32 row of the partial tile
-struct SkBars {
-  uint64_t full[SK_STAGES];
-  uint64_t empty[SK_STAGES];
+// Weight-streaming GEMM for small M (at most 256 rows): D^T = B . A^T.  The
+// weights B [N][K] are the MMA's A operand (128 output columns per CTA, on
+// the TMEM lanes) and the rows A [M][K] its B operand (M rounded up to 16, on
+// the TMEM columns), so every weight byte is read from HBM once and no MMA
+// work goes to padding rows.  A cluster of SPLITK CTAs splits K.  Rank r owns
+// rows [r * tpr, (r + 1) * tpr) of the tile: after every rank's MMAs are done
+// (cluster barrier), each rank pushes its fp32 partial of those rows into the
+// owner's shared memory (16-byte remote stores, no round trips), and after
+// a second barrier the owner sums the SPLITK partials (rank order) while
+// running the epilogue, spread over (row, piece) items.  The epilogue warps
+// warm L2 with the epilogue's side data while the MMAs run.  The stage ring holds as many
+// stages as fit for this M (rows are loaded in 64-row boxes, only as needed).
+constexpr int SKN_MAX_ROWS = 256;
+constexpr int SKN_W_BYTES = 128 * BK * 2;        // 16 KB of weights per k-block
+constexpr int SKN_XBOX = 64;                     // rows per load of A
+constexpr int SKN_RING = 192 * 1024;
+constexpr int SKN_MAX_ST = 8;
+struct SknBars {
+  uint64_t full[SKN_MAX_ST];
+  uint64_t empty[SKN_MAX_ST];
   uint64_t tfull;
   uint32_t tmem;
   int abort;
 };
-constexpr size_t SK_SMEM = 1024 + SK_STAGES * STAGE_BYTES + sizeof(SkBars);
-static_assert(BM * RED_LD * 4 <= SK_STAGES * STAGE_BYTES, "partial tile must fit in the stage ring");
+constexpr size_t SKN_SMEM = 1024 + SKN_RING + sizeof(SknBars);
 
-struct LocalRowLoader {
-  const float* row;
+// Rows per rank (a multiple of 4) and the row stride of the receive buffer
+// recv[rank][column][ldr], padded so that ldr / 4 is odd: a warp's 16-byte
+// pushes (a lane per column, four rows each) spread over all banks.
+__host__ __device__ constexpr int skn_tpr(int M, int S) { return ((M + S - 1) / S + 3) & ~3; }
+__host__ __device__ constexpr int skn_ldr(int tpr) { return (tpr / 4) % 2 ? tpr : tpr + 4; }
+static_assert(8 * 128 * skn_ldr(skn_tpr(SKN_MAX_ROWS, 8)) * 4 <= SKN_RING, "receive buffer fits in the ring");
+static_assert(6 * 128 * skn_ldr(skn_tpr(SKN_MAX_ROWS, 6)) * 4 <= SKN_RING, "receive buffer fits in the ring");
+static_assert(4 * 128 * skn_ldr(skn_tpr(SKN_MAX_ROWS, 4)) * 4 <= SKN_RING, "receive buffer fits in the ring");
+static_assert(3 * 128 * skn_ldr(skn_tpr(SKN_MAX_ROWS, 3)) * 4 <= SKN_RING, "receive buffer fits in the ring");
+static_assert(2 * 128 * skn_ldr(skn_tpr(SKN_MAX_ROWS, 2)) * 4 <= SKN_RING, "receive buffer fits in the ring");
+
+// Columns [col, col + 32) of local row rr of the owner's tile: the sum, in
+// rank order, of the SPLITK partials pushed into recv.
+template <int SPLITK>
+struct RecvSumLoader {
+  const float* recv;
+  int ldr, rr;
   __device__ __forceinline__ void operator()(int col, float (&v)[32]) const {
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      const float4 x = *reinterpret_cast<const float4*>(row + col + j);
-      v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
-    }
+    for (int j = 0; j < 32; ++j) v[j] = recv[(col + j) * ldr + rr];
+#pragma unroll
+    for (int p = 1; p < SPLITK; ++p)
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] += recv[((p * 128) + col + j) * ldr + rr];
   }
 };
 
-// A CTA overwrites only its own slice of rows with their sums; no other CTA
-// reads those rows, and each thread reads its element before writing it.
-__device__ __forceinline__ void partial_sum_store(float* dst, float4 v) { *reinterpret_cast<float4*>(dst) = v; }
-
 template <class Epi, int SPLITK>
 __global__ void __launch_bounds__(THREADS, 1)
-    gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       int M_host, const int* __restrict__ M_dev, int M_cap, int M_max, int N, int K, Epi epi,
+    gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       int M_host, const int* __restrict__ M_dev, int M_cap, int N, int K, Epi epi,
                        unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint8_t* sa = smem;
-  uint8_t* sb = smem + SK_STAGES * A_BYTES;
-  SkBars* bars = reinterpret_cast<SkBars*>(smem + SK_STAGES * STAGE_BYTES);
-  float* red = reinterpret_cast<float*>(smem);      // [BM][RED_LD], after the mainloop
+  SknBars* bars = reinterpret_cast<SknBars*>(smem + SKN_RING);
+  float* recv = reinterpret_cast<float*>(smem);    // [SPLITK][128][ldr], after the mainloop
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = M_dev ? min(*M_dev, M_cap) : M_host;
-  const int nN = (N + BN - 1) / BN, nK = (K + BK - 1) / BK;
-  const int tile = blockIdx.x / SPLITK;
+  // the same decision in every CTA of the cluster
+  if (M <= 0 || M > SKN_MAX_ROWS) return;
   const int rank = static_cast<int>(cluster_rank());
-  const int mb = tile / nN, nb = tile % nN;
-  // the same decision in every CTA of the cluster: skip the tile entirely
-  if (M > M_max || mb * BM >= M) return;
-  const int kpc = (nK + SPLITK - 1) / SPLITK;
+  const int nb = blockIdx.x / SPLITK;
+  const int nK = (K + BK - 1) / BK, kpc = (nK + SPLITK - 1) / SPLITK;
   const int kb0 = rank * kpc, kb1 = min(nK, kb0 + kpc);
-  const bool has_k = kb1 > kb0;   // an empty K range contributes zeros
+  const bool has_k = kb1 > kb0;
+  const int xrows = (M + SKN_XBOX - 1) / SKN_XBOX * SKN_XBOX;   // rows loaded per k-block
+  const int nx = xrows / SKN_XBOX;
+  const int n_mma = (M + 15) / 16 * 16;
+  const int stage_bytes = SKN_W_BYTES + xrows * 128;
+  const int n_st = min(SKN_MAX_ST, SKN_RING / stage_bytes);
+  const int tpr = skn_tpr(M, SPLITK), ldr = skn_ldr(tpr);
+  const int r0 = rank * tpr, r1 = min(M, r0 + tpr);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < SK_STAGES; ++s) {
+    for (int s = 0; s < n_st; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
@@ -407,107 +432,103 @@ __global__ void __launch_bounds__(THREADS, 1)
     bars->abort = 0;
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(&bars->tmem, BN);
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem;
   volatile int* abort = &bars->abort;
+  // the producer starts at once; warps 1-5 meet after the TMEM allocation
+  uint32_t tmem = 0;
+  if (warp >= 1) {
+    if (warp == 1) tmem_alloc(&bars->tmem, 256);
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(THREADS - 32) : "memory");
+    tc_fence_after();
+    tmem = bars->tmem;
+  }
 
+  int ok = 1;
   if (warp == 0) {
     if (lane == 0) {
-      prefetch_tmap(&tmA);
-      prefetch_tmap(&tmB);
+      prefetch_tmap(&tmW);
+      prefetch_tmap(&tmX);
       uint32_t issued = 0, par = 0;
       for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
-        const int stage = i % SK_STAGES;
-        const uint32_t phase = (i / SK_STAGES) & 1u;
+        const int stage = i % n_st;
+        const uint32_t phase = (i / n_st) & 1u;
         if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort, err)) break;
-        mbar_expect_tx(&bars->full[stage], STAGE_BYTES);
-        tma_load_2d(sa + stage * A_BYTES, &tmA, kb * BK, mb * BM, &bars->full[stage]);
-        tma_load_2d(sb + stage * B_BYTES, &tmB, kb * BK, nb * BN, &bars->full[stage]);
+        uint8_t* st = smem + stage * stage_bytes;
+        mbar_expect_tx(&bars->full[stage], stage_bytes);
+        tma_load_2d(st, &tmW, kb * BK, nb * 128, &bars->full[stage]);
+        for (int j = 0; j < nx; ++j)
+          tma_load_2d(st + SKN_W_BYTES + j * SKN_XBOX * 128, &tmX, kb * BK, j * SKN_XBOX, &bars->full[stage]);
         issued |= 1u << stage;
         par = (par & ~(1u << stage)) | (phase << stage);
       }
       if (*abort)
-        for (int s = 0; s < SK_STAGES; ++s)
+        for (int s = 0; s < n_st; ++s)
           if (issued & (1u << s)) mbar_wait(&bars->full[s], (par >> s) & 1u, nullptr, err);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(BM, BN);
+      const uint32_t idesc = idesc_bf16(128, n_mma);
       for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
-        const int stage = i % SK_STAGES;
-        const uint32_t phase = (i / SK_STAGES) & 1u;
+        const int stage = i % n_st;
+        const uint32_t phase = (i / n_st) & 1u;
         if (!mbar_wait(&bars->full[stage], phase, abort, err)) break;
         tc_fence_after();
-        const uint32_t a0 = smem_u32(sa + stage * A_BYTES), b0 = smem_u32(sb + stage * B_BYTES);
+        const uint32_t w0 = smem_u32(smem + stage * stage_bytes), x0 = w0 + SKN_W_BYTES;
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)
-          tc_mma_bf16(tmem, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc, (i | k) != 0 ? 1u : 0u);
+          tc_mma_bf16(tmem, sdesc_sw128(w0 + k * 32), sdesc_sw128(x0 + k * 32), idesc, (i | k) != 0 ? 1u : 0u);
         tc_commit(&bars->empty[stage]);
       }
-      // completes once every MMA above is done (also when none was issued)
-      tc_commit(&bars->tfull);
+      tc_commit(&bars->tfull);   // completes once every MMA above is done
     }
   } else {
-    // partial accumulator -> shared memory (all MMAs done: the ring is free)
-    const int q = warp & 3;
-    int ok = 1;
+    // while the MMAs run: warm L2 with the epilogue's side data of our rows
+    for (int r = r0 + static_cast<int>(threadIdx.x) - 64; r < r1; r += THREADS - 64) epi.prefetch(r, nb * 128, M, N);
     if (lane == 0) ok = mbar_wait(&bars->tfull, 0, abort, err) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
+  }
+  // every rank's MMAs are done: the stage rings are free to receive partials
+  tc_fence_before();
+  cluster_barrier();
+  if (warp >= 2) {
     tc_fence_after();
-    const int r = q * 32 + lane;
+    const int q = warp & 3, f = q * 32 + lane;   // this thread's output column
+    const bool live = ok && has_k;
     float v[32];
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = 0; c < xrows / 32; ++c) {
       tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v);
-      float* dst = red + r * RED_LD + c * 32;
 #pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(dst + j) = (ok && has_k) ? make_float4(v[j], v[j + 1], v[j + 2], v[j + 3])
-                                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < 32; j += 4) {
+        const int r = c * 32 + j;   // four rows, never split between owners
+        if (r >= M) break;
+        const int owner = r / tpr, rr = r - owner * tpr;
+        const uint32_t la = smem_u32(recv + (rank * 128 + f) * ldr + rr);
+        uint32_t ra;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(owner));
+        const float4 x = live ? make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ra), "f"(x.x), "f"(x.y),
+                     "f"(x.z), "f"(x.w)
+                     : "memory");
+      }
     }
   }
   tc_fence_before();
-  cluster_barrier();
-  // rows [rank * RPC, (rank + 1) * RPC) of the tile: every thread sums float4
-  // column groups over the cluster's partials (rank order) into this CTA's own
-  // copy of those rows, which no other CTA reads
-  constexpr int RPC = BM / SPLITK, G4 = BN / 4;
-  const int row0 = rank * RPC;
-  for (int e = threadIdx.x; e < RPC * G4; e += THREADS) {
-    const int r = row0 + e / G4, c = (e % G4) * 4;
-    const uint32_t la = smem_u32(red + r * RED_LD + c);
-    float4 part[SPLITK];            // all remote loads in flight, then sum in rank order
-#pragma unroll
-    for (int p = 0; p < SPLITK; ++p) {
-      uint32_t ra;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(p));
-      asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                   : "=f"(part[p].x), "=f"(part[p].y), "=f"(part[p].z), "=f"(part[p].w)
-                   : "r"(ra)
-                   : "memory");
-    }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int p = 0; p < SPLITK; ++p) {
-      acc.x += part[p].x; acc.y += part[p].y; acc.z += part[p].z; acc.w += part[p].w;
-    }
-    partial_sum_store(red + r * RED_LD + c, acc);
-  }
-  __syncthreads();
-  if (threadIdx.x < RPC) {
-    const int r = row0 + threadIdx.x;
-    LocalRowLoader ld{red + r * RED_LD};
-    epi.run(mb * BM + r, nb * BN, BN / 32, M, N, ld);
-  }
-  cluster_barrier();
+  cluster_barrier();       // every partial has landed; no remote access follows
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, BN);
+    tmem_dealloc(tmem, 256);
+  }
+  // (row, piece) items, rows fastest so a warp reads consecutive rows
+  const int nrows = r1 - r0;
+  for (int it = threadIdx.x; it < nrows * Epi::PARTS; it += THREADS) {
+    const int rr = it % nrows, piece = it / nrows;
+    RecvSumLoader<SPLITK> ldr_{recv, ldr, rr};
+    epi.run_part(r0 + rr, nb * 128, piece, M, N, ldr_);
   }
 }
+
 }  // namespace tc
 
 namespace simt {

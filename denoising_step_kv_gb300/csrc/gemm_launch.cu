@@ -9,9 +9,6 @@ namespace dllm {
 namespace {
 
 
-// Rows at or below which a projection streams its weights (split-K path).
-constexpr int SMALL_M = 512;
-
 template <class Epi, int STAGES>
 cudaError_t launch_persistent(dllm_cache* c, const CUtensorMap& ta, const CUtensorMap& tb, int a_rows, int M_host,
                               const int* M_dev, int M_min, int N, int K, const Epi& epi, cudaStream_t st) {
@@ -61,21 +58,22 @@ cudaError_t launch_pair(dllm_cache* c, const CUtensorMap& ta, const CUtensorMap&
 }
 
 template <class Epi, int S>
-cudaError_t launch_splitk(dllm_cache* c, const CUtensorMap& ta, const CUtensorMap& tb, int a_rows, int M_host,
-                          const int* M_dev, int M_max, int N, int K, const Epi& epi, cudaStream_t st) {
+cudaError_t launch_skinny(dllm_cache* c, const void* A, int a_rows, int M_host, const int* M_dev, const void* W,
+                          int N, int K, const Epi& epi, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = set_smem(tc::gemm_splitk_kernel<Epi, S>, tc::SK_SMEM);
+    cudaError_t e = set_smem(tc::gemm_skinny_kernel<Epi, S>, tc::SKN_SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int m_rows = std::min(M_dev ? a_rows : M_host, M_max);
-  const int tiles = cdiv(m_rows, tc::BM) * cdiv(N, tc::BN);
-  if (tiles <= 0) return cudaSuccess;
+  CUtensorMap tw, tx;
+  if (!make_tmap_2d(&tw, W, K, N, static_cast<uint64_t>(K) * 2, tc::BK, 128, true) ||
+      !make_tmap_2d(&tx, A, K, a_rows, static_cast<uint64_t>(K) * 2, tc::BK, tc::SKN_XBOX, true))
+    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(tiles * S);
+  cfg.gridDim = dim3(cdiv(N, 128) * S);
   cfg.blockDim = dim3(tc::THREADS);
-  cfg.dynamicSmemBytes = tc::SK_SMEM;
+  cfg.dynamicSmemBytes = tc::SKN_SMEM;
   cfg.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -84,48 +82,92 @@ cudaError_t launch_splitk(dllm_cache* c, const CUtensorMap& ta, const CUtensorMa
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc::gemm_splitk_kernel<Epi, S>, ta, tb, M_host, M_dev, a_rows, M_max, N, K, epi,
+  return cudaLaunchKernelEx(&cfg, tc::gemm_skinny_kernel<Epi, S>, tw, tx, M_host, M_dev, a_rows, N, K, epi,
                             c->err);
 }
 
+// Clusters of the weight-streaming kernel (split s) that fit on the GPU at
+// once: clusters must sit inside one GPC, so this can be below num_sms / s.
+template <class Epi, int S>
+int skinny_resident(dllm_cache* c) {
+  static int n = -1;
+  if (n < 0) {
+    if (set_smem(tc::gemm_skinny_kernel<Epi, S>, tc::SKN_SMEM) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S * c->num_sms);
+    cfg.blockDim = dim3(tc::THREADS);
+    cfg.dynamicSmemBytes = tc::SKN_SMEM;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = S;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int k = 0;
+    if (cudaOccupancyMaxActiveClusters(&k, tc::gemm_skinny_kernel<Epi, S>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      k = 0;
+    }
+    n = k;
+  }
+  return n;
+}
+
+// Split of K for the weight-streaming kernel: the largest whose clusters
+// (one per 128 output columns) are all resident at once, 0 if none is.
+template <class Epi>
+int skinny_split(dllm_cache* c, int N) {
+  const int nN = cdiv(N, 128);
+  if (nN <= skinny_resident<Epi, 8>(c)) return 8;
+  if (nN <= skinny_resident<Epi, 6>(c)) return 6;
+  if (nN <= skinny_resident<Epi, 4>(c)) return 4;
+  if (nN <= skinny_resident<Epi, 3>(c)) return 3;
+  if (nN <= skinny_resident<Epi, 2>(c)) return 2;
+  if (nN <= skinny_resident<Epi, 1>(c)) return 1;
+  return 0;
+}
+
+template <class Epi>
+cudaError_t run_skinny(dllm_cache* c, int split, const void* A, int a_rows, int M_host, const int* M_dev,
+                       const void* W, int N, int K, const Epi& epi, cudaStream_t st) {
+  switch (split) {
+    case 8: return launch_skinny<Epi, 8>(c, A, a_rows, M_host, M_dev, W, N, K, epi, st);
+    case 6: return launch_skinny<Epi, 6>(c, A, a_rows, M_host, M_dev, W, N, K, epi, st);
+    case 4: return launch_skinny<Epi, 4>(c, A, a_rows, M_host, M_dev, W, N, K, epi, st);
+    case 3: return launch_skinny<Epi, 3>(c, A, a_rows, M_host, M_dev, W, N, K, epi, st);
+    case 2: return launch_skinny<Epi, 2>(c, A, a_rows, M_host, M_dev, W, N, K, epi, st);
+    default: return launch_skinny<Epi, 1>(c, A, a_rows, M_host, M_dev, W, N, K, epi, st);
+  }
+}
+
 // bf16 D = A . B^T with epilogue `epi`.  M is M_host, or the device count
-// M_dev (at most a_rows).  Small M streams the weights: a split-K cluster
-// kernel spreads them over enough CTAs to fill the GPU.  Large M is
-// tensor-bound: the multicast pair kernel (256-wide tiles; `wide_ok` says the
-// epilogue accepts them), else the persistent kernel.  With a device count
-// both sizes are launched and each one skips the other's range.
+// M_dev (at most a_rows).  Up to 256 rows the weights are streamed once by
+// the swapped-operand split-K kernel (when their 128-column tiles fit on the
+// SMs).  More rows are tensor-bound: the multicast pair kernel (256-wide
+// tiles; `wide_ok` says the epilogue accepts them), else the persistent
+// kernel.  With a device count both sizes are launched; each skips the
+// other's range.
 template <class Epi>
 cudaError_t run_tc(dllm_cache* c, const void* A, int a_rows, int M_host, const int* M_dev, const void* B, int N,
                    int K, const Epi& epi, cudaStream_t st, bool wide_ok = true) {
   if (!M_dev && M_host <= 0) return cudaSuccess;
+  const int split = skinny_split<Epi>(c, N);
+  const int m_rows = M_dev ? a_rows : M_host;     // most rows this call can see
+  cudaError_t e = cudaSuccess;
+  if (split > 0 && (M_dev || M_host <= tc::SKN_MAX_ROWS)) {
+    e = run_skinny(c, split, A, a_rows, M_host, M_dev, B, N, K, epi, st);
+    if (e != cudaSuccess || m_rows <= tc::SKN_MAX_ROWS) return e;
+  }
+  const int M_min = split > 0 ? tc::SKN_MAX_ROWS + 1 : 0;
   CUtensorMap ta, tb;
   if (!make_tmap_2d(&ta, A, K, a_rows, static_cast<uint64_t>(K) * 2, tc::BK, tc::BM, true) ||
       !make_tmap_2d(&tb, B, K, N, static_cast<uint64_t>(K) * 2, tc::BK, tc::BN, true))
     return cudaErrorInvalidValue;
-  const int nN = cdiv(N, tc::BN);
-  const int small_rows = std::min(M_dev ? a_rows : M_host, SMALL_M);
-  const int small_tiles = cdiv(small_rows, tc::BM) * nN;
-  const bool want_small = M_dev ? true : (M_host <= SMALL_M && small_tiles < c->num_sms);
-  const bool want_large = M_dev ? a_rows > SMALL_M : !want_small;
-  cudaError_t e = cudaSuccess;
-  if (want_small) {
-    const int ratio = cdiv(c->num_sms, std::max(1, small_tiles));
-    if (M_dev) e = launch_splitk<Epi, 2>(c, ta, tb, a_rows, M_host, M_dev, SMALL_M, N, K, epi, st);
-    else if (ratio >= 8) e = launch_splitk<Epi, 8>(c, ta, tb, a_rows, M_host, M_dev, SMALL_M, N, K, epi, st);
-    else if (ratio >= 4) e = launch_splitk<Epi, 4>(c, ta, tb, a_rows, M_host, M_dev, SMALL_M, N, K, epi, st);
-    else if (ratio >= 2) e = launch_splitk<Epi, 2>(c, ta, tb, a_rows, M_host, M_dev, SMALL_M, N, K, epi, st);
-    else e = launch_persistent<Epi, 3>(c, ta, tb, a_rows, M_host, M_dev, 0, N, K, epi, st);
-    if (e != cudaSuccess) return e;
-  }
-  if (want_large) {
-    const int M_min = M_dev ? SMALL_M + 1 : 0;
-    const int m_rows = M_dev ? a_rows : M_host;
-    if (m_rows <= 256) return launch_persistent<Epi, 3>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
-    if (wide_ok && N % tc::PBN == 0)
-      return launch_pair<Epi, 4>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
-    return launch_persistent<Epi, 4>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
-  }
-  return e;
+  if (m_rows <= 256) return launch_persistent<Epi, 3>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
+  if (wide_ok && N % tc::PBN == 0)
+    return launch_pair<Epi, 4>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
+  return launch_persistent<Epi, 4>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
 }
 
 template <int NCH, class Epi>
@@ -165,9 +207,12 @@ cudaError_t qkv_dh(dllm_cache* c, int layer, const void* A, int M_cap, const int
                    const void* w, cudaStream_t st) {
   const int d = c->d, N = 3 * d;
   const int M_host = M_dev ? 0 : M_cap;
-  if (c->cfg.dtype == DLLM_BF16)
-    return run_tc(c, A, M_cap, M_host, M_dev, w, N, d, make_qkv<bf16, DH>(c, layer, rows), st,
-                  d % tc::PBN == 0);   // a 256-wide tile stays inside q, k or v
+  if (c->cfg.dtype == DLLM_BF16) {
+    if constexpr (DH >= 64)    // bf16 caches have head_dim 64 or 128
+      return run_tc(c, A, M_cap, M_host, M_dev, w, N, d, make_qkv<bf16, DH>(c, layer, rows), st,
+                    d % tc::PBN == 0);   // a 256-wide tile stays inside q, k or v
+    return cudaErrorInvalidValue;
+  }
   if (d % 128 == 0) return run_simt<4>(A, M_cap, M_host, M_dev, w, N, d, make_qkv<float, DH>(c, layer, rows), st);
   if constexpr (DH <= 64)
     return run_simt<2>(A, M_cap, M_host, M_dev, w, N, d, make_qkv<float, DH>(c, layer, rows), st);

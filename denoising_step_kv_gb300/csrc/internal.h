@@ -32,7 +32,7 @@ struct dllm_cache {
   float* hist_p = nullptr;
   int* hist_n = nullptr;    // [B][blk]
   uint32_t* words = nullptr;// [B][Lw] refresh flags
-  float2* rope = nullptr;   // [max_pos][head_dim/2]
+  float2* rope = nullptr;   // [head_dim/2] RoPE frequencies as (hi, lo) float pairs
   unsigned* err = nullptr;  // device error word
   unsigned* ticket = nullptr; // arrival counter of the SWD kernel's blocks
   // scratch
@@ -96,6 +96,11 @@ int lm_tile_cols(const dllm_cache* c);
 // Queries: positions [q_pos0, q_pos0 + q_len) (ring slot in streaming mode)
 // of each of n_seq sequences; keys/values: positions [0, kv_len).  out:
 // [n_seq][q_len][d] in the cache dtype.
+// Queries = the sorted row list rows[0, *n_rows) (bf16 caches, batch <= 256).
+cudaError_t attn_rows_dense(dllm_cache* c, int layer, const int* rows, const int* n_rows, void* out,
+                            cudaStream_t st);
+cudaError_t launch_active_rows(dllm_cache* c, const void* src, const int* rows, const int* n_rows, int q_start,
+                               int q_len, void* dst, cudaStream_t st);
 cudaError_t attn_dense(dllm_cache* c, int layer, int q_pos0, int q_len, int kv_len, int n_seq, void* out,
                        cudaStream_t st);
 

@@ -299,7 +299,43 @@ __global__ void reset_kernel(int* version, int n_version, int* tok_w, uint8_t* s
   if (i0 == 0) *err = 0u;
 }
 
+// Active-block rows out of a compact row-list buffer: dst[b * q_len + j] =
+// src[i] for the i with rows[i] == b * L + q_start + j (binary search of the
+// sorted list; one warp per output row).  A row missing from the list sets
+// DLLM_ERR_ROW and its output row is zero-filled.
+__global__ void __launch_bounds__(256) active_rows_kernel(const uint4* __restrict__ src, const int* __restrict__ rows,
+                                                          const int* __restrict__ n_rows, int cap, int L,
+                                                          int q_start, int q_len, int n_out, int row_vec,
+                                                          uint4* __restrict__ dst, unsigned* err) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (w >= n_out) return;
+  const int b = w / q_len, j = w - b * q_len;
+  const int key = b * L + q_start + j;
+  const int n = min(*n_rows, cap);
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (rows[mid] < key) lo = mid + 1; else hi = mid;
+  }
+  const bool found = lo < n && rows[lo] == key;
+  if (!found && lane == 0) set_err(err, DLLM_ERR_ROW);
+  const uint4* s = src + static_cast<size_t>(found ? lo : 0) * row_vec;
+  uint4* o = dst + static_cast<size_t>(w) * row_vec;
+  for (int c = lane; c < row_vec; c += 32) o[c] = found ? s[c] : make_uint4(0u, 0u, 0u, 0u);
+}
+
 }  // namespace
+
+cudaError_t launch_active_rows(dllm_cache* c, const void* src, const int* rows, const int* n_rows, int q_start,
+                               int q_len, void* dst, cudaStream_t st) {
+  const int n_out = c->cfg.batch * q_len;
+  if (n_out <= 0) return cudaSuccess;
+  const int row_vec = c->d * c->elem / 16;
+  active_rows_kernel<<<cdiv(n_out * 32, 256), 256, 0, st>>>(static_cast<const uint4*>(src), rows, n_rows,
+                                                            c->seq_rows, c->cfg.seq_len, q_start, q_len, n_out,
+                                                            row_vec, static_cast<uint4*>(dst), c->err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gather(dllm_cache* c, int layer, const int* rows, const int* n_rows, int n_host, const void* x,
                           const int* tok, const void* embed, int t, cudaStream_t st) {

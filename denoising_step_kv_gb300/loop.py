@@ -9,6 +9,11 @@ One step of a single-layer denoiser is:
     lmhead_conf  argmax, top-1 probability, entropy of the active rows
     stab_update  SWD update, commits, next step's refresh set
 
+A multi-layer step runs the refresh rows through every layer (kv_refresh,
+block_attn_rows, attn_out, ffn_gelu per layer) before the LM head.  An
+attention-sink stream appends one token per step and attends over the sink
+and rolling entries.
+
 The refresh-set size stays on the device, so no step synchronises with the
 host and a whole generation can be captured as one CUDA graph.
 """
@@ -142,6 +147,87 @@ class DenseGenerator:
     def kernel_times_ms(self, kernel):
         """Per-step durations of `kernel` recorded by the last run/replay."""
         return [a.elapsed_time(b) for a, b in self.prof.get(kernel, [])]
+
+
+class LayerStackGenerator:
+    """Multi-layer cached denoiser (dense positional cache).
+
+    The rows P of the refresh set (sorted flat ids; the active block is part
+    of it) pass through every layer: their Q/K/V are re-projected into that
+    layer's cache, their queries attend over the layer's whole cache, then
+    W_o + residual and the FFN.  Every other row's deeper-layer K/V stays as
+    cached.  The LM head and the SWD update then run on the active rows.
+    Buffers are compact over P (row i = rows[i]); its size stays on the device.
+    """
+
+    def __init__(self, w, weights, device="cuda"):
+        assert not w.streaming and w.ffn
+        self.w = w
+        self.W = weights
+        B, L, d, blk = w.batch, w.seq_len, w.d_model, w.block_len
+        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        self.cache = K.dllm_cache_init(K.make_cfg(w))
+        i32 = dict(dtype=torch.int32, device=device)
+        self.tok = torch.zeros(B, L, **i32)
+        self.rows = torch.zeros(B * L, **i32)
+        self.n_rows = torch.zeros(1, **i32)
+        self.O = torch.zeros(B * L, d, dtype=dt, device=device)          # attention output of the rows
+        self.H = [torch.zeros(B * L, d, dtype=dt, device=device) for _ in range(2)]
+        self.o = torch.zeros(B * blk, d, dtype=dt, device=device)        # last layer, active rows
+        self.h = torch.zeros(B * blk, d, dtype=dt, device=device)
+        self.argmax = torch.zeros(B * blk, **i32)
+        self.p1 = torch.zeros(B * blk, dtype=torch.float32, device=device)
+        self.ent = torch.zeros(B * blk, dtype=torch.float32, device=device)
+        self.tok_in = torch.zeros(B, L, **i32)
+        self.graph = None
+
+    close = DenseGenerator.close
+    __del__ = DenseGenerator.__del__
+    schedule = DenseGenerator.schedule
+
+    def step(self, t, q0, s, stream=None):
+        w, c, W = self.w, self.cache, self.W
+        blk = w.block_len
+        if t == 0:
+            K.refresh_all(c, q0, self.rows, self.n_rows, stream)
+        x = None                       # layer 0: embeddings of the rows, gathered by kv_refresh
+        for l in range(w.n_layers):
+            K.kv_refresh(c, l, x, self.tok, W["embed"], W["w_qkv"][l], self.rows, self.n_rows, t, stream)
+            K.block_attn_rows(c, l, self.rows, self.n_rows, self.O, stream)
+            h = self.H[l % 2]
+            K.attn_out(c, self.O, W["w_o"][l], x, None, None, 0, 1, self.n_rows, h, stream)
+            K.ffn_gelu(c, h, W["w1"][l], W["w2"][l], w.ffn, 0, self.n_rows, h, stream)
+            x = h
+        K.active_rows(c, x, self.rows, self.n_rows, q0, blk, self.h, stream)
+        K.active_rows(c, self.O, self.rows, self.n_rows, q0, blk, self.o, stream)
+        K.lmhead_conf(c, self.h, W["w_lm"], w.batch * blk, w.vocab, w.d_model, w.mask_id, self.argmax,
+                      self.p1, self.ent, stream)
+        K.stab_update(c, self.argmax, self.p1, self.tok, q0, t, s == w.steps_per_block - 1, self.rows,
+                      self.n_rows, stream)
+
+    def run(self, stream=None, on_step=None, n_steps=None):
+        K.dllm_cache_reset(self.cache, stream)
+        self.tok.copy_(self.tok_in)
+        for t, q0, s in self.schedule():
+            if n_steps is not None and t >= n_steps:
+                break
+            self.step(t, q0, s, stream)
+            if on_step is not None:
+                on_step(t, q0, s)
+        return self.tok
+
+    def capture(self, n_steps=None):
+        self.run(n_steps=n_steps)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run(n_steps=n_steps)
+        self.graph = g
+        return g
+
+    def replay(self):
+        self.graph.replay()
+        return self.tok
 
 
 class StreamGenerator:

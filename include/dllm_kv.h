@@ -190,18 +190,37 @@ dllm_status kv_refresh(dllm_cache* c, int layer, const void* x_dev, const int32_
 dllm_status block_attn(dllm_cache* c, int layer, int q_start, int q_len, void* out_dev,
                        void* stream);
 
-/* Same attention for an explicit query row list (multi-layer denoiser: the
-   rows that pass through the layers): queries q_rows_dev[0 .. *n_q_dev),
-   out_dev [n][d] compact. */
+/* Same attention for an explicit query row list (the multi-layer denoiser's
+   rows that pass through every layer, [LaCache] "Inference workflow"; the
+   queries are the refreshed rows, so the Q cache holds them):
+   q_rows_dev[0 .. *n_q_dev) flat rows b * L + pos in ascending order (as
+   stab_update and refresh_all write them), device int32; each query attends
+   over all L positions of its own sequence in layer `layer`.
+   out_dev [n][d] bf16, row i = query q_rows_dev[i], caller-owned.
+   bf16 caches and batch <= 256 only (EUNSUPPORTED otherwise); rows outside
+   [0, B*L) are skipped.  Asynchronous on `stream`. */
 dllm_status block_attn_rows(dllm_cache* c, int layer, const int32_t* q_rows_dev,
                             const int32_t* n_q_dev, void* out_dev, void* stream);
+
+/* The active block's rows out of a compact row-list buffer (no counterpart
+   on the pages; plumbing of the multi-layer step): dst_dev[b * q_len + j] =
+   src_dev[i] for the i with rows_dev[i] == b * L + q_start + j, for
+   b < batch, j < q_len.  src_dev [*n_rows_dev][d] and dst_dev [B*q_len][d]
+   in the cache dtype, caller-owned, 16-byte aligned; rows_dev sorted
+   ascending.  A row missing from the list sets DLLM_ERR_ROW and its output
+   row is zero.  Asynchronous on `stream`. */
+dllm_status active_rows(dllm_cache* c, const void* src_dev, const int32_t* rows_dev,
+                        const int32_t* n_rows_dev, int q_start, int q_len, void* dst_dev,
+                        void* stream);
 
 /* Residual stream after attention: h_dev[i] = x_i + o_dev[i] . W_o^T for
    i < M (M = B * q_len rows, row i = sequence i / q_len, position
    q_start + i % q_len), W_o [d][d] row-major.  x_i = x_res_dev[i] if given,
    else embed_dev[tok_dev[b * L + q_start + i % q_len]].
    m_dev (device int32, may be NULL) overrides M with a device count (at most
-   B*L; o_dev, x_res_dev and h_dev then hold B*L rows). */
+   B*L; o_dev, x_res_dev and h_dev then hold B*L rows).  With m_dev and no
+   x_res_dev, x_i is row i of the layer-0 input the last kv_refresh gathered
+   (the embeddings of its row list, compact). */
 dllm_status attn_out(dllm_cache* c, const void* o_dev, const void* w_o_dev, const void* x_res_dev,
                      const int32_t* tok_dev, const void* embed_dev, int q_start, int q_len,
                      const int32_t* m_dev, void* h_dev, void* stream);

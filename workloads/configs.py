@@ -126,7 +126,9 @@ MID_MULTI = Workload(
     vocab=1000, ffn=512, swd_K=3, swd_tau=0.9, swd_R=2, expiry=2, seed=14,
     refresh_active=1)
 
-# More rows than the weight-streaming path takes (512): the projection runs
+MID_MULTI_SHARP = replace(MID_MULTI, name="mid_multi_sharp", lm_scale=40.0, steps_per_block=10, seed=18)
+
+# More rows than the weight-streaming path takes (256): the projection runs
 # on the large-M kernels.  600 rows = 5 row tiles (an odd count: the last
 # cluster pair has a half past the end), 900 rows = 7 tiles + 4 rows.
 BIG_ROWS = replace(MID_BF16, name="big_rows", batch=2, seq_len=300, n_prompt=268, seed=16)
@@ -134,7 +136,7 @@ BIG_ROWS_DH64 = replace(MID_BF16_DH64, name="big_rows_dh64", batch=3, seq_len=30
 
 ALL = dict(NAMED)
 for _w in (MID_BF16, MID_BF16_DH64, TINY_FP32_SHARP, MID_BF16_SHARP, MID_SINK, TINY_SINK_F32, MID_MULTI,
-           BIG_ROWS, BIG_ROWS_DH64):
+           MID_MULTI_SHARP, BIG_ROWS, BIG_ROWS_DH64):
     ALL[_w.name] = _w
 
 
