@@ -67,6 +67,15 @@ def close_rows(a, b, rtol=BF16_RTOL):
     return bool(np.all(np.max(np.abs(a - b), axis=1) <= rtol * np.maximum(np.max(np.abs(b), axis=1), 1e-30)))
 
 
+def worst(a, b, w):
+    """(count over tolerance, got, want) at the element farthest past it."""
+    rtol, atol = tol(w)
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    ex = np.abs(a - b) - (atol + rtol * np.abs(b))
+    i = np.unravel_index(np.argmax(ex), ex.shape)
+    return int(np.sum(ex > 0)), float(a[i]), float(b[i]), tuple(int(x) for x in i)
+
+
 def max_err(a, b):
     return float(np.max(np.abs(np.asarray(a) - np.asarray(b)))) if np.size(a) else 0.0
 
