@@ -67,21 +67,9 @@ cudaError_t launch_tc_r(dllm_cache* c, const uint8_t* Ql, const uint8_t* Kl, con
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_split, H, n_seq);
-  cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = S::SMEM;
-  cfg.stream = st;
-  cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = n_split;
-  attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = 1;
-  cfg.attrs = attrs;
-  cfg.numAttrs = 1;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(DH));
-  return cudaLaunchKernelEx(&cfg, attn_tc::attn_tc_kernel<DH, R>, Ql, Kl, Vl, c->kv, c->d, q_pos0, q_len, kv_len,
-                            keys_per_split, scale_log2, out, c->err);
+  return launch_ex(attn_tc::attn_tc_kernel<DH, R>, dim3(n_split, H, n_seq), dim3(192), S::SMEM, st, n_split, Ql, Kl,
+                   Vl, c->kv, c->d, q_pos0, q_len, kv_len, keys_per_split, scale_log2, out, c->err);
 }
 
 // Replicas R of the queries in the 128 MMA rows: as many as fit.
@@ -106,10 +94,8 @@ cudaError_t launch_rows(dllm_cache* c, const uint8_t* Ql, const uint8_t* Kl, con
     attr = true;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(DH));
-  attn_rows::attn_rows_kernel<DH><<<c->num_sms, 192, S::SMEM, st>>>(
-      Ql, Kl, Vl, c->kv, c->cfg.seq_len, c->cfg.batch, c->cfg.n_heads, rows, n_rows, c->seq_rows, scale_log2, out,
-      c->err);
-  return cudaGetLastError();
+  return launch_ex(attn_rows::attn_rows_kernel<DH>, dim3(c->num_sms), dim3(192), S::SMEM, st, 0, Ql, Kl, Vl, c->kv,
+                   c->cfg.seq_len, c->cfg.batch, c->cfg.n_heads, rows, n_rows, c->seq_rows, scale_log2, out, c->err);
 }
 
 cudaError_t attn_rows_dense(dllm_cache* c, int layer, const int* rows, const int* n_rows, void* out,

@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(192, 1)
   int* first_item = reinterpret_cast<int*>(sm + S::OFF_SEQ);   // [n_seq + 1], in (b, tile) units
   int* row_start = first_item + MAX_SEQ + 1;                     // [n_seq + 1]
   volatile int* abort = &bars->abort;
+  pdl_launch();
+  pdl_wait();
   const int n = min(*n_rows, rows_cap);
   const int n_tiles = cdiv(L, KT);
 

@@ -199,6 +199,8 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
+  pdl_launch();
+  pdl_wait();     // the cache rows of this step are written by the projection
 
   // per-row results of the softmax warps (kept for the merge)
   float m_ref = -INFINITY, l_sum = 0.f;

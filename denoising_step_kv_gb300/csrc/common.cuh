@@ -94,6 +94,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // lets the kernel wind down instead of hanging the GPU.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 
+// ---------------------------------------------------------------- launch overlap
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while its predecessor on the stream is finishing:
+// it sets up shared memory, barriers and TMEM, then pdl_wait() blocks until
+// the predecessor has completed and its writes are visible (a no-op for a
+// kernel launched without the attribute).  pdl_launch() lets the successor
+// start once every CTA of this grid has issued it or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -65,10 +65,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + STAGES * STAGE_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int M = M_dev ? min(*M_dev, M_cap) : M_host;   // never past A's rows
-  const int nM = (M + BM - 1) / BM, nN = (N + BN - 1) / BN, nK = (K + BK - 1) / BK;
-  // M below M_min belongs to the split-K kernel launched beside this one
-  const int tiles = (M > 0 && M >= M_min) ? nM * nN : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -84,16 +80,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(&bars->tmem, TMEM_COLS);
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
   volatile int* abort = &bars->abort;
+  pdl_launch();
+  pdl_wait();
+  const int M = M_dev ? min(*M_dev, M_cap) : M_host;   // never past A's rows
+  const int nM = (M + BM - 1) / BM, nN = (N + BN - 1) / BN, nK = (K + BK - 1) / BK;
+  // M below M_min belongs to the kernel launched beside this one
+  const int tiles = (M > 0 && M >= M_min) ? nM * nN : 0;
 
   if (warp == 0) {
     if (lane == 0) {
-      prefetch_tmap(&tmA);
-      prefetch_tmap(&tmB);
       int stage = 0;
       uint32_t phase = 0, issued = 0, par = 0;
       for (int tile = blockIdx.x; tile < tiles && !*abort; tile += gridDim.x) {
@@ -214,10 +218,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = static_cast<int>(cluster_rank());
-  const int M = M_dev ? min(*M_dev, M_cap) : M_host;
-  const int nM = (M + BM - 1) / BM, nMP = (nM + 1) / 2, nN = (N + PBN - 1) / PBN, nK = (K + BK - 1) / BK;
-  // the same in both CTAs of a cluster: both run the same tiles and k-blocks
-  const int tiles = (M > 0 && M >= M_min) ? nMP * nN : 0;
   const int cl = blockIdx.x >> 1, n_cl = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
@@ -234,17 +234,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(&bars->tmem, PTMEM_COLS);
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
   tc_fence_before();
   __syncthreads();
   cluster_barrier();       // the peer's barriers exist before any multicast lands
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
   volatile int* abort = &bars->abort;
+  pdl_launch();
+  pdl_wait();
+  const int M = M_dev ? min(*M_dev, M_cap) : M_host;
+  const int nM = (M + BM - 1) / BM, nMP = (nM + 1) / 2, nN = (N + PBN - 1) / PBN, nK = (K + BK - 1) / BK;
+  // the same in both CTAs of a cluster: both run the same tiles and k-blocks
+  const int tiles = (M > 0 && M >= M_min) ? nMP * nN : 0;
 
   if (warp == 0) {
     if (lane == 0) {
-      prefetch_tmap(&tmA);
-      prefetch_tmap(&tmB);
       int stage = 0;
       uint32_t phase = 0, issued = 0, par = 0;
       for (int tile = cl; tile < tiles && !*abort; tile += n_cl) {
@@ -407,6 +415,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   float* recv = reinterpret_cast<float*>(smem);    // [SPLITK][128][ldr], after the mainloop
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch();
+  pdl_wait();
   const int M = M_dev ? min(*M_dev, M_cap) : M_host;
   // the same decision in every CTA of the cluster
   if (M <= 0 || M > SKN_MAX_ROWS) return;

@@ -23,9 +23,8 @@ cudaError_t launch_persistent(dllm_cache* c, const CUtensorMap& ta, const CUtens
   const int tiles = cdiv(m_rows, tc::BM) * cdiv(N, tc::BN);
   const int per_sm = STAGES <= 3 ? 2 : 1;
   const int grid = std::max(1, std::min(tiles, per_sm * c->num_sms));
-  tc::gemm_tc_kernel<Epi, STAGES><<<grid, tc::THREADS, smem, st>>>(ta, tb, M_host, M_dev, a_rows, M_min, N, K, epi,
-                                                                   c->err);
-  return cudaGetLastError();
+  return launch_ex(tc::gemm_tc_kernel<Epi, STAGES>, dim3(grid), dim3(tc::THREADS), smem, st, 0, ta, tb, M_host, M_dev,
+                   a_rows, M_min, N, K, epi, c->err);
 }
 
 template <class Epi, int STAGES>
@@ -41,20 +40,8 @@ cudaError_t launch_pair(dllm_cache* c, const CUtensorMap& ta, const CUtensorMap&
   const int m_rows = M_dev ? a_rows : M_host;
   const int pairs = cdiv(cdiv(m_rows, tc::BM), 2) * cdiv(N, tc::PBN);
   const int clusters = std::max(1, std::min(pairs, c->num_sms / 2));
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * clusters);
-  cfg.blockDim = dim3(tc::THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc::gemm_pair_kernel<Epi, STAGES>, ta, tb, M_host, M_dev, a_rows, M_min, N, K,
-                            epi, c->err);
+  return launch_ex(tc::gemm_pair_kernel<Epi, STAGES>, dim3(2 * clusters), dim3(tc::THREADS), smem, st, 2, ta, tb,
+                   M_host, M_dev, a_rows, M_min, N, K, epi, c->err);
 }
 
 template <class Epi, int S>
@@ -70,20 +57,8 @@ cudaError_t launch_skinny(dllm_cache* c, const void* A, int a_rows, int M_host, 
   if (!make_tmap_2d(&tw, W, K, N, static_cast<uint64_t>(K) * 2, tc::BK, 128, true) ||
       !make_tmap_2d(&tx, A, K, a_rows, static_cast<uint64_t>(K) * 2, tc::BK, tc::SKN_XBOX, true))
     return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cdiv(N, 128) * S);
-  cfg.blockDim = dim3(tc::THREADS);
-  cfg.dynamicSmemBytes = tc::SKN_SMEM;
-  cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = S;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc::gemm_skinny_kernel<Epi, S>, tw, tx, M_host, M_dev, a_rows, N, K, epi,
-                            c->err);
+  return launch_ex(tc::gemm_skinny_kernel<Epi, S>, dim3(cdiv(N, 128) * S), dim3(tc::THREADS), tc::SKN_SMEM, st, S, tw,
+                   tx, M_host, M_dev, a_rows, N, K, epi, c->err);
 }
 
 // Clusters of the weight-streaming kernel (split s) that fit on the GPU at

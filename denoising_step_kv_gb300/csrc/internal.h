@@ -1,5 +1,6 @@
 // Host-side internals shared by the translation units of libdllmkv.
 #pragma once
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -96,6 +97,35 @@ int lm_tile_cols(const dllm_cache* c);
 // Queries: positions [q_pos0, q_pos0 + q_len) (ring slot in streaming mode)
 // of each of n_seq sequences; keys/values: positions [0, kv_len).  out:
 // [n_seq][q_len][d] in the cache dtype.
+// Launch `kernel` with programmatic stream serialisation (it may start while
+// its predecessor on `st` finishes; it calls pdl_wait() before touching
+// anything earlier work writes) and, if cluster > 0, clusters of that size
+// along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster,
+                      Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  int n = 0;
+  at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 0) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Queries = the sorted row list rows[0, *n_rows) (bf16 caches, batch <= 256).
 cudaError_t attn_rows_dense(dllm_cache* c, int layer, const int* rows, const int* n_rows, void* out,
                             cudaStream_t st);

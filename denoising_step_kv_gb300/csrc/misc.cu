@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const int* __restrict__ row
                                                      unsigned* err) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * 8 + warp;
+  pdl_launch();
+  pdl_wait();
   int n = n_rows ? *n_rows : n_host;
   if (n > x_cap) {          // more rows than the compact buffers hold
     if (i == 0 && lane == 0) set_err(err, DLLM_ERR_ROW);
@@ -95,6 +97,8 @@ __global__ void __launch_bounds__(256) rownorm_kernel(const T* __restrict__ h, i
                                                       float eps, float* __restrict__ rs) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * 8 + warp;
+  pdl_launch();
+  pdl_wait();
   const int M = M_dev ? *M_dev : M_host;
   if (i >= M) return;
   constexpr int VN = Vec<T>::N, U = 8;
@@ -125,6 +129,8 @@ __global__ void __launch_bounds__(MERGE_THREADS) lm_merge_kernel(const LMPart* _
   __shared__ float s_m[MERGE_THREADS / 32], s_s[MERGE_THREADS / 32], s_a[MERGE_THREADS / 32];
   __shared__ int s_i[MERGE_THREADS / 32];
   const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_launch();
+  pdl_wait();
   if (i >= M) return;
   float m = -INFINITY, s = 0.f, a = 0.f;
   int idx = 0x7fffffff;
@@ -166,6 +172,8 @@ __global__ void __launch_bounds__(1024) swd_kernel(
   __shared__ uint8_t s_unst[64];
   __shared__ int s_last;
   const int b = blockIdx.x;
+  pdl_launch();
+  pdl_wait();
   const int nac = min(blk, L - q0);
   if (threadIdx.x < nac) {
     const int j = threadIdx.x;
@@ -308,6 +316,8 @@ __global__ void __launch_bounds__(256) active_rows_kernel(const uint4* __restric
                                                           int q_start, int q_len, int n_out, int row_vec,
                                                           uint4* __restrict__ dst, unsigned* err) {
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  pdl_launch();
+  pdl_wait();
   if (w >= n_out) return;
   const int b = w / q_len, j = w - b * q_len;
   const int key = b * L + q_start + j;
@@ -331,10 +341,9 @@ cudaError_t launch_active_rows(dllm_cache* c, const void* src, const int* rows, 
   const int n_out = c->cfg.batch * q_len;
   if (n_out <= 0) return cudaSuccess;
   const int row_vec = c->d * c->elem / 16;
-  active_rows_kernel<<<cdiv(n_out * 32, 256), 256, 0, st>>>(static_cast<const uint4*>(src), rows, n_rows,
-                                                            c->seq_rows, c->cfg.seq_len, q_start, q_len, n_out,
-                                                            row_vec, static_cast<uint4*>(dst), c->err);
-  return cudaGetLastError();
+  return launch_ex(active_rows_kernel, dim3(cdiv(n_out * 32, 256)), dim3(256), 0, st, 0,
+                   static_cast<const uint4*>(src), rows, n_rows, c->seq_rows, c->cfg.seq_len, q_start, q_len, n_out,
+                   row_vec, static_cast<uint4*>(dst), c->err);
 }
 
 cudaError_t launch_gather(dllm_cache* c, int layer, const int* rows, const int* n_rows, int n_host, const void* x,
@@ -345,45 +354,41 @@ cudaError_t launch_gather(dllm_cache* c, int layer, const int* rows, const int* 
   int* version = dense ? c->version + static_cast<size_t>(layer) * c->seq_rows : nullptr;
   int* tok_w = (dense && layer == 0 && !x) ? c->tok_w : nullptr;
   const dim3 grid(cdiv(cap, 8));
+  const int* nr = rows ? n_rows : nullptr;
+  const int streaming = dense ? 0 : 1;
   if (c->cfg.dtype == DLLM_BF16)
-    gather_kernel<bf16><<<grid, 256, 0, st>>>(rows, rows ? n_rows : nullptr, n_host, static_cast<const bf16*>(x),
-                                               tok, static_cast<const bf16*>(embed), static_cast<bf16*>(c->X), c->rs,
-                                               tok_w, version, t, c->d, c->rows, c->max_pos, !dense, c->cfg.vocab,
-                                               c->cfg.rms_eps, c->seq_rows, c->err);
-  else
-    gather_kernel<float><<<grid, 256, 0, st>>>(rows, rows ? n_rows : nullptr, n_host, static_cast<const float*>(x),
-                                                tok, static_cast<const float*>(embed), static_cast<float*>(c->X),
-                                                c->rs, tok_w, version, t, c->d, c->rows, c->max_pos, !dense,
-                                                c->cfg.vocab, c->cfg.rms_eps, c->seq_rows, c->err);
-  return cudaGetLastError();
+    return launch_ex(gather_kernel<bf16>, grid, dim3(256), 0, st, 0, rows, nr, n_host, static_cast<const bf16*>(x), tok,
+                     static_cast<const bf16*>(embed), static_cast<bf16*>(c->X), c->rs, tok_w, version, t, c->d,
+                     c->rows, c->max_pos, streaming, c->cfg.vocab, c->cfg.rms_eps, c->seq_rows, c->err);
+  return launch_ex(gather_kernel<float>, grid, dim3(256), 0, st, 0, rows, nr, n_host, static_cast<const float*>(x), tok,
+                   static_cast<const float*>(embed), static_cast<float*>(c->X), c->rs, tok_w, version, t, c->d,
+                   c->rows, c->max_pos, streaming, c->cfg.vocab, c->cfg.rms_eps, c->seq_rows, c->err);
 }
 
 cudaError_t launch_rownorm(dllm_cache* c, const void* h, int M, const int* M_dev, int d, float* rs,
                            cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
   if (c->cfg.dtype == DLLM_BF16)
-    rownorm_kernel<bf16><<<cdiv(M, 8), 256, 0, st>>>(static_cast<const bf16*>(h), M, M_dev, d, c->cfg.rms_eps, rs);
-  else
-    rownorm_kernel<float><<<cdiv(M, 8), 256, 0, st>>>(static_cast<const float*>(h), M, M_dev, d, c->cfg.rms_eps,
-                                                       rs);
-  return cudaGetLastError();
+    return launch_ex(rownorm_kernel<bf16>, dim3(cdiv(M, 8)), dim3(256), 0, st, 0, static_cast<const bf16*>(h), M, M_dev,
+                     d, c->cfg.rms_eps, rs);
+  return launch_ex(rownorm_kernel<float>, dim3(cdiv(M, 8)), dim3(256), 0, st, 0, static_cast<const float*>(h), M,
+                   M_dev, d, c->cfg.rms_eps, rs);
 }
 
 cudaError_t launch_lm_merge(const void* part, int M, int n_tiles, int* argmax, float* p1, float* ent,
                             cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
-  lm_merge_kernel<<<M, MERGE_THREADS, 0, st>>>(static_cast<const LMPart*>(part), M, n_tiles, argmax, p1, ent);
-  return cudaGetLastError();
+  return launch_ex(lm_merge_kernel, dim3(M), dim3(MERGE_THREADS), 0, st, 0, static_cast<const LMPart*>(part), M,
+                   n_tiles, argmax, p1, ent);
 }
 
 cudaError_t launch_stab(dllm_cache* c, const int* argmax, const float* p1, int* tok, int q_start, int t, int last,
                         int* rows, int* n_rows, cudaStream_t st) {
   const dllm_cache_cfg& g = c->cfg;
-  swd_kernel<<<g.batch, 1024, 0, st>>>(argmax, p1, tok, c->stable, c->hist_tok, c->hist_p, c->hist_n, c->tok_w,
-                                       c->version, c->words, g.seq_len, c->Lw, c->seq_rows, g.n_layers, g.block_len,
-                                       g.swd_K, g.swd_tau, g.swd_R, q_start, t, last, g.expiry, g.refresh_active,
-                                       c->ticket, rows, n_rows);
-  return cudaGetLastError();
+  return launch_ex(swd_kernel, dim3(g.batch), dim3(1024), 0, st, 0, argmax, p1, tok, c->stable, c->hist_tok, c->hist_p,
+                   c->hist_n, c->tok_w, c->version, c->words, g.seq_len, c->Lw, c->seq_rows, g.n_layers, g.block_len,
+                   g.swd_K, g.swd_tau, g.swd_R, q_start, t, last, g.expiry, g.refresh_active, c->ticket, rows,
+                   n_rows);
 }
 
 cudaError_t launch_refresh_all(dllm_cache* c, int q_start, int* rows, int* n_rows, cudaStream_t st) {
