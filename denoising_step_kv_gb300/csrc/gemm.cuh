@@ -350,6 +350,168 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// Shared-A kernel for few rows and many output columns (the LM head):
+// persistent clusters of CS CTAs on CS adjacent 128 x 128 tiles of the same
+// 128 rows.  Each CTA loads its own weight tile and a 128/CS-row piece of the
+// rows' tile, multicast into every CTA of the cluster, so the rows are read
+// once per cluster instead of once per CTA.  A stage is reloaded once all CS
+// CTAs' MMAs have read it (every commit arrives on all CS empty barriers).
+// The row count is a host value: before the grid dependency each CTA warms
+// L2 with its first weight tile, which no earlier kernel writes.
+template <int STAGES>
+constexpr size_t sharea_smem_bytes() { return 1024 + STAGES * STAGE_BYTES + sizeof(Bars); }
+
+template <class Epi, int STAGES, int CS>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_sharea_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M,
+                       int N, int K, Epi epi, unsigned* err) {
+  static_assert(CS == 2 || CS == 4, "the rows' tile splits into CS whole 8-row swizzle groups");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + STAGES * A_BYTES;
+  Bars* bars = reinterpret_cast<Bars*>(smem + STAGES * STAGE_BYTES);
+  constexpr uint16_t ALL = (1u << CS) - 1;
+  constexpr int PIECE = BM / CS;                  // rows of the shared tile each CTA loads
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_rank());
+  const int cl = blockIdx.x / CS, n_cl = gridDim.x / CS;
+  const int nM = (M + BM - 1) / BM, nN = (N + BN - 1) / BN, nK = (K + BK - 1) / BK;
+  const int nG = (nN + CS - 1) / CS;
+  const int tiles = M > 0 ? nM * nG : 0;          // cluster tiles (row tile, group of CS column tiles)
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], CS);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bars->tfull[a], 1);
+      mbar_init(&bars->tempty[a], 4);
+    }
+    mbar_init(&bars->done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&bars->tmem, TMEM_COLS);
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    if (cl < tiles) {
+      const int nb = (cl / nM) * CS + rank;
+      if (nb < nN)
+        for (int kb = 0; kb < nK; ++kb) tma_prefetch_l2_2d(&tmB, kb * BK, nb * BN);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier();       // every CTA's barriers exist before any multicast lands
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  volatile int* abort = &bars->abort;
+  pdl_launch();
+  pdl_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, par = 0;
+      for (int tile = cl; tile < tiles && !*abort; tile += n_cl) {
+        const int mb = tile % nM, nb = (tile / nM) * CS + rank;
+        for (int kb = 0; kb < nK; ++kb) {
+          if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort, err)) break;
+          mbar_expect_tx(&bars->full[stage], STAGE_BYTES);
+          tma_load_2d_mc(sa + stage * A_BYTES + rank * (PIECE * 128), &tmA, kb * BK, mb * BM + rank * PIECE,
+                         &bars->full[stage], ALL);
+          tma_load_2d(sb + stage * B_BYTES, &tmB, kb * BK, nb * BN, &bars->full[stage]);
+          issued |= 1u << stage;
+          par = (par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*abort) {
+        for (int s = 0; s < STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait(&bars->full[s], (par >> s) & 1u, nullptr, err);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(BM, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      for (int tile = cl; tile < tiles && !*abort; tile += n_cl) {
+        if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1u, abort, err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nK; ++kb) {
+          if (!mbar_wait(&bars->full[stage], phase, abort, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sa + stage * A_BYTES), b0 = smem_u32(sb + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma_bf16(d_tmem, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc,
+                        (kb | k) != 0 ? 1u : 0u);
+          tc_commit_mc(&bars->empty[stage], ALL);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&bars->tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // every MMA and the empty-barrier arrivals it owes the peers complete
+      // before the cluster barrier below
+      tc_commit(&bars->done);
+      mbar_wait(&bars->done, 0, nullptr, err);
+    }
+  } else {
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = cl; tile < tiles; tile += n_cl) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&bars->tfull[acc], acc_phase, abort, err) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const int mb = tile % nM, nb = (tile / nM) * CS + rank;
+      if (nb < nN) {   // the last group may run past the columns
+        const int m = mb * BM + q * 32 + lane;
+        TmemLoader ld{tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN)};
+        epi.run(m, nb * BN, BN / 32, M, N, ld);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier();       // no multicast copy or commit still targets this CTA
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
 // Weight-streaming GEMM for small M (at most 256 rows): D^T = B . A^T.  The
 // weights B [N][K] are the MMA's A operand (128 output columns per CTA, on
 // the TMEM lanes) and the rows A [M][K] its B operand (M rounded up to 16, on

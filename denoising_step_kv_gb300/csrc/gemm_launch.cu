@@ -44,6 +44,26 @@ cudaError_t launch_pair(dllm_cache* c, const CUtensorMap& ta, const CUtensorMap&
                    M_host, M_dev, a_rows, M_min, N, K, epi, c->err);
 }
 
+template <class Epi, int STAGES, int CS>
+cudaError_t launch_sharea(dllm_cache* c, const void* A, int M, const void* B, int N, int K, const Epi& epi,
+                          cudaStream_t st) {
+  constexpr size_t smem = tc::sharea_smem_bytes<STAGES>();
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(tc::gemm_sharea_kernel<Epi, STAGES, CS>, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  CUtensorMap ta, tb;
+  if (!make_tmap_2d(&ta, A, K, M, static_cast<uint64_t>(K) * 2, tc::BK, tc::BM / CS, true) ||
+      !make_tmap_2d(&tb, B, K, N, static_cast<uint64_t>(K) * 2, tc::BK, tc::BN, true))
+    return cudaErrorInvalidValue;
+  const int tiles = cdiv(M, tc::BM) * cdiv(cdiv(N, tc::BN), CS);
+  const int clusters = std::max(1, std::min(tiles, 2 * c->num_sms / CS));
+  return launch_ex(tc::gemm_sharea_kernel<Epi, STAGES, CS>, dim3(CS * clusters), dim3(tc::THREADS), smem, st, CS, ta,
+                   tb, M, N, K, epi, c->err);
+}
+
 template <class Epi, int S>
 cudaError_t launch_skinny(dllm_cache* c, const void* A, int a_rows, int M_host, const int* M_dev, const void* W,
                           int N, int K, const Epi& epi, cudaStream_t st) {
@@ -239,7 +259,11 @@ cudaError_t gemm_gelu(dllm_cache* c, const void* A, const void* W, int M, int M_
 cudaError_t gemm_lm(dllm_cache* c, const void* A, const void* W, int M, int V, int d, const float* rs,
                     int mask_id, void* part, int n_tiles, cudaStream_t st) {
   EpiLM e{rs, mask_id, static_cast<LMPart*>(part), n_tiles};
-  if (c->cfg.dtype == DLLM_BF16) return run_tc(c, A, M, M, nullptr, W, V, d, e, st);
+  if (c->cfg.dtype == DLLM_BF16) {
+    // many vocab tiles: clusters of 4 share the rows' tile (two CTAs per SM)
+    if (M > 0 && cdiv(V, tc::BN) >= 8) return launch_sharea<EpiLM, 3, 4>(c, A, M, W, V, d, e, st);
+    return run_tc(c, A, M, M, nullptr, W, V, d, e, st);
+  }
   return run_simt<4>(A, M, M, nullptr, W, V, d, e, st);
 }
 

@@ -243,6 +243,37 @@ def test_lmhead_conf(name):
         K.dllm_cache_free(c)
 
 
+@pytest.mark.parametrize("V,M", [(1640, 32), (1640, 200), (4100, 256), (9, 5)])
+def test_lmhead_conf_vocab_groups(V, M):
+    """Vocab sizes whose 128-column tiles do not fill the last cluster group
+    (13 tiles in groups of 4), more than one 128-row tile, and a vocab below
+    one group (the plain persistent kernel)."""
+    from dataclasses import replace
+    w = replace(C.get("mid_bf16"), vocab=V, batch=1, block_len=min(64, M), seq_len=max(160, M))
+    c = K.dllm_cache_init(K.make_cfg(w))
+    try:
+        h = G.normal(43, (M, w.d_model), 1.0, "bf16")
+        wl = G.normal(44, (V, w.d_model), 0.8, "bf16")
+        am = torch.zeros(M, dtype=torch.int32, device="cuda")
+        p1 = torch.zeros(M, dtype=torch.float32, device="cuda")
+        ent = torch.zeros(M, dtype=torch.float32, device="cuda")
+        out = K.lmhead_conf_noalloc if M > w.batch * w.block_len else None
+        if out is None:
+            K.lmhead_conf(c, to_device(h), to_device(wl), M, V, w.d_model, 0, am, p1, ent, None)
+        else:
+            K.lmhead_conf_noalloc(to_device(h), to_device(wl), M, V, w.d_model, K.DLLM_BF16, 0, 1e-6, am, p1, ent)
+        assert K.dllm_cache_check(c) == 0
+        torch.cuda.synchronize()
+        a_o, p_o, e_o, margin = O.lm_head_conf(O.bf16_bits_to_f64(h), O.bf16_bits_to_f64(wl), 0)
+        ok = margin > 1e-2
+        assert np.array_equal(am.cpu().numpy()[ok], a_o[ok])
+        rtol, atol = tol(w)
+        assert np.allclose(p1.cpu().numpy(), p_o, rtol=rtol, atol=atol), max_err(p1.cpu().numpy(), p_o)
+        assert np.allclose(ent.cpu().numpy(), e_o, rtol=rtol, atol=atol), max_err(ent.cpu().numpy(), e_o)
+    finally:
+        K.dllm_cache_free(c)
+
+
 def _ring_to_lists(ht, hp, hn, K_):
     """Device ring (slot n % K) -> oracle per-position lists, oldest first."""
     toks, ps = [], []
