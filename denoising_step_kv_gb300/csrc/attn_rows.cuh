@@ -130,18 +130,23 @@ __global__ void __launch_bounds__(192, 1)
   };
 
   if (warp == 0) {
-    if (lane < 2) {
-      const uint8_t* src = lane == 0 ? Kl : Vl;
-      const int slots = lane == 0 ? KS : VS;
-      uint64_t* fullb = lane == 0 ? bars->k_full : bars->v_full;
-      uint64_t* emptyb = lane == 0 ? bars->k_empty : bars->v_empty;
-      uint8_t* ring = sm + (lane == 0 ? S::OFF_K : S::OFF_V);
+    // lanes 0/2 stream K, lanes 1/3 V (even and odd tiles of the CTA's
+    // running tile count J: two issuers per ring)
+    if (lane < 4) {
+      const bool is_k = (lane & 1) == 0;
+      const int sub = lane >> 1;
+      const uint8_t* src = is_k ? Kl : Vl;
+      const int slots = is_k ? KS : VS;
+      uint64_t* fullb = is_k ? bars->k_full : bars->v_full;
+      uint64_t* emptyb = is_k ? bars->k_empty : bars->v_empty;
+      uint8_t* ring = sm + (is_k ? S::OFF_K : S::OFF_V);
       uint32_t issued = 0, par = 0;
       int J = 0;   // tile counter over all items of this CTA
       for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
         int b, qt, h;
         decode(item, b, qt, h);
         for (int j = 0; j < n_tiles; ++j, ++J) {
+          if ((J & 1) != sub) continue;
           const int s = J % slots;
           const uint32_t ph = (J / slots) & 1u;
           if (!mbar_wait(&emptyb[s], ph ^ 1u, abort, err)) break;

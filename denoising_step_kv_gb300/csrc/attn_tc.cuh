@@ -1,8 +1,8 @@
 // Cached attention on the 5th-generation tensor cores (bf16).
 //
 // One CTA = (key split, head, sequence); clusters of n_split CTAs along the
-// key splits.  Two lanes of warp 0 stream 64-key K and V tiles through
-// separate rings with one bulk copy each (the cache stores every tile as the
+// key splits.  Four lanes of warp 0 stream 64-key K and V tiles through
+// separate rings (two issuers per ring) with one bulk copy each (the cache stores every tile as the
 // 128-byte-swizzled image the tensor cores read; K is released once S_j is
 // done, V once P_j V_j is done).  One thread of warp 1 issues
 //   S_j = Q K_j^T            M = 128 query rows, N = 64 keys, into one of two
@@ -206,16 +206,19 @@ __global__ void __launch_bounds__(192, 1)
   float m_ref = -INFINITY, l_sum = 0.f;
 
   if (warp == 0) {
-    // lane 0 streams K tiles, lane 1 streams V tiles (independent rings); a
-    // tile of the tiled cache is one contiguous bulk copy
-    if (lane < 2) {
-      const uint8_t* src = lane == 0 ? Kl : Vl;
-      const int slots = lane == 0 ? KS : VS;
-      uint64_t* fullb = lane == 0 ? bars->k_full : bars->v_full;
-      uint64_t* emptyb = lane == 0 ? bars->k_empty : bars->v_empty;
-      uint8_t* ring = sm + (lane == 0 ? S::OFF_K : S::OFF_V);
+    // lanes 0 and 2 stream K tiles, lanes 1 and 3 V tiles (independent rings,
+    // even and odd tiles: bulk copies from one thread are served one after
+    // another, so two issuers per ring keep twice the copies moving); a tile
+    // of the tiled cache is one contiguous bulk copy
+    if (lane < 4) {
+      const bool is_k = (lane & 1) == 0;
+      const uint8_t* src = is_k ? Kl : Vl;
+      const int slots = is_k ? KS : VS;
+      uint64_t* fullb = is_k ? bars->k_full : bars->v_full;
+      uint64_t* emptyb = is_k ? bars->k_empty : bars->v_empty;
+      uint8_t* ring = sm + (is_k ? S::OFF_K : S::OFF_V);
       uint32_t issued = 0, par = 0;
-      for (int j = 0; j < n_tiles; ++j) {
+      for (int j = lane >> 1; j < n_tiles; j += 2) {
         const int s = j % slots;
         const uint32_t ph = (j / slots) & 1u;
         if (!mbar_wait(&emptyb[s], ph ^ 1u, abort, err)) break;
@@ -233,10 +236,21 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t id_s = idesc_bf16(QROWS, KT);
       const uint32_t id_pv = idesc_bf16_bmn(QROWS, 64);
       const uint32_t q_base = smem_u32(sm + S::OFF_Q);
-      auto pv = [&](int i) -> bool {
+      // S_j = Q K_j^T into TMEM S buffer j & 1
+      auto issue_s = [&](int j) {
+        const int ks = j % KS, sb = j & 1;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(sm + S::OFF_K + ks * S::KV_TILE);
+#pragma unroll
+        for (int kc = 0; kc < DH / 16; ++kc)
+          tc_mma_bf16(tmem + S::S_COL + sb * KT, sdesc_sw128(q_base + (kc >> 2) * (QROWS * 128) + (kc & 3) * 32),
+                      sdesc_sw128(kb + (kc >> 2) * (KT * 128) + (kc & 3) * 32), id_s, kc > 0 ? 1u : 0u);
+        tc_commit(&bars->s_full[sb]);
+        tc_commit(&bars->k_empty[ks]);
+      };
+      // O += P_i,hi V_i + P_i,lo V_i
+      auto issue_pv = [&](int i) {
         const int pb = i & 1, vs = i % VS;
-        if (!mbar_wait(&bars->p_full[pb], (i >> 1) & 1u, abort, err)) return false;
-        if (!mbar_wait(&bars->v_full[vs], (i / VS) & 1u, abort, err)) return false;
         tc_fence_after();
         const uint32_t vb = smem_u32(sm + S::OFF_V + vs * S::KV_TILE);
 #pragma unroll
@@ -253,24 +267,41 @@ __global__ void __launch_bounds__(192, 1)
         }
         tc_commit(&bars->pv_done[pb]);
         tc_commit(&bars->v_empty[vs]);
-        return true;
       };
+      // issue whichever MMA is ready: S of the next tile once its K tile and
+      // S buffer are there, P V as soon as the softmax has written P (so the
+      // V slot is released without waiting for the next K tile)
       bool ok = mbar_wait(&bars->q_ready, 0, abort, err);
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int ks = j % KS, sb = j & 1;
-        if (!mbar_wait(&bars->k_full[ks], (j / KS) & 1u, abort, err)) break;
-        if (!mbar_wait(&bars->s_empty[sb], ((j >> 1) & 1u) ^ 1u, abort, err)) break;
-        tc_fence_after();
-        const uint32_t kb = smem_u32(sm + S::OFF_K + ks * S::KV_TILE);
-#pragma unroll
-        for (int kc = 0; kc < DH / 16; ++kc)
-          tc_mma_bf16(tmem + S::S_COL + sb * KT, sdesc_sw128(q_base + (kc >> 2) * (QROWS * 128) + (kc & 3) * 32),
-                      sdesc_sw128(kb + (kc >> 2) * (KT * 128) + (kc & 3) * 32), id_s, kc > 0 ? 1u : 0u);
-        tc_commit(&bars->s_full[sb]);
-        tc_commit(&bars->k_empty[ks]);
-        if (j > 0) ok = pv(j - 1);
+      int js = 0, jp = 0;
+      uint32_t idle = 0;
+      uint64_t t_idle = 0;
+      while (ok && jp < n_tiles) {
+        bool did = false;
+        if (js < n_tiles && mbar_try(&bars->k_full[js % KS], (js / KS) & 1u) &&
+            mbar_try(&bars->s_empty[js & 1], ((js >> 1) & 1u) ^ 1u)) {
+          issue_s(js++);
+          did = true;
+        }
+        if (jp < js && mbar_try(&bars->p_full[jp & 1], (jp >> 1) & 1u) &&
+            mbar_try(&bars->v_full[jp % VS], (jp / VS) & 1u)) {
+          issue_pv(jp++);
+          did = true;
+        }
+        if (did) {
+          idle = 0;
+          continue;
+        }
+        if (idle++ == 0) {
+          t_idle = globaltimer_ns();
+        } else if ((idle & 63) == 0) {   // bounded: no progress for kWaitLimitNs ends the loop
+          if (*abort) break;
+          if (globaltimer_ns() - t_idle > kWaitLimitNs) {
+            set_err(err, DLLM_ERR_TIMEOUT);
+            *abort = 1;
+            break;
+          }
+        }
       }
-      if (ok && n_tiles > 0 && !*abort) pv(n_tiles - 1);
       tc_commit(&bars->done);
       mbar_wait(&bars->done, 0, nullptr, err);
     }
