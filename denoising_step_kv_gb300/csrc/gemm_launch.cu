@@ -216,7 +216,9 @@ cudaError_t qkv_dh(dllm_cache* c, int layer, const void* A, int M_cap, const int
 
 }  // namespace
 
-int lm_tile_cols(const dllm_cache*) { return 128; }
+// Vocab columns per LM-head partial: 256 when the pair kernel runs (more
+// than one 128-row tile: two row tiles share each weight tile), else 128.
+int lm_tile_cols(const dllm_cache* c, int M) { return c->cfg.dtype == DLLM_BF16 && M > tc::BM ? tc::PBN : tc::BN; }
 
 cudaError_t gemm_qkv(dllm_cache* c, int layer, const void* A, int M_cap, const int* M_dev, const int* rows,
                      const void* w_qkv, cudaStream_t st) {
@@ -260,7 +262,14 @@ cudaError_t gemm_lm(dllm_cache* c, const void* A, const void* W, int M, int V, i
                     int mask_id, void* part, int n_tiles, cudaStream_t st) {
   EpiLM e{rs, mask_id, static_cast<LMPart*>(part), n_tiles};
   if (c->cfg.dtype == DLLM_BF16) {
-    // many vocab tiles: clusters of 4 share the rows' tile (two CTAs per SM)
+    if (M > tc::BM) {   // pairs of row tiles share each 256-column weight tile
+      CUtensorMap ta, tb;
+      if (!make_tmap_2d(&ta, A, d, M, static_cast<uint64_t>(d) * 2, tc::BK, tc::BM, true) ||
+          !make_tmap_2d(&tb, W, d, V, static_cast<uint64_t>(d) * 2, tc::BK, tc::BN, true))
+        return cudaErrorInvalidValue;
+      return launch_pair<EpiLM, 4>(c, ta, tb, M, M, nullptr, 0, V, d, e, st);
+    }
+    // one row tile, many vocab tiles: clusters of 4 share the rows' tile
     if (M > 0 && cdiv(V, tc::BN) >= 8) return launch_sharea<EpiLM, 3, 4>(c, A, M, W, V, d, e, st);
     return run_tc(c, A, M, M, nullptr, W, V, d, e, st);
   }
