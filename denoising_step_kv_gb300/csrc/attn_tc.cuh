@@ -2,25 +2,25 @@
 //
 // One CTA = (key split, head, sequence); clusters of n_split CTAs along the
 // key splits.  Four lanes of warp 0 stream 64-key K and V tiles through
-// separate rings (two issuers per ring) with one bulk copy each (the cache stores every tile as the
-// 128-byte-swizzled image the tensor cores read; K is released once S_j is
-// done, V once P_j V_j is done).  One thread of warp 1 issues
+// separate rings (two issuers per ring) with one bulk copy each (the cache
+// stores every tile as the 128-byte-swizzled image the tensor cores read; K
+// is released once S_j is done, V once P_j V_j is done).  One thread of
+// warp 1 issues, as soon as each one's inputs are ready,
 //   S_j = Q K_j^T            M = 128 query rows, N = 64 keys, into one of two
 //                            TMEM buffers (64 columns each),
-//   O  += P_j,hi V_j + P_j,lo V_j   M = 128, N = 64 per 64-dim half, K = 16,
-// with V read as an MN-major operand straight from its TMA tile.  The 128
-// MMA rows hold R = 128 / QP replicas of the QP (padded) queries; replica
-// g's softmax thread (thread = row = TMEM lane, warps 2-5) takes only the
-// tile's key columns [g 64/R, (g + 1) 64/R), so every one of the 128
-// threads works on a short row segment.  The replicas of a query agree on
-// its running max through shared memory (one named barrier per tile), keep
-// an online softmax in the log2 domain with a lazy reference (moved only
-// when the max grows by more than 2^8, and then O is rescaled in TMEM), and
-// write their P_j segment as hi + lo bf16 in the 128-byte-swizzled K-major
-// layout the MMA reads; the rest of a replica's P row stays zero, so its O
-// row is the partial sum over its key group.  The partials (m, l, O) of
-// every replica and every split are merged across the cluster through
-// distributed shared memory.
+//   O  += P_j,hi V_j + P_j,lo V_j   M = 128, N = DH, K = 16,
+// with P read from TMEM (it overwrites S_j in place) and V as an MN-major
+// operand straight from its tile.  The 128 MMA rows hold R replicas of the
+// block's queries, row g * QP + r for replica g of query r; replica g's
+// softmax thread (thread = row = TMEM lane, warps 2-5) takes only the tile's
+// key columns [g 64/R, (g + 1) 64/R), and a query's replicas agree on its
+// running maximum through shared memory (one named barrier per tile).  The online softmax runs
+// in the log2 domain with a lazy reference (moved only when the max grows by
+// more than 2^8, and then O is rescaled in TMEM); each thread writes its
+// whole P row (its segment as hi + lo bf16 pairs, zeros elsewhere), so a
+// replica's O row is the partial sum over its key group.  The partials
+// (m, l, O) of every replica and every split are merged across the cluster
+// through distributed shared memory.
 #pragma once
 #include "common.cuh"
 
@@ -28,8 +28,8 @@ namespace dllm {
 namespace attn_tc {
 
 constexpr int KT = 64;                  // keys per tile
-constexpr int KS = 3;                   // K ring slots (released after S_j)
-constexpr int VS = 4;                   // V ring slots (released after P_j V_j)
+constexpr int KS = 5;                   // K ring slots (released after S_j)
+constexpr int VS = 6;                   // V ring slots (released after P_j V_j)
 constexpr int QROWS = 128;              // MMA M (query rows, padded)
 constexpr float LAZY = 8.f;             // log2 headroom before the reference moves
 
@@ -40,15 +40,15 @@ struct Shape {
   static constexpr int SUB = DH / 64;                 // 64-dim sub-tiles
   static constexpr int Q_BYTES = QROWS * DH * 2;
   static constexpr int KV_TILE = KT * DH * 2;         // one K or V tile
-  static constexpr int P_BYTES = QROWS * KT * 2;      // one P part (hi or lo)
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_P = OFF_Q + Q_BYTES;       // [2 buffers][hi, lo]
-  static constexpr int OFF_K = OFF_P + 4 * P_BYTES;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + KS * KV_TILE;
   static constexpr int OFF_MX = OFF_V + VS * KV_TILE; // [2][QROWS] replica maxima
   static constexpr int OFF_BAR = OFF_MX + 2 * QROWS * 4;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
-  static constexpr uint32_t TMEM_COLS = 256;          // S: 2 x 64 columns, O: DH columns
+  // S_j: 64 fp32 columns of buffer j & 1, overwritten in place by P_j as
+  // bf16 pairs (hi: columns 0-31, lo: 32-63); O: DH columns
+  static constexpr uint32_t TMEM_COLS = 256;
   static constexpr uint32_t S_COL = 0, O_COL = 128;
   // tail: partials reuse the drained K/V rings
   static constexpr int PLD = DH + 4;                  // padded fp32 row
@@ -57,7 +57,7 @@ struct Shape {
 
 struct Bars {
   uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
-  uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
+  uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t q_ready, done;
   uint32_t tmem;
   int abort;
@@ -69,7 +69,7 @@ struct Bars {
 __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(8192 >> 4) << 16;                 // next MN atom (unused: N = 64)
+  d |= static_cast<uint64_t>(8192 >> 4) << 16;                 // next 64-wide MN atom (N = 128)
   d |= static_cast<uint64_t>(1024 >> 4) << 32;                 // next 8 K rows
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
@@ -96,6 +96,30 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+      "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// D += A B with A (M x 16 bf16, packed in pairs along TMEM columns, one row
+// per lane) read from TMEM and B from shared memory.
+__device__ __forceinline__ void tc_mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // 32 lanes x 16 consecutive fp32 columns from TMEM (warp-collective).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   uint32_t r[16];
@@ -110,9 +134,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void softmax_bar() {   // the 4 softmax warps
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-}
 
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -185,7 +206,6 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_empty[i], 4);
       mbar_init(&bars->p_full[i], 4);
       mbar_init(&bars->pv_done[i], 1);
     }
@@ -234,7 +254,7 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(QROWS, KT);
-      const uint32_t id_pv = idesc_bf16_bmn(QROWS, 64);
+      const uint32_t id_pv = idesc_bf16_bmn(QROWS, DH);
       const uint32_t q_base = smem_u32(sm + S::OFF_Q);
       // S_j = Q K_j^T into TMEM S buffer j & 1
       auto issue_s = [&](int j) {
@@ -253,37 +273,35 @@ __global__ void __launch_bounds__(192, 1)
         const int pb = i & 1, vs = i % VS;
         tc_fence_after();
         const uint32_t vb = smem_u32(sm + S::OFF_V + vs * S::KV_TILE);
+        // N = DH in one MMA: the V tile's 64-dim halves are MN atoms 8 KB apart
 #pragma unroll
-        for (int half = 0; half < S::SUB; ++half) {
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t pt = tmem + S::S_COL + pb * KT + part * (KT / 2);   // P_i hi / lo in TMEM
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            const uint32_t pbase = smem_u32(sm + S::OFF_P + (pb * 2 + part) * S::P_BYTES);
-#pragma unroll
-            for (int k = 0; k < KT / 16; ++k)
-              tc_mma_bf16(tmem + S::O_COL + half * 64, sdesc_sw128(pbase + k * 32),
-                          sdesc_sw128_mn(vb + half * KT * 128 + k * 2048), id_pv,
-                          (i > 0 || part > 0 || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < KT / 16; ++k)
+            tc_mma_bf16_ta(tmem + S::O_COL, pt + k * 8, sdesc_sw128_mn(vb + k * 2048), id_pv,
+                           (i > 0 || part > 0 || k > 0) ? 1u : 0u);
         }
         tc_commit(&bars->pv_done[pb]);
         tc_commit(&bars->v_empty[vs]);
       };
-      // issue whichever MMA is ready: S of the next tile once its K tile and
-      // S buffer are there, P V as soon as the softmax has written P (so the
-      // V slot is released without waiting for the next K tile)
+      // issue whichever MMA is ready: S of the next tile once its K tile is
+      // there, P V as soon as the softmax has written P (so the V slot is
+      // released without waiting for the next K tile)
       bool ok = mbar_wait(&bars->q_ready, 0, abort, err);
       int js = 0, jp = 0;
       uint32_t idle = 0;
       uint64_t t_idle = 0;
       while (ok && jp < n_tiles) {
         bool did = false;
-        if (js < n_tiles && mbar_try(&bars->k_full[js % KS], (js / KS) & 1u) &&
-            mbar_try(&bars->s_empty[js & 1], ((js >> 1) & 1u) ^ 1u)) {
+        // S_js overwrites P_{js-2}: only after P_{js-2} V_{js-2} is issued
+        // (the MMAs run in order)
+        if (js < n_tiles && js <= jp + 1 && mbar_test(&bars->k_full[js % KS], (js / KS) & 1u)) {
           issue_s(js++);
           did = true;
         }
-        if (jp < js && mbar_try(&bars->p_full[jp & 1], (jp >> 1) & 1u) &&
-            mbar_try(&bars->v_full[jp % VS], (jp / VS) & 1u)) {
+        if (jp < js && mbar_test(&bars->p_full[jp & 1], (jp >> 1) & 1u) &&
+            mbar_test(&bars->v_full[jp % VS], (jp / VS) & 1u)) {
           issue_pv(jp++);
           did = true;
         }
@@ -306,17 +324,26 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait(&bars->done, 0, nullptr, err);
     }
   } else {
-    // ---- stage Q (row g * QP + r holds query r; zero past q_len) and zero P
+    // ---- stage Q: row g * QP + r holds query r (zero past q_len); every
+    // (query, chunk) is loaded once, all loads in flight before the stores
     {
       const int st = tid - 64;   // 128 staging threads
-      for (int e = st; e < QROWS * (DH / 8); e += 128) {
-        const int m = e / (DH / 8), c = e % (DH / 8), r = m % QP;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < q_len) v = *reinterpret_cast<const uint4*>(Ql + kv.chunk_off(b, h, q_pos0 + r, c));
-        *reinterpret_cast<uint4*>(sm + S::OFF_Q + (c >> 3) * (QROWS * 128) + sw128_off(m, c & 7)) = v;
+      constexpr int NQ = QP * (DH / 8), PER = (NQ + 127) / 128;
+      uint4 v[PER];
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int e = st + u * 128, r = e / (DH / 8), c = e % (DH / 8);
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (e < NQ && r < q_len) v[u] = *reinterpret_cast<const uint4*>(Ql + kv.chunk_off(b, h, q_pos0 + r, c));
       }
-      for (int e = st; e < 4 * S::P_BYTES / 16; e += 128)
-        *reinterpret_cast<uint4*>(sm + S::OFF_P + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int e = st + u * 128, r = e / (DH / 8), c = e % (DH / 8);
+        if (e >= NQ) continue;
+#pragma unroll
+        for (int g2 = 0; g2 < R; ++g2)
+          *reinterpret_cast<uint4*>(sm + S::OFF_Q + (c >> 3) * (QROWS * 128) + sw128_off(g2 * QP + r, c & 7)) = v[u];
+      }
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->q_ready);
@@ -325,9 +352,9 @@ __global__ void __launch_bounds__(192, 1)
     // owning the tile's key columns [g * KG, g * KG + KG)
     const int wq = warp & 3;
     const int m = wq * 32 + lane, g = m / QP, r = m % QP;
+    float* mx = reinterpret_cast<float*>(sm + S::OFF_MX);   // [2][QROWS]
     const bool valid = r < q_len;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    float* mx = reinterpret_cast<float*>(sm + S::OFF_MX);   // [2][QROWS]
     for (int j = 0; j < n_tiles; ++j) {
       const int sb = j & 1;
       int ok = 1;
@@ -357,9 +384,6 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_empty[sb]);
       // this segment's maximum, then the query's maximum over its replicas
       const int key0 = k_begin + j * KT + g * KG;
       float mt = -INFINITY;
@@ -368,9 +392,9 @@ __global__ void __launch_bounds__(192, 1)
         sv[i] = (valid && key0 + i < k_end) ? sv[i] * scale_log2 : -INFINITY;
         mt = fmaxf(mt, sv[i]);
       }
-      if constexpr (R > 1) {
+      if constexpr (R > 1) {   // the query's maximum over its replicas (other warps)
         mx[sb * QROWS + m] = mt;
-        softmax_bar();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
 #pragma unroll
         for (int gg = 0; gg < R; ++gg) mt = fmaxf(mt, mx[sb * QROWS + gg * QP + r]);
       }
@@ -404,33 +428,33 @@ __global__ void __launch_bounds__(192, 1)
           tmem_st32(tmem + lane_off + S::O_COL + c * 32, o);
         }
       }
-      // P buffer sb was last read by P V of tile j - 2
-      if (j >= 2) {
-        int ok3 = 1;
-        if (lane == 0) ok3 = mbar_wait(&bars->pv_done[sb], ((j - 2) >> 1) & 1u, abort, err) ? 1 : 0;
-        ok3 = __shfl_sync(0xffffffffu, ok3, 0);
-        if (!ok3) break;
-      }
-      if (valid) {
-        uint8_t* ph = sm + S::OFF_P + (sb * 2) * S::P_BYTES;
-        uint8_t* pl = ph + S::P_BYTES;
+      // P_j over S_j in TMEM: this row's segment as hi + lo bf16 pairs, the
+      // other replicas' keys (and rows past q_len) zero
+      {
+        uint32_t ph[KG / 2], pl[KG / 2];
 #pragma unroll
-        for (int c = 0; c < KG / 8; ++c) {
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float a = sv[c * 8 + 2 * i], bb = sv[c * 8 + 2 * i + 1];
-            const __nv_bfloat162 hb = __floats2bfloat162_rn(a, bb);
-            const float2 hf = __bfloat1622float2(hb);
-            hi[i] = *reinterpret_cast<const uint32_t*>(&hb);
-            lo[i] = pack2(a - hf.x, bb - hf.y);
-          }
-          const uint32_t off = sw128_off(m, g * (KG / 8) + c);
-          *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(pl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        for (int i = 0; i < KG / 2; ++i) {
+          const float a = sv[2 * i], bb = sv[2 * i + 1];
+          const __nv_bfloat162 hb = __floats2bfloat162_rn(a, bb);
+          const float2 hf = __bfloat1622float2(hb);
+          ph[i] = valid ? *reinterpret_cast<const uint32_t*>(&hb) : 0u;
+          pl[i] = valid ? pack2(a - hf.x, bb - hf.y) : 0u;
         }
+        // segment g of the row (g is the same in every lane of the warp);
+        // constant indices keep the row in registers
+        uint32_t hi[KT / 2], lo[KT / 2];
+#pragma unroll
+        for (int gg = 0; gg < R; ++gg)
+#pragma unroll
+          for (int i = 0; i < KG / 2; ++i) {
+            hi[gg * (KG / 2) + i] = gg == g ? ph[i] : 0u;
+            lo[gg * (KG / 2) + i] = gg == g ? pl[i] : 0u;
+          }
+        const uint32_t pt = tmem + lane_off + S::S_COL + sb * KT;
+        tmem_st32u(pt, hi);
+        tmem_st32u(pt + KT / 2, lo);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
-      fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->p_full[sb]);
