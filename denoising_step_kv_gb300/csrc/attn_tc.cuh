@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(192, 1)
       float ls = 0.f;
 #pragma unroll
       for (int i = 0; i < KG; ++i) {
-        sv[i] = m_ref == -INFINITY ? 0.f : exp2f(sv[i] - m_ref);
+        sv[i] = m_ref == -INFINITY ? 0.f : ex2_fast(sv[i] - m_ref);
         ls += sv[i];
       }
       l_sum = l_sum * alpha + ls;

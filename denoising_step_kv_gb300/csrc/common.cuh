@@ -79,6 +79,14 @@ template <> __device__ __forceinline__ void load_row<float>(const float* src, fl
   }
 }
 
+// 2^x on the special-function unit (ex2.approx: a few ulp, -inf -> +0); the
+// softmax weights of the attention kernels.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- errors
 __device__ __forceinline__ void set_err(unsigned* err, unsigned bit) {
   if (err) atomicOr(err, bit);
