@@ -8,9 +8,10 @@
 // row ranges come from a binary search of the sorted list at kernel start.
 // Within an item the pipeline is the one of attn_tc_kernel with one query per
 // MMA row (no replicas, no key splits): lanes 0/1 of warp 0 stream K/V tiles
-// (one bulk copy each), one thread of warp 1 issues S = Q K^T and
-// O += P_hi V + P_lo V on tcgen05, warps 2-5 run the online softmax (one
-// query per thread) and, after the last tile, normalise O and store it.  The
+// (two issuers per ring), one thread of warp 1 issues S = Q K^T and
+// O += P_hi V + P_lo V on tcgen05 as each one's inputs are ready (P kept in
+// TMEM over S), warps 2-5 run the online softmax (one query per thread) and,
+// after the last tile, normalise O and store it.  The
 // barrier phases run on a tile counter shared by all items of the CTA.
 #pragma once
 #include "attn_tc.cuh"
@@ -20,27 +21,25 @@ namespace attn_rows {
 
 using attn_tc::KT;
 using attn_tc::LAZY;
-constexpr int KS = 3, VS = 4, QROWS = 128, MAX_SEQ = 256;
+constexpr int KS = 5, VS = 6, QROWS = 128, MAX_SEQ = 256;
 
 template <int DH>
 struct Shape {
   static constexpr int Q_BYTES = QROWS * DH * 2;
   static constexpr int KV_TILE = KT * DH * 2;
-  static constexpr int P_BYTES = QROWS * KT * 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_P = OFF_Q + Q_BYTES;        // [2 buffers][hi, lo]
-  static constexpr int OFF_K = OFF_P + 4 * P_BYTES;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + KS * KV_TILE;
   static constexpr int OFF_SEQ = OFF_V + VS * KV_TILE;  // [MAX_SEQ + 1] first item, [MAX_SEQ + 1] first row
   static constexpr int OFF_BAR = OFF_SEQ + (2 * MAX_SEQ + 2) * 4;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
-  static constexpr uint32_t TMEM_COLS = 256;           // S: 2 x 64 columns, O: DH columns
+  static constexpr uint32_t TMEM_COLS = 256;           // S / P: 2 x 64 columns, O: DH columns
   static constexpr uint32_t S_COL = 0, O_COL = 128;
 };
 
 struct Bars {
   uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
-  uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
+  uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t q_ready, done;
   uint32_t tmem;
   int abort;
@@ -80,7 +79,6 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_empty[i], 4);
       mbar_init(&bars->p_full[i], 4);
       mbar_init(&bars->pv_done[i], 1);
     }
@@ -163,51 +161,72 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(QROWS, KT);
-      const uint32_t id_pv = attn_tc::idesc_bf16_bmn(QROWS, 64);
+      const uint32_t id_pv = attn_tc::idesc_bf16_bmn(QROWS, DH);
       const uint32_t q_base = smem_u32(sm + S::OFF_Q);
-      // P_J V_J; `first`: the first tile of an item (overwrites O)
-      auto pv = [&](int J, bool first) -> bool {
+      // the CTA's tiles J = 0, 1, ... run through its items in order; every
+      // item has n_tiles tiles, so tile J belongs to item J / n_tiles
+      const int my_items = blockIdx.x < n_items ? (n_items - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+      const int total = my_items * n_tiles;
+      auto issue_s = [&](int J) {
+        const int ks = J % KS, sb = J & 1;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(sm + S::OFF_K + ks * S::KV_TILE);
+#pragma unroll
+        for (int kc = 0; kc < DH / 16; ++kc)
+          tc_mma_bf16(tmem + S::S_COL + sb * KT, sdesc_sw128(q_base + (kc >> 2) * (QROWS * 128) + (kc & 3) * 32),
+                      sdesc_sw128(kb + (kc >> 2) * (KT * 128) + (kc & 3) * 32), id_s, kc > 0 ? 1u : 0u);
+        tc_commit(&bars->s_full[sb]);
+        tc_commit(&bars->k_empty[ks]);
+      };
+      // O += P_J V_J with P from TMEM, N = DH in one MMA per 16 keys; the
+      // first tile of an item overwrites O
+      auto issue_pv = [&](int J) {
         const int pb = J & 1, vs = J % VS;
-        if (!mbar_wait(&bars->p_full[pb], (J >> 1) & 1u, abort, err)) return false;
-        if (!mbar_wait(&bars->v_full[vs], (J / VS) & 1u, abort, err)) return false;
+        const bool first = J % n_tiles == 0;
         tc_fence_after();
         const uint32_t vb = smem_u32(sm + S::OFF_V + vs * S::KV_TILE);
 #pragma unroll
-        for (int half = 0; half < DH / 64; ++half) {
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t pt = tmem + S::S_COL + pb * KT + part * (KT / 2);
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            const uint32_t pbase = smem_u32(sm + S::OFF_P + (pb * 2 + part) * S::P_BYTES);
-#pragma unroll
-            for (int k = 0; k < KT / 16; ++k)
-              tc_mma_bf16(tmem + S::O_COL + half * 64, sdesc_sw128(pbase + k * 32),
-                          attn_tc::sdesc_sw128_mn(vb + half * KT * 128 + k * 2048), id_pv,
-                          (!first || part > 0 || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < KT / 16; ++k)
+            attn_tc::tc_mma_bf16_ta(tmem + S::O_COL, pt + k * 8, attn_tc::sdesc_sw128_mn(vb + k * 2048), id_pv,
+                                    (!first || part > 0 || k > 0) ? 1u : 0u);
         }
         tc_commit(&bars->pv_done[pb]);
         tc_commit(&bars->v_empty[vs]);
-        return true;
       };
-      bool ok = true;
-      int J = 0, it = 0;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
-        ok = mbar_wait(&bars->q_ready, it & 1u, abort, err);
-        const int J0 = J;
-        for (int j = 0; j < n_tiles && ok; ++j, ++J) {
-          const int ks = J % KS, sb = J & 1;
-          if (!mbar_wait(&bars->k_full[ks], (J / KS) & 1u, abort, err)) { ok = false; break; }
-          if (!mbar_wait(&bars->s_empty[sb], ((J >> 1) & 1u) ^ 1u, abort, err)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t kb = smem_u32(sm + S::OFF_K + ks * S::KV_TILE);
-#pragma unroll
-          for (int kc = 0; kc < DH / 16; ++kc)
-            tc_mma_bf16(tmem + S::S_COL + sb * KT, sdesc_sw128(q_base + (kc >> 2) * (QROWS * 128) + (kc & 3) * 32),
-                        sdesc_sw128(kb + (kc >> 2) * (KT * 128) + (kc & 3) * 32), id_s, kc > 0 ? 1u : 0u);
-          tc_commit(&bars->s_full[sb]);
-          tc_commit(&bars->k_empty[ks]);
-          if (j > 0) ok = pv(J - 1, J - 1 == J0);
+      int js = 0, jp = 0;
+      uint32_t idle = 0;
+      uint64_t t_idle = 0;
+      while (jp < total) {
+        bool did = false;
+        // S_js: its K tile, the item's Q (first tile), and P_{js-2} V_{js-2}
+        // issued (S_js overwrites P_{js-2}; the MMAs run in order)
+        if (js < total && js <= jp + 1 && mbar_test(&bars->k_full[js % KS], (js / KS) & 1u) &&
+            (js % n_tiles != 0 || mbar_test(&bars->q_ready, static_cast<uint32_t>(js / n_tiles) & 1u))) {
+          issue_s(js++);
+          did = true;
         }
-        if (ok && !*abort) ok = pv(J - 1, J - 1 == J0);
+        if (jp < js && mbar_test(&bars->p_full[jp & 1], (jp >> 1) & 1u) &&
+            mbar_test(&bars->v_full[jp % VS], (jp / VS) & 1u)) {
+          issue_pv(jp++);
+          did = true;
+        }
+        if (did) {
+          idle = 0;
+          continue;
+        }
+        if (idle++ == 0) {
+          t_idle = globaltimer_ns();
+        } else if ((idle & 63) == 0) {
+          if (*abort) break;
+          if (globaltimer_ns() - t_idle > kWaitLimitNs) {
+            set_err(err, DLLM_ERR_TIMEOUT);
+            *abort = 1;
+            break;
+          }
+        }
       }
       tc_commit(&bars->done);
       mbar_wait(&bars->done, 0, nullptr, err);
@@ -216,9 +235,6 @@ __global__ void __launch_bounds__(192, 1)
     const int wq = warp & 3, m = wq * 32 + lane;   // this thread's query row (TMEM lane)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const int st = tid - 64;                        // 128 staging threads
-    // P rows of queries past the tile's count keep their zeros
-    for (int e = st; e < 4 * S::P_BYTES / 16; e += 128)
-      *reinterpret_cast<uint4*>(sm + S::OFF_P + e * 16) = make_uint4(0u, 0u, 0u, 0u);
     int J = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
@@ -229,14 +245,20 @@ __global__ void __launch_bounds__(192, 1)
       const int nq = min(QROWS, r_end - r0);
       // ---- stage Q of rows r0 .. r0 + nq (zero past nq); the previous item's
       // S MMAs are done (its last P V has completed before we got here)
-      for (int e = st; e < QROWS * (DH / 8); e += 128) {
-        const int q = e / (DH / 8), c = e % (DH / 8);
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (q < nq) {
-          const int row = rows[r0 + q];
-          v = *reinterpret_cast<const uint4*>(Ql + kv.chunk_off(b, h, row - b * L, c));
+      {   // all loads in flight before the stores
+        constexpr int PER = QROWS * (DH / 8) / 128;
+        uint4 v[PER];
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+          const int e = st + u * 128, q = e / (DH / 8), c = e % (DH / 8);
+          v[u] = make_uint4(0u, 0u, 0u, 0u);
+          if (q < nq) v[u] = *reinterpret_cast<const uint4*>(Ql + kv.chunk_off(b, h, rows[r0 + q] - b * L, c));
         }
-        *reinterpret_cast<uint4*>(sm + S::OFF_Q + (c >> 3) * (QROWS * 128) + sw128_off(q, c & 7)) = v;
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+          const int e = st + u * 128, q = e / (DH / 8), c = e % (DH / 8);
+          *reinterpret_cast<uint4*>(sm + S::OFF_Q + (c >> 3) * (QROWS * 128) + sw128_off(q, c & 7)) = v[u];
+        }
       }
       attn_tc::fence_async_smem();
       tc_fence_before();
@@ -245,7 +267,6 @@ __global__ void __launch_bounds__(192, 1)
 
       const bool valid = m < nq;
       float m_ref = -INFINITY, l_sum = 0.f;
-      const int J0 = J;
       for (int j = 0; j < n_tiles; ++j, ++J) {
         const int sb = J & 1;
         int w_ok = 1;
@@ -265,9 +286,6 @@ __global__ void __launch_bounds__(192, 1)
             sv[i + 32] = t1[i];
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->s_empty[sb]);
         const int key0 = j * KT;
         float mt = -INFINITY;
 #pragma unroll
@@ -304,33 +322,22 @@ __global__ void __launch_bounds__(192, 1)
             attn_tc::tmem_st32(tmem + lane_off + S::O_COL + c * 32, o);
           }
         }
-        // P buffer sb was last read by P V of tile J - 2
-        if (J >= 2) {
-          int ok3 = 1;
-          if (lane == 0) ok3 = mbar_wait(&bars->pv_done[sb], ((J - 2) >> 1) & 1u, abort, err) ? 1 : 0;
-          ok3 = __shfl_sync(0xffffffffu, ok3, 0);
-          if (!ok3) { ok = false; break; }
-        }
-        if (valid) {
-          uint8_t* ph = sm + S::OFF_P + (sb * 2) * S::P_BYTES;
-          uint8_t* pl = ph + S::P_BYTES;
+        // P_J over S_J in TMEM as hi + lo bf16 pairs (zeros past the tile's rows)
+        {
+          uint32_t hi[KT / 2], lo[KT / 2];
 #pragma unroll
-          for (int c = 0; c < KT / 8; ++c) {
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float a = sv[c * 8 + 2 * i], bb = sv[c * 8 + 2 * i + 1];
-              const __nv_bfloat162 hb = __floats2bfloat162_rn(a, bb);
-              const float2 hf = __bfloat1622float2(hb);
-              hi[i] = *reinterpret_cast<const uint32_t*>(&hb);
-              lo[i] = pack2(a - hf.x, bb - hf.y);
-            }
-            const uint32_t off = sw128_off(m, c);
-            *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(pl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          for (int i = 0; i < KT / 2; ++i) {
+            const float a = sv[2 * i], bb = sv[2 * i + 1];
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(a, bb);
+            const float2 hf = __bfloat1622float2(hb);
+            hi[i] = valid ? *reinterpret_cast<const uint32_t*>(&hb) : 0u;
+            lo[i] = valid ? pack2(a - hf.x, bb - hf.y) : 0u;
           }
+          const uint32_t pt = tmem + lane_off + S::S_COL + sb * KT;
+          attn_tc::tmem_st32u(pt, hi);
+          attn_tc::tmem_st32u(pt + KT / 2, lo);
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
-        attn_tc::fence_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full[sb]);
@@ -355,7 +362,6 @@ __global__ void __launch_bounds__(192, 1)
             store_row(orow + c * 32, o, 32);
           }
         }
-        (void)J0;
         tc_fence_before();   // O reads ordered before the next item's first P V
       }
     }
