@@ -1,26 +1,31 @@
 // Cached attention on the 5th-generation tensor cores (bf16).
 //
 // One CTA = (key split, head, sequence); clusters of n_split CTAs along the
-// key splits.  Four lanes of warp 0 stream 64-key K and V tiles through
-// separate rings (two issuers per ring) with one bulk copy each (the cache
-// stores every tile as the 128-byte-swizzled image the tensor cores read; K
-// is released once S_j is done, V once P_j V_j is done).  One thread of
-// warp 1 issues, as soon as each one's inputs are ready,
-//   S_j = Q K_j^T            M = 128 query rows, N = 64 keys, into one of two
-//                            TMEM buffers (64 columns each),
+// key splits.  Four lanes of warp 0 stream 64-key tiles into a ring of
+// NSLOT slots, each holding tile j's K and V (one bulk copy each: the cache
+// stores every tile as the 128-byte-swizzled image the tensor cores read;
+// lanes 0/1 take the K/V of even tiles, lanes 2/3 of odd ones, as one
+// thread's bulk copies are served one after another).  One thread of warp 1
+// issues, in a fixed order (S_{j+1} before P_j V_j),
+//   S_j = Q K_j^T    M = 128 query rows, N = 64 keys, into one of two TMEM
+//                    buffers (64 columns each),
 //   O  += P_j,hi V_j + P_j,lo V_j   M = 128, N = DH, K = 16,
-// with P read from TMEM (it overwrites S_j in place) and V as an MN-major
-// operand straight from its tile.  The 128 MMA rows hold R replicas of the
-// block's queries, row g * QP + r for replica g of query r; replica g's
-// softmax thread (thread = row = TMEM lane, warps 2-5) takes only the tile's
-// key columns [g 64/R, (g + 1) 64/R), and a query's replicas agree on its
-// running maximum through shared memory (one named barrier per tile).  The online softmax runs
-// in the log2 domain with a lazy reference (moved only when the max grows by
-// more than 2^8, and then O is rescaled in TMEM); each thread writes its
-// whole P row (its segment as hi + lo bf16 pairs, zeros elsewhere), so a
-// replica's O row is the partial sum over its key group.  The partials
-// (m, l, O) of every replica and every split are merged across the cluster
-// through distributed shared memory.
+// with P read from TMEM as a bf16 pair (hi + lo, so that O keeps fp32-level
+// accuracy; P_j overwrites S_j in place, and the fixed order puts S_{j+2}
+// behind P_j V_j) and V as an MN-major operand straight from its tile.  At these sizes the issuing thread spends 50-65 clocks per
+// MMA and about as much per commit or barrier test, so a tile costs it 16
+// MMAs, 2 commits (S_j done; P_j V_j done, which frees the slot) and 2
+// blocking waits (K_j landed; P_j written, which the softmax signals only
+// once V_j has landed too).  The 128 MMA rows hold R replicas
+// of the block's queries, row g * QP + r for replica g of query r; replica
+// g's softmax thread (thread = row = TMEM lane, warps 2-5) takes only the
+// tile's key columns [g 64/R, (g + 1) 64/R) and keeps its own running
+// maximum, so a replica row is an independent partial softmax over its key
+// group.  The online softmax runs in the log2 domain with a lazy reference
+// (moved only when the max grows by more than 2^8, and then O is rescaled in
+// TMEM).  A thread writes its whole P row: its segment, zeros elsewhere.  The partials (m, l, O) of every
+// replica and every split are merged across the cluster through distributed
+// shared memory.
 #pragma once
 #include "common.cuh"
 
@@ -28,8 +33,7 @@ namespace dllm {
 namespace attn_tc {
 
 constexpr int KT = 64;                  // keys per tile
-constexpr int KS = 5;                   // K ring slots (released after S_j)
-constexpr int VS = 6;                   // V ring slots (released after P_j V_j)
+constexpr int NSLOT = 6;                // ring slots (K and V of one tile each)
 constexpr int QROWS = 128;              // MMA M (query rows, padded)
 constexpr float LAZY = 8.f;             // log2 headroom before the reference moves
 
@@ -41,23 +45,22 @@ struct Shape {
   static constexpr int Q_BYTES = QROWS * DH * 2;
   static constexpr int KV_TILE = KT * DH * 2;         // one K or V tile
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + KS * KV_TILE;
-  static constexpr int OFF_MX = OFF_V + VS * KV_TILE; // [2][QROWS] replica maxima
-  static constexpr int OFF_BAR = OFF_MX + 2 * QROWS * 4;
+  static constexpr int OFF_RING = OFF_Q + Q_BYTES;    // slot s: K at s * 2 KV_TILE, V after it
+  static constexpr int OFF_BAR = OFF_RING + NSLOT * 2 * KV_TILE;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
   // S_j: 64 fp32 columns of buffer j & 1, overwritten in place by P_j as
   // bf16 pairs (hi: columns 0-31, lo: 32-63); O: DH columns
   static constexpr uint32_t TMEM_COLS = 256;
-  static constexpr uint32_t S_COL = 0, O_COL = 128;
-  // tail: partials reuse the drained K/V rings
+  static constexpr uint32_t S_COL = 0, O_COL = 2 * KT;
+  static_assert(O_COL + DH <= TMEM_COLS, "TMEM budget");
+  // tail: partials reuse the drained ring
   static constexpr int PLD = DH + 4;                  // padded fp32 row
-  static_assert(QROWS * PLD * 4 + QROWS * 8 + QROWS * 8 * 4 <= (KS + VS) * KV_TILE, "tail fits in the rings");
+  static_assert(QROWS * PLD * 4 + QROWS * 8 + QROWS * 8 * 4 <= NSLOT * 2 * KV_TILE, "tail fits in the ring");
 };
 
 struct Bars {
-  uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
-  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t k_full[NSLOT], v_full[NSLOT], empty[NSLOT];
+  uint64_t s_full[2], p_full[2];
   uint64_t q_ready, done;
   uint32_t tmem;
   int abort;
@@ -181,6 +184,7 @@ __global__ void __launch_bounds__(192, 1)
                    bf16* __restrict__ out, unsigned* err) {
   using S = Shape<DH, R>;
   constexpr int QP = S::QP, KG = S::KG;
+  static_assert(sizeof(Bars) <= 256, "barrier block");
   const int split = blockIdx.x, n_split = gridDim.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -196,18 +200,14 @@ __global__ void __launch_bounds__(192, 1)
 
   // ---- barriers and TMEM first, so that the K/V streams start at once
   if (tid == 0) {
-    for (int s = 0; s < KS; ++s) {
+    for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-    }
-    for (int s = 0; s < VS; ++s) {
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 4);
-      mbar_init(&bars->pv_done[i], 1);
     }
     mbar_init(&bars->q_ready, 4);
     mbar_init(&bars->done, 1);
@@ -226,29 +226,23 @@ __global__ void __launch_bounds__(192, 1)
   float m_ref = -INFINITY, l_sum = 0.f;
 
   if (warp == 0) {
-    // lanes 0 and 2 stream K tiles, lanes 1 and 3 V tiles (independent rings,
-    // even and odd tiles: bulk copies from one thread are served one after
-    // another, so two issuers per ring keep twice the copies moving); a tile
-    // of the tiled cache is one contiguous bulk copy
     if (lane < 4) {
       const bool is_k = (lane & 1) == 0;
       const uint8_t* src = is_k ? Kl : Vl;
-      const int slots = is_k ? KS : VS;
+      uint8_t* ring = sm + S::OFF_RING + (is_k ? 0 : S::KV_TILE);
       uint64_t* fullb = is_k ? bars->k_full : bars->v_full;
-      uint64_t* emptyb = is_k ? bars->k_empty : bars->v_empty;
-      uint8_t* ring = sm + (is_k ? S::OFF_K : S::OFF_V);
       uint32_t issued = 0, par = 0;
       for (int j = lane >> 1; j < n_tiles; j += 2) {
-        const int s = j % slots;
-        const uint32_t ph = (j / slots) & 1u;
-        if (!mbar_wait(&emptyb[s], ph ^ 1u, abort, err)) break;
+        const int s = j % NSLOT;
+        const uint32_t ph = (j / NSLOT) & 1u;
+        if (!mbar_wait(&bars->empty[s], ph ^ 1u, abort, err)) break;
         mbar_expect_tx(&fullb[s], S::KV_TILE);
-        bulk_load(ring + s * S::KV_TILE, src + kv.tile_off(b, h, k_begin + j * KT), S::KV_TILE, &fullb[s]);
+        bulk_load(ring + s * 2 * S::KV_TILE, src + kv.tile_off(b, h, k_begin + j * KT), S::KV_TILE, &fullb[s]);
         issued |= 1u << s;
         par = (par & ~(1u << s)) | (ph << s);
       }
-      if (*abort)
-        for (int s = 0; s < slots; ++s)
+      if (*abort)   // drain this lane's copies in flight
+        for (int s = 0; s < NSLOT; ++s)
           if (issued & (1u << s)) mbar_wait(&fullb[s], (par >> s) & 1u, nullptr, err);
     }
   } else if (warp == 1) {
@@ -256,69 +250,44 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t id_s = idesc_bf16(QROWS, KT);
       const uint32_t id_pv = idesc_bf16_bmn(QROWS, DH);
       const uint32_t q_base = smem_u32(sm + S::OFF_Q);
-      // S_j = Q K_j^T into TMEM S buffer j & 1
+      // S_j = Q K_j^T into TMEM S buffer j & 1, where P_{j-2} was: P_{j-2}
+      // V_{j-2} is issued before it, and the MMAs run in order
       auto issue_s = [&](int j) {
-        const int ks = j % KS, sb = j & 1;
+        const int sb = j & 1;
         tc_fence_after();
-        const uint32_t kb = smem_u32(sm + S::OFF_K + ks * S::KV_TILE);
+        const uint32_t kb = smem_u32(sm + S::OFF_RING + (j % NSLOT) * 2 * S::KV_TILE);
 #pragma unroll
         for (int kc = 0; kc < DH / 16; ++kc)
           tc_mma_bf16(tmem + S::S_COL + sb * KT, sdesc_sw128(q_base + (kc >> 2) * (QROWS * 128) + (kc & 3) * 32),
                       sdesc_sw128(kb + (kc >> 2) * (KT * 128) + (kc & 3) * 32), id_s, kc > 0 ? 1u : 0u);
         tc_commit(&bars->s_full[sb]);
-        tc_commit(&bars->k_empty[ks]);
       };
       // O += P_i,hi V_i + P_i,lo V_i
       auto issue_pv = [&](int i) {
-        const int pb = i & 1, vs = i % VS;
+        const int s = i % NSLOT;
         tc_fence_after();
-        const uint32_t vb = smem_u32(sm + S::OFF_V + vs * S::KV_TILE);
+        const uint32_t vb = smem_u32(sm + S::OFF_RING + s * 2 * S::KV_TILE + S::KV_TILE);
         // N = DH in one MMA: the V tile's 64-dim halves are MN atoms 8 KB apart
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
-          const uint32_t pt = tmem + S::S_COL + pb * KT + part * (KT / 2);   // P_i hi / lo in TMEM
+          const uint32_t pt = tmem + S::S_COL + (i & 1) * KT + part * (KT / 2);   // P_i hi / lo in TMEM
 #pragma unroll
           for (int k = 0; k < KT / 16; ++k)
             tc_mma_bf16_ta(tmem + S::O_COL, pt + k * 8, sdesc_sw128_mn(vb + k * 2048), id_pv,
                            (i > 0 || part > 0 || k > 0) ? 1u : 0u);
         }
-        tc_commit(&bars->pv_done[pb]);
-        tc_commit(&bars->v_empty[vs]);
+        tc_commit(&bars->empty[s]);   // P_i V_i done: slot s free
       };
-      // issue whichever MMA is ready: S of the next tile once its K tile is
-      // there, P V as soon as the softmax has written P (so the V slot is
-      // released without waiting for the next K tile)
-      bool ok = mbar_wait(&bars->q_ready, 0, abort, err);
-      int js = 0, jp = 0;
-      uint32_t idle = 0;
-      uint64_t t_idle = 0;
-      while (ok && jp < n_tiles) {
-        bool did = false;
-        // S_js overwrites P_{js-2}: only after P_{js-2} V_{js-2} is issued
-        // (the MMAs run in order)
-        if (js < n_tiles && js <= jp + 1 && mbar_test(&bars->k_full[js % KS], (js / KS) & 1u)) {
-          issue_s(js++);
-          did = true;
+      bool ok = n_tiles == 0 || (mbar_wait(&bars->q_ready, 0, abort, err) &&
+                                 mbar_wait(&bars->k_full[0], 0, abort, err));
+      if (ok && n_tiles > 0) issue_s(0);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j + 1 < n_tiles) {
+          if (!mbar_wait(&bars->k_full[(j + 1) % NSLOT], ((j + 1) / NSLOT) & 1u, abort, err)) break;
+          issue_s(j + 1);
         }
-        if (jp < js && mbar_test(&bars->p_full[jp & 1], (jp >> 1) & 1u) &&
-            mbar_test(&bars->v_full[jp % VS], (jp / VS) & 1u)) {
-          issue_pv(jp++);
-          did = true;
-        }
-        if (did) {
-          idle = 0;
-          continue;
-        }
-        if (idle++ == 0) {
-          t_idle = globaltimer_ns();
-        } else if ((idle & 63) == 0) {   // bounded: no progress for kWaitLimitNs ends the loop
-          if (*abort) break;
-          if (globaltimer_ns() - t_idle > kWaitLimitNs) {
-            set_err(err, DLLM_ERR_TIMEOUT);
-            *abort = 1;
-            break;
-          }
-        }
+        if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1u, abort, err)) break;
+        issue_pv(j);
       }
       tc_commit(&bars->done);
       mbar_wait(&bars->done, 0, nullptr, err);
@@ -352,7 +321,6 @@ __global__ void __launch_bounds__(192, 1)
     // owning the tile's key columns [g * KG, g * KG + KG)
     const int wq = warp & 3;
     const int m = wq * 32 + lane, g = m / QP, r = m % QP;
-    float* mx = reinterpret_cast<float*>(sm + S::OFF_MX);   // [2][QROWS]
     const bool valid = r < q_len;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     for (int j = 0; j < n_tiles; ++j) {
@@ -384,19 +352,13 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      // this segment's maximum, then the query's maximum over its replicas
+      // this segment's maximum against the row's reference
       const int key0 = k_begin + j * KT + g * KG;
       float mt = -INFINITY;
 #pragma unroll
       for (int i = 0; i < KG; ++i) {
         sv[i] = (valid && key0 + i < k_end) ? sv[i] * scale_log2 : -INFINITY;
         mt = fmaxf(mt, sv[i]);
-      }
-      if constexpr (R > 1) {   // the query's maximum over its replicas (other warps)
-        mx[sb * QROWS + m] = mt;
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-#pragma unroll
-        for (int gg = 0; gg < R; ++gg) mt = fmaxf(mt, mx[sb * QROWS + gg * QP + r]);
       }
       float alpha = 1.f;
       bool moved = false;
@@ -412,10 +374,11 @@ __global__ void __launch_bounds__(192, 1)
         ls += sv[i];
       }
       l_sum = l_sum * alpha + ls;
-      // rescale this warp's rows of O once the previous P V has landed
+      // rescale this warp's rows of O once the previous P V has landed (the
+      // commit of P_i V_i completes phase i / NSLOT of slot i % NSLOT)
       if (__any_sync(0xffffffffu, moved)) {
         int ok2 = 1;
-        if (lane == 0) ok2 = mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1u, abort, err) ? 1 : 0;
+        if (lane == 0) ok2 = mbar_wait(&bars->empty[(j - 1) % NSLOT], ((j - 1) / NSLOT) & 1u, abort, err) ? 1 : 0;
         ok2 = __shfl_sync(0xffffffffu, ok2, 0);
         if (!ok2) break;
         tc_fence_after();
@@ -457,15 +420,21 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[sb]);
+      int okv = 1;
+      if (lane == 0) {   // P_j written and V_j landed: P_j V_j may go
+        okv = mbar_wait(&bars->v_full[j % NSLOT], (j / NSLOT) & 1u, abort, err) ? 1 : 0;
+        if (okv) mbar_arrive(&bars->p_full[sb]);
+      }
+      okv = __shfl_sync(0xffffffffu, okv, 0);
+      if (!okv) break;
     }
   }
 
-  // ---- partials of this CTA into the drained K/V rings:
+  // ---- partials of this CTA into the drained ring:
   //   po[m][PLD] fp32 O row of MMA row m = g * QP + r, pml[m] = (m_ref, l)
   tc_fence_before();
   __syncthreads();
-  float* po = reinterpret_cast<float*>(sm + S::OFF_K);
+  float* po = reinterpret_cast<float*>(sm + S::OFF_RING);
   float* pml = po + QROWS * S::PLD;
   float* wts = pml + QROWS * 2;                           // [QROWS][8] merge weights
   if (warp >= 2) {
@@ -473,7 +442,8 @@ __global__ void __launch_bounds__(192, 1)
     const int m = wq * 32 + lane, r = m % QP;
     if (n_tiles > 0) {
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&bars->pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1u, abort, err) ? 1 : 0;
+      if (lane == 0)
+        ok = mbar_wait(&bars->empty[(n_tiles - 1) % NSLOT], ((n_tiles - 1) / NSLOT) & 1u, abort, err) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       tc_fence_after();
       const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
@@ -495,23 +465,36 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
   __syncthreads();
-  // replicas of a query share m_ref: sum their O and l into replica 0's row
+  // a query's replicas: weight each by 2^(m_g - M) and sum O and l into
+  // replica 0's row, whose reference becomes M
   if constexpr (R > 1) {
-    for (int e = tid; e < q_len * (DH / 4); e += 192) {
-      const int r = e / (DH / 4), c = (e % (DH / 4)) * 4;
-      float4 acc = *reinterpret_cast<const float4*>(po + r * S::PLD + c);
-#pragma unroll
-      for (int g = 1; g < R; ++g) {
-        const float4 v = *reinterpret_cast<const float4*>(po + (g * QP + r) * S::PLD + c);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      }
-      *reinterpret_cast<float4*>(po + r * S::PLD + c) = acc;
-    }
     for (int r = tid; r < q_len; r += 192) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int g = 0; g < R; ++g) M = fmaxf(M, pml[(g * QP + r) * 2]);
       float l = 0.f;
 #pragma unroll
-      for (int g = 0; g < R; ++g) l += pml[(g * QP + r) * 2 + 1];
+      for (int g = 0; g < R; ++g) {
+        const float mg = pml[(g * QP + r) * 2];
+        const float w = mg == -INFINITY ? 0.f : exp2f(mg - M);
+        wts[r * 8 + g] = w;
+        l += w * pml[(g * QP + r) * 2 + 1];
+      }
+      pml[r * 2] = M;
       pml[r * 2 + 1] = l;
+    }
+    __syncthreads();
+    for (int e = tid; e < q_len * (DH / 4); e += 192) {
+      const int r = e / (DH / 4), c = (e % (DH / 4)) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int g = 0; g < R; ++g) {
+        const float w = wts[r * 8 + g];
+        const float4 v = *reinterpret_cast<const float4*>(po + (g * QP + r) * S::PLD + c);
+        acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
+      }
+      *reinterpret_cast<float4*>(po + r * S::PLD + c) = acc;
     }
   }
   tc_fence_before();
