@@ -163,7 +163,7 @@ __device__ void compact_words(const uint32_t* __restrict__ words, int nw, int L,
 
 // Stable-Window-Decoding update of the active block of sequence blockIdx.x,
 // then one flag bit per position for the next step's refresh set.
-__global__ void __launch_bounds__(1024) swd_kernel(
+__global__ void __launch_bounds__(1024, 1) swd_kernel(
     const int* __restrict__ argmax, const float* __restrict__ p1, int* __restrict__ tok,
     uint8_t* __restrict__ stable, int* __restrict__ hist_tok, float* __restrict__ hist_p, int* __restrict__ hist_n,
     const int* __restrict__ tok_w, const int* __restrict__ version, uint32_t* __restrict__ words, int L, int Lw,
@@ -179,22 +179,51 @@ __global__ void __launch_bounds__(1024) swd_kernel(
     const int j = threadIdx.x;
     const int r = b * L + q0 + j;
     const int h = b * blk + j;
+    // every load of this row's state at once: its ring of K <= 8 records
+    // stays in registers, so nothing written here is read back
+    constexpr int KMAX = 8;
     bool st = stable[r] != 0;
     const int a = argmax[h];
+    const float pa = p1[h];
+    int n = hist_n[h];
+    int ht[KMAX];
+    float hp[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      if (k < K) {
+        ht[k] = hist_tok[h * K + k];
+        hp[k] = hist_p[h * K + k];
+      }
     if (!st) {
-      int n = hist_n[h];
-      hist_tok[h * K + n % K] = a;
-      hist_p[h * K + n % K] = p1[h];
+      const int slot_new = n % K;
+      hist_tok[h * K + slot_new] = a;
+      hist_p[h * K + slot_new] = pa;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if (k == slot_new) {
+          ht[k] = a;
+          hp[k] = pa;
+        }
       ++n;
       hist_n[h] = n;
       if (n >= K) {
         bool same = true;
         float s = 0.f;
-        for (int k = 0; k < K; ++k) {        // oldest -> newest
-          const int slot = (n - K + k) % K;
-          same = same && hist_tok[h * K + slot] == a;
-          s = s + hist_p[h * K + slot];
-        }
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)      // oldest -> newest: slot (n - K + k) % K
+          if (k < K) {
+            const int slot = (n - K + k) % K;
+            int tk = 0;
+            float pk = 0.f;
+#pragma unroll
+            for (int u = 0; u < KMAX; ++u)
+              if (u == slot) {
+                tk = ht[u];
+                pk = hp[u];
+              }
+            same = same && tk == a;
+            s = s + pk;
+          }
         const float mean = s / static_cast<float>(K);
         if (same && mean > tau) {
           st = true;
@@ -218,12 +247,17 @@ __global__ void __launch_bounds__(1024) swd_kernel(
       if (last) {
         f = true;
       } else {
-        const int lo = max(p - R, q0), hi = min(p + R, q0 + nac - 1);
-        for (int u = lo; u <= hi; ++u) f = f || s_unst[u - q0];
-        if (refresh_active && p >= q0 && p < q0 + nac) f = true;
-        f = f || tok[r] != tok_w[r];
+        // independent loads (no short-circuit between them): any layer's
+        // version expired <=> the oldest one did
+        const int tk = tok[r], tw = tok_w[r];
+        int vmin = 0x7fffffff;
         if (expiry >= 0)
-          for (int l = 0; l < n_layers; ++l) f = f || (t + 1) - version[l * seq_rows + r] > expiry;
+          for (int l = 0; l < n_layers; ++l) vmin = min(vmin, version[l * seq_rows + r]);
+        const int lo = max(p - R, q0), hi = min(p + R, q0 + nac - 1);
+        for (int u = lo; u <= hi; ++u) f |= s_unst[u - q0] != 0;
+        if (refresh_active && p >= q0 && p < q0 + nac) f = true;
+        f |= tk != tw;
+        if (expiry >= 0) f |= (t + 1) - vmin > expiry;
       }
     }
     const uint32_t word = __ballot_sync(0xffffffffu, f);
