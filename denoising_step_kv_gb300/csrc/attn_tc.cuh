@@ -174,6 +174,12 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Bring `bytes` (a multiple of 16) at a 16-byte aligned address into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
 // Ql, Kl, Vl: the layer's tiled Q/K/V caches (KvLayout kv).  Queries are
 // positions [q_pos0, q_pos0 + q_len) of sequence blockIdx.z, keys/values its
 // positions [0, kv_len); out [n_seq][q_len][ld] bf16.
@@ -219,6 +225,13 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
+  // K and V of the first two tiles into L2 while the projection may still
+  // run (it writes only the refreshed rows, and L2 is where they meet): one
+  // bulk prefetch per warp, as one warp's bulk operations issue one by one
+  if (warp >= 2 && lane == 0) {
+    const int j = (warp - 2) >> 1;
+    if (j < n_tiles) bulk_prefetch_l2(((warp & 1) ? Vl : Kl) + kv.tile_off(b, h, k_begin + j * KT), S::KV_TILE);
+  }
   pdl_launch();
   pdl_wait();     // the cache rows of this step are written by the projection
 
