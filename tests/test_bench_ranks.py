@@ -1,0 +1,72 @@
+"""The bench's multi-rank host logic on CPU: two gloo ranks agree on the
+slowest rank's time, and the whole-job rate counts every rank's units over
+it.  Each rank gets its own prompts but the same model, and the reference arm
+prints on rank 0 only."""
+import os
+import socket
+import sys
+from types import SimpleNamespace
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from workloads import configs as C  # noqa: E402
+from workloads import generate as G  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, ms, q):
+    import torch.distributed as dist
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        slowest = bench.max_over_ranks(ms[rank], world, "cpu")
+        q.put((rank, slowest, bench.whole_job_rate(128, world, slowest)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_take_the_slowest_time():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port, ms = _free_port(), [12.5, 30.0]
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, ms, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, slowest, rate in got:
+        assert slowest == 30.0
+        assert rate == 2 * 128 / 0.030
+
+
+def test_one_rank_needs_no_process_group():
+    assert bench.max_over_ranks(7.0, 1, "cpu") == 7.0
+    assert bench.whole_job_rate(100, 1, 50.0) == 2000.0
+
+
+def test_ranks_share_the_model_not_the_prompts():
+    w = C.get("mid_bf16")
+    w0, w1 = bench.rank_workload(w, 0), bench.rank_workload(w, 1)
+    assert w0 == w
+    assert not np.array_equal(G.prompt_tokens(w0), G.prompt_tokens(w1))
+    # everything but the seed (the shapes, the model's scale, the schedule)
+    # is the base workload's; the bench draws the weights from the base
+    assert w1.seed != w.seed and bench.replace(w1, seed=w.seed) == w
+
+
+def test_reference_arm_prints_on_rank_zero_only(capsys):
+    args = SimpleNamespace(gpus=2, steps=1, warmup=0)
+    bench.reference_arm(args, C.get("tiny_fp32"), 1)
+    assert capsys.readouterr().out == ""
