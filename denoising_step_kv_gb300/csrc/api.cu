@@ -418,7 +418,7 @@ dllm_status lmhead_conf(dllm_cache* c, const void* h_dev, const void* w_lm_dev, 
   if (!aligned16(h_dev) || !aligned16(w_lm_dev)) return fail(DLLM_EINVAL, "lmhead_conf: pointers not 16-byte aligned");
   if (M == 0) return DLLM_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int n_tiles = cdiv(V, lm_tile_cols(c, M));
+  const int n_tiles = cdiv(V, lm_tile_cols(c, M, V));
   DLLM_LAUNCH(launch_rownorm(c, h_dev, M, nullptr, d, c->lm_rs, st), "lmhead_conf: norm");
   {
     ProfScope prof(c, DLLM_PROF_LM_GEMM, st);

@@ -351,34 +351,39 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // Shared-A kernel for few rows and many output columns (the LM head):
-// persistent clusters of CS CTAs on CS adjacent 128 x 128 tiles of the same
+// persistent clusters of CS CTAs on CS adjacent 128 x SBN tiles of the same
 // 128 rows.  Each CTA loads its own weight tile and a 128/CS-row piece of the
 // rows' tile, multicast into every CTA of the cluster, so the rows are read
 // once per cluster instead of once per CTA.  A stage is reloaded once all CS
 // CTAs' MMAs have read it (every commit arrives on all CS empty barriers).
 // The row count is a host value: before the grid dependency each CTA warms
-// L2 with its first weight tile, which no earlier kernel writes.
-template <int STAGES>
-constexpr size_t sharea_smem_bytes() { return 1024 + STAGES * STAGE_BYTES + sizeof(Bars); }
+// L2 with the first PREF k-blocks of its first weight tile, which no earlier
+// kernel writes.  With SBN = 256, one CTA per SM keeps four stages of 32 KB
+// of weights in flight.
+template <int STAGES, int SBN>
+constexpr size_t sharea_smem_bytes() { return 1024 + STAGES * (A_BYTES + SBN * BK * 2) + sizeof(Bars); }
 
-template <class Epi, int STAGES, int CS>
+template <class Epi, int STAGES, int CS, int SBN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_sharea_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M,
                        int N, int K, Epi epi, unsigned* err) {
   static_assert(CS == 2 || CS == 4, "the rows' tile splits into CS whole 8-row swizzle groups");
+  static_assert(SBN == 128 || SBN == 256, "one MMA per 16-deep slice (N <= 256)");
+  constexpr int SB_BYTES = SBN * BK * 2, S_BYTES = A_BYTES + SB_BYTES, PREF = 8;
+  constexpr uint32_t S_TMEM = 2 * SBN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint8_t* sa = smem;
   uint8_t* sb = smem + STAGES * A_BYTES;
-  Bars* bars = reinterpret_cast<Bars*>(smem + STAGES * STAGE_BYTES);
+  Bars* bars = reinterpret_cast<Bars*>(smem + STAGES * S_BYTES);
   constexpr uint16_t ALL = (1u << CS) - 1;
   constexpr int PIECE = BM / CS;                  // rows of the shared tile each CTA loads
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = static_cast<int>(cluster_rank());
   const int cl = blockIdx.x / CS, n_cl = gridDim.x / CS;
-  const int nM = (M + BM - 1) / BM, nN = (N + BN - 1) / BN, nK = (K + BK - 1) / BK;
+  const int nM = (M + BM - 1) / BM, nN = (N + SBN - 1) / SBN, nK = (K + BK - 1) / BK;
   const int nG = (nN + CS - 1) / CS;
   const int tiles = M > 0 ? nM * nG : 0;          // cluster tiles (row tile, group of CS column tiles)
 
@@ -395,14 +400,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     bars->abort = 0;
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(&bars->tmem, TMEM_COLS);
+  if (warp == 1) tmem_alloc(&bars->tmem, S_TMEM);
   if (threadIdx.x == 32) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     if (cl < tiles) {
       const int nb = (cl / nM) * CS + rank;
       if (nb < nN)
-        for (int kb = 0; kb < nK; ++kb) tma_prefetch_l2_2d(&tmB, kb * BK, nb * BN);
+        for (int kb = 0; kb < min(nK, PREF); ++kb) tma_prefetch_l2_2d(&tmB, kb * BK, nb * SBN);
     }
   }
   tc_fence_before();
@@ -422,10 +427,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int mb = tile % nM, nb = (tile / nM) * CS + rank;
         for (int kb = 0; kb < nK; ++kb) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort, err)) break;
-          mbar_expect_tx(&bars->full[stage], STAGE_BYTES);
+          mbar_expect_tx(&bars->full[stage], S_BYTES);
           tma_load_2d_mc(sa + stage * A_BYTES + rank * (PIECE * 128), &tmA, kb * BK, mb * BM + rank * PIECE,
                          &bars->full[stage], ALL);
-          tma_load_2d(sb + stage * B_BYTES, &tmB, kb * BK, nb * BN, &bars->full[stage]);
+          tma_load_2d(sb + stage * SB_BYTES, &tmB, kb * BK, nb * SBN, &bars->full[stage]);
           issued |= 1u << stage;
           par = (par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -441,13 +446,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(BM, BN);
+      const uint32_t idesc = idesc_bf16(BM, SBN);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       for (int tile = cl; tile < tiles && !*abort; tile += n_cl) {
         if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1u, abort, err)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * SBN);
         bool ok = true;
         for (int kb = 0; kb < nK; ++kb) {
           if (!mbar_wait(&bars->full[stage], phase, abort, err)) {
@@ -455,7 +460,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sa + stage * A_BYTES), b0 = smem_u32(sb + stage * B_BYTES);
+          const uint32_t a0 = smem_u32(sa + stage * A_BYTES), b0 = smem_u32(sb + stage * SB_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             tc_mma_bf16(d_tmem, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc,
@@ -491,8 +496,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int mb = tile % nM, nb = (tile / nM) * CS + rank;
       if (nb < nN) {   // the last group may run past the columns
         const int m = mb * BM + q * 32 + lane;
-        TmemLoader ld{tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN)};
-        epi.run(m, nb * BN, BN / 32, M, N, ld);
+        TmemLoader ld{tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * SBN)};
+        epi.run(m, nb * SBN, SBN / 32, M, N, ld);
       }
       tc_fence_before();
       __syncwarp();
@@ -508,7 +513,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   cluster_barrier();       // no multicast copy or commit still targets this CTA
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc(tmem, S_TMEM);
   }
 }
 

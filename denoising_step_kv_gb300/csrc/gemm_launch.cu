@@ -44,23 +44,24 @@ cudaError_t launch_pair(dllm_cache* c, const CUtensorMap& ta, const CUtensorMap&
                    M_host, M_dev, a_rows, M_min, N, K, epi, c->err);
 }
 
-template <class Epi, int STAGES, int CS>
+template <class Epi, int STAGES, int CS, int SBN>
 cudaError_t launch_sharea(dllm_cache* c, const void* A, int M, const void* B, int N, int K, const Epi& epi,
                           cudaStream_t st) {
-  constexpr size_t smem = tc::sharea_smem_bytes<STAGES>();
+  constexpr size_t smem = tc::sharea_smem_bytes<STAGES, SBN>();
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = set_smem(tc::gemm_sharea_kernel<Epi, STAGES, CS>, smem);
+    cudaError_t e = set_smem(tc::gemm_sharea_kernel<Epi, STAGES, CS, SBN>, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   CUtensorMap ta, tb;
   if (!make_tmap_2d(&ta, A, K, M, static_cast<uint64_t>(K) * 2, tc::BK, tc::BM / CS, true) ||
-      !make_tmap_2d(&tb, B, K, N, static_cast<uint64_t>(K) * 2, tc::BK, tc::BN, true))
+      !make_tmap_2d(&tb, B, K, N, static_cast<uint64_t>(K) * 2, tc::BK, SBN, true))
     return cudaErrorInvalidValue;
-  const int tiles = cdiv(M, tc::BM) * cdiv(cdiv(N, tc::BN), CS);
-  const int clusters = std::max(1, std::min(tiles, 2 * c->num_sms / CS));
-  return launch_ex(tc::gemm_sharea_kernel<Epi, STAGES, CS>, dim3(CS * clusters), dim3(tc::THREADS), smem, st, CS, ta,
+  const int tiles = cdiv(M, tc::BM) * cdiv(cdiv(N, SBN), CS);
+  const int per_sm = 2 * tc::sharea_smem_bytes<STAGES, SBN>() <= 227 * 1024 ? 2 : 1;
+  const int clusters = std::max(1, std::min(tiles, per_sm * c->num_sms / CS));
+  return launch_ex(tc::gemm_sharea_kernel<Epi, STAGES, CS, SBN>, dim3(CS * clusters), dim3(tc::THREADS), smem, st, CS, ta,
                    tb, M, N, K, epi, c->err);
 }
 
@@ -218,7 +219,12 @@ cudaError_t qkv_dh(dllm_cache* c, int layer, const void* A, int M_cap, const int
 
 // Vocab columns per LM-head partial: 256 when the pair kernel runs (more
 // than one 128-row tile: two row tiles share each weight tile), else 128.
-int lm_tile_cols(const dllm_cache* c, int M) { return c->cfg.dtype == DLLM_BF16 && M > tc::BM ? tc::PBN : tc::BN; }
+// Vocab columns per partial of the LM head: 256 on the pair kernel (M > 128)
+// and on the shared-A kernel (M <= 128, at least 8 such tiles), else 128.
+int lm_tile_cols(const dllm_cache* c, int M, int V) {
+  if (c->cfg.dtype != DLLM_BF16) return tc::BN;
+  return M > tc::BM || (M > 0 && cdiv(V, tc::PBN) >= 8) ? tc::PBN : tc::BN;
+}
 
 cudaError_t gemm_qkv(dllm_cache* c, int layer, const void* A, int M_cap, const int* M_dev, const int* rows,
                      const void* w_qkv, cudaStream_t st) {
@@ -269,8 +275,9 @@ cudaError_t gemm_lm(dllm_cache* c, const void* A, const void* W, int M, int V, i
         return cudaErrorInvalidValue;
       return launch_pair<EpiLM, 4>(c, ta, tb, M, M, nullptr, 0, V, d, e, st);
     }
-    // one row tile, many vocab tiles: clusters of 4 share the rows' tile
-    if (M > 0 && cdiv(V, tc::BN) >= 8) return launch_sharea<EpiLM, 3, 4>(c, A, M, W, V, d, e, st);
+    // one row tile, many vocab tiles: clusters of 4 share the rows' tile,
+    // one 128 x 256 tile per CTA and SM
+    if (M > 0 && cdiv(V, tc::PBN) >= 8) return launch_sharea<EpiLM, 4, 4, tc::PBN>(c, A, M, W, V, d, e, st);
     return run_tc(c, A, M, M, nullptr, W, V, d, e, st);
   }
   return run_simt<4>(A, M, M, nullptr, W, V, d, e, st);
