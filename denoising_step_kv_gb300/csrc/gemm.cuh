@@ -548,8 +548,6 @@ constexpr size_t SKN_SMEM = 1024 + SKN_RING + sizeof(SknBars);
 // pushes (a lane per column, four rows each) spread over all banks.
 __host__ __device__ constexpr int skn_tpr(int M, int S) { return ((M + S - 1) / S + 3) & ~3; }
 __host__ __device__ constexpr int skn_ldr(int tpr) { return (tpr / 4) % 2 ? tpr : tpr + 4; }
-static_assert(8 * 128 * skn_ldr(skn_tpr(SKN_MAX_ROWS, 8)) * 4 <= SKN_RING, "receive buffer fits in the ring");
-static_assert(6 * 128 * skn_ldr(skn_tpr(SKN_MAX_ROWS, 6)) * 4 <= SKN_RING, "receive buffer fits in the ring");
 static_assert(4 * 128 * skn_ldr(skn_tpr(SKN_MAX_ROWS, 4)) * 4 <= SKN_RING, "receive buffer fits in the ring");
 static_assert(3 * 128 * skn_ldr(skn_tpr(SKN_MAX_ROWS, 3)) * 4 <= SKN_RING, "receive buffer fits in the ring");
 static_assert(2 * 128 * skn_ldr(skn_tpr(SKN_MAX_ROWS, 2)) * 4 <= SKN_RING, "receive buffer fits in the ring");

@@ -110,13 +110,14 @@ int skinny_resident(dllm_cache* c) {
   return n;
 }
 
-// Split of K for the weight-streaming kernel: the largest whose clusters
-// (one per 128 output columns) are all resident at once, 0 if none is.
+// Split of K for the weight-streaming kernel: the largest, up to 4, whose
+// clusters (one per 128 output columns) are all resident at once, 0 if none
+// is.  Past 4 the exchange of the partials costs more than the extra CTAs
+// gain (W_o at 128 rows, d = 2048, L2 flushed: 19.1 us with 6 ranks, 17.0
+// with 4 or 3).
 template <class Epi>
 int skinny_split(dllm_cache* c, int N) {
   const int nN = cdiv(N, 128);
-  if (nN <= skinny_resident<Epi, 8>(c)) return 8;
-  if (nN <= skinny_resident<Epi, 6>(c)) return 6;
   if (nN <= skinny_resident<Epi, 4>(c)) return 4;
   if (nN <= skinny_resident<Epi, 3>(c)) return 3;
   if (nN <= skinny_resident<Epi, 2>(c)) return 2;
@@ -128,8 +129,6 @@ template <class Epi>
 cudaError_t run_skinny(dllm_cache* c, int split, const void* A, int a_rows, int M_host, const int* M_dev,
                        const void* W, int N, int K, const Epi& epi, cudaStream_t st) {
   switch (split) {
-    case 8: return launch_skinny<Epi, 8>(c, A, a_rows, M_host, M_dev, W, N, K, epi, st);
-    case 6: return launch_skinny<Epi, 6>(c, A, a_rows, M_host, M_dev, W, N, K, epi, st);
     case 4: return launch_skinny<Epi, 4>(c, A, a_rows, M_host, M_dev, W, N, K, epi, st);
     case 3: return launch_skinny<Epi, 3>(c, A, a_rows, M_host, M_dev, W, N, K, epi, st);
     case 2: return launch_skinny<Epi, 2>(c, A, a_rows, M_host, M_dev, W, N, K, epi, st);
