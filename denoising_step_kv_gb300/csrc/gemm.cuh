@@ -1,12 +1,14 @@
 // D = A . B^T for K-major A [M][K] (rows) and B [N][K] (weights), finished
 // by an epilogue functor that receives one output row of a tile at a time.
 //
-// bf16, three tcgen05 kernels (TMA loads with 128-byte swizzle into an
+// bf16, four tcgen05 kernels (TMA loads with 128-byte swizzle into an
 // mbarrier ring, one thread issuing the MMAs, fp32 accumulators in TMEM):
 //   gemm_tc_kernel      persistent, 128 x 128 tiles, two TMEM accumulators so
 //                       the epilogue of one tile overlaps the next tile's MMAs;
 //   gemm_pair_kernel    the same with clusters of two CTAs on 128 x 256 tiles
 //                       that share (multicast) the weight tile - large M;
+//   gemm_sharea_kernel  clusters of CTAs on adjacent weight tiles of the same
+//                       128 rows, which they share (multicast) - the LM head;
 //   gemm_skinny_kernel  weights as the MMA's A operand, the few rows as its B
 //                       operand, K split over a cluster - M <= 256, weight
 //                       streaming.
