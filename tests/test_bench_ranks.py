@@ -70,3 +70,11 @@ def test_reference_arm_prints_on_rank_zero_only(capsys):
     args = SimpleNamespace(gpus=2, steps=1, warmup=0)
     bench.reference_arm(args, C.get("tiny_fp32"), 1)
     assert capsys.readouterr().out == ""
+
+
+def test_profile_hash_ignores_comments_only():
+    a = "int f(int x) {  // the sum\n  return x + 1; /* one\n more */ }\n"
+    b = "int f(int x) {\n  return x + 1;\n}\n"
+    c = "int f(int x) {\n  return x + 2;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(b) != bench._code_only(c)
