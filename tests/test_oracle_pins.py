@@ -402,3 +402,21 @@ def test_sharp_variants_exercise_swd():
         w, W, tok0 = _load(name)
         tr = O.run_dense(w, W, tok0, mode="cached")
         assert sum(int(r["newly"].sum()) for r in tr) >= 8, name
+
+
+# --- the multi-layer quality figure (cached loop against full recompute) -----
+def test_drift_is_zero_where_the_cache_is_exact():
+    """Reuse is exact in the first layer, so a one-layer model drifts nowhere;
+    with several layers nothing drifts while no token changes inside a block
+    (the stale deeper-layer K/V then equal the recomputed ones), and every
+    block's first step is a full refresh in both loops."""
+    from oracle.drift import drift
+    for name in ("mid_bf16_sharp", "mid_multi"):
+        w = C.get(name)
+        steps, tok_agree, first = drift(w, G.model(w), G.prompt_tokens(w))
+        assert all(r["max_dp1"] == 0.0 and r["argmax_agree"] == 1.0 for r in steps), name
+        assert tok_agree == 1.0 and first is None, name
+    w = C.get("mid_multi_sharp")
+    steps, _, _ = drift(w, G.model(w), G.prompt_tokens(w))
+    assert all(r["max_dp1"] == 0.0 for r in steps if r["s"] == 0)
+    assert any(r["max_dp1"] > 0.0 for r in steps)          # commits inside a block: stale K/V
