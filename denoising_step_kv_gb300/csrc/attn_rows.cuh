@@ -14,9 +14,10 @@
 // online softmax, one query of 64 keys per thread per tile, and after the
 // last tile normalise O and store it.  The barrier phases run on a tile
 // counter shared by all items of the CTA.  Unlike attn_tc_kernel, whose
-// issuing thread limits it, this kernel is bound by its softmax: the fixed
-// issue order with one K+V ring measured slower here (full 12-layer step,
-// 16 x 2048 rows: 1274 against 1109 us per layer).
+// issuing thread limits it, this kernel is bound by its softmax: a fixed
+// issue order with one K+V ring and P in TMEM buffers of its own measured
+// slower here (all 16 x 2048 rows of a 64-dim layer: 1202-1274 against
+// 1109 us).
 #pragma once
 #include "attn_tc.cuh"
 
