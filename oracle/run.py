@@ -16,9 +16,11 @@ Sources, cited by page title and section:
 
 Two dense modes:
   * ``cached``: explicit per-layer Q/K/V caches with versions; only the refresh
-    set is recomputed (single-layer: exactly the method; multi-layer: the rows
-    P = refresh set pass through every layer and all other rows' deeper-layer
-    K/V stay as cached);
+    set Rf is recomputed (single-layer: exactly the method; multi-layer: the
+    rows P = Rf, plus the active block when the workload asks for active
+    queries, pass through every layer as queries; only the rows of Rf rewrite
+    their K/V and version, so the stability mask gates the per-layer refresh,
+    and every other row's deeper-layer K/V stays as cached);
   * ``recompute``: the plain definition, a full forward of every row every step.
 For one layer the two agree bit for bit (tested).
 """
@@ -38,12 +40,14 @@ def weights_f64(w, m):
     return {k: ([conv(x) for x in v] if isinstance(v, list) else conv(v)) for k, v in m.items()}
 
 
-def _layer_stack(w, W, x, pos_rows, rows_flat, caches):
+def _layer_stack(w, W, x, pos_rows, rows_flat, caches, write_kv=None):
     """Run rows through every layer of the cached algorithm.
 
     x: [n, d] layer-0 input of the rows; rows_flat: their flat ids b*L+pos.
-    Writes each layer's Q/K/V for the rows into ``caches``; queries are the rows
-    themselves.  Returns (last O stored [n, d], final hidden [n, d]).
+    write_kv: bool [n], the rows that rewrite their K/V (the refresh set);
+    None = every row.  Every row's Q is computed and stored; the queries are
+    the rows themselves and attend over the layer's cache after this layer's
+    K/V writes.  Returns (last O stored [n, d], final hidden [n, d]).
     """
     B, L, H = w.batch, w.seq_len, w.n_heads
     b_of = rows_flat // L
@@ -51,9 +55,10 @@ def _layer_stack(w, W, x, pos_rows, rows_flat, caches):
     for l in range(w.n_layers):
         q, k, v = M.project_qkv(x, W["w_qkv"][l], pos_rows, H, w.dtype, w.rope_theta, w.rms_eps)
         Qc, Kc, Vc = caches
+        wr = np.ones(len(rows_flat), dtype=bool) if write_kv is None else write_kv
         Qc[l].reshape(B * L, H, -1)[rows_flat] = q
-        Kc[l].reshape(B * L, H, -1)[rows_flat] = k
-        Vc[l].reshape(B * L, H, -1)[rows_flat] = v
+        Kc[l].reshape(B * L, H, -1)[rows_flat[wr]] = k[wr]
+        Vc[l].reshape(B * L, H, -1)[rows_flat[wr]] = v[wr]
         o = np.zeros_like(q)
         for b in range(B):
             sel = b_of == b
@@ -101,7 +106,7 @@ def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre
                               "tok_w": tok_w.copy(), "swd": swd.copy(),
                               "caches": tuple(c.copy() for c in caches)}
             full = s == 0 or force_all or mode == "recompute"
-            rows = flat_all if full else rows_next
+            rows = flat_all if full else rows_next          # the refresh set Rf
             rec["rows"] = rows.copy()
             # layer-0 bookkeeping of the refreshed rows
             version[:, rows // L, rows % L] = t
@@ -121,9 +126,11 @@ def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre
                 o_ac = M.round_store(o.reshape(B * blk, d), w.dtype)
                 h_ac = M.out_proj(o_ac, W["w_o"][0], x_emb[ac_flat], w.dtype)
             else:
-                o_p, h_p = _layer_stack(w, W, x_emb[rows], rows % L, rows, caches)
-                where = np.searchsorted(rows, ac_flat)
-                assert np.array_equal(rows[where], ac_flat), "active rows must be refreshed"
+                P = _query_rows(w, rows, ac_flat)
+                rec["queries"] = P.copy()
+                o_p, h_p = _layer_stack(w, W, x_emb[P], P % L, P, caches, np.isin(P, rows))
+                where = np.searchsorted(P, ac_flat)
+                assert np.array_equal(P[where], ac_flat), "active rows must pass through the layers"
                 o_ac, h_ac = o_p[where], h_p[where]
             am, p1, ent, margin = M.lm_head_conf(h_ac, W["w_lm"], w.mask_id, w.rms_eps)
             am, p1 = am.reshape(B, blk), p1.reshape(B, blk)
@@ -135,13 +142,24 @@ def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre
                 swd.reset()
                 rows_next = flat_all
             else:
-                rows_next = refresh_rows(stable, tok, tok_w, version, q0, blk, w.swd_R, t + 1,
-                                         w.expiry, bool(w.refresh_active))
+                rows_next = refresh_rows(stable, tok, tok_w, version, q0, blk, w.swd_R, t + 1, w.expiry)
+            # the row list the next step runs on: Rf, plus the active block
+            # when every active row queries (the next step is in this block
+            # unless this was its last step, and then Rf is every row)
             rec.update(tok=tok.copy(), stable=stable.copy(), version=version.copy(),
-                       tok_w=tok_w.copy(), swd=swd.copy(), rows_next=rows_next.copy())
+                       tok_w=tok_w.copy(), swd=swd.copy(), rf_next=rows_next.copy(),
+                       rows_next=_query_rows(w, rows_next, ac_flat))
             trace.append(rec)
             t += 1
     return trace
+
+
+def _query_rows(w, rf, ac_flat):
+    """Rows that pass through the layers: the refresh set, plus the active
+    block when the workload runs every active row as a query."""
+    if not w.active_queries or len(rf) == w.batch * w.seq_len:
+        return rf.copy()
+    return np.union1d(rf, ac_flat).astype(rf.dtype)
 
 
 def _recompute_step(w, W, x_emb, pos_all, ac_flat):

@@ -28,8 +28,7 @@ Readings (also listed in the design notes):
     options it offers; the other, ending, is what a fixed Tb gives);
   * t is the global step counter; refresh set for step t+1 =
       dilate_R(unstable) U {p : tok[p] != token the entry was computed from}
-      U {p : (t+1) - version[p] > expiry}  (U the active block when the
-      workload asks every active row to be recomputed).
+      U {p : (t+1) - version[p] > expiry}.
 """
 import numpy as np
 
@@ -116,16 +115,13 @@ def expired_rows(version, t, expiry):
     return np.any(t - version > expiry, axis=0)
 
 
-def refresh_rows(stable, tok, tok_w, version, q0, blk, R, t_next, expiry,
-                 refresh_active=False):
+def refresh_rows(stable, tok, tok_w, version, q0, blk, R, t_next, expiry):
     """Refresh set for step t_next as sorted flat row indices b*L + pos."""
     B, L = tok.shape
     rf = np.zeros((B, L), dtype=bool)
     for b in range(B):
         unstable = [q0 + j for j in range(blk) if not stable[b, q0 + j]]
         rf[b] |= dilate(unstable, R, L)
-        if refresh_active:
-            rf[b, q0:q0 + blk] = True
     rf |= tok != tok_w
     rf |= expired_rows(version, t_next, expiry)
     return np.flatnonzero(rf.reshape(-1)).astype(np.int32)

@@ -138,6 +138,65 @@ def test_out_proj_and_ffn_reduce():
     assert np.array_equal(O.ffn(x, np.ones((4, 8)), np.zeros((8, 4)), "bf16"), x)
 
 
+def _bf16_rne(x):
+    """Round one float to bf16 (8 significant bits, ties to even), written
+    from frexp and Python's round() (which rounds halves to even)."""
+    if x == 0.0 or not math.isfinite(x):
+        return x
+    m, e = math.frexp(x)                 # x = m * 2^e, 0.5 <= |m| < 1
+    return round(m * 256.0) / 256.0 * 2.0 ** e
+
+
+def _gelu_erf(x):
+    return 0.5 * x * (1.0 + math.erf(x / math.sqrt(2.0)))
+
+
+def test_ffn_closed_form_with_selection_weights():
+    """FFN = h + W2 . store(GELU(W1 . RMSNorm(h))) pinned by weights that
+    select entries: W1 row j picks input a[j] (rows past d are zero), W2 row i
+    adds 2 f[b[i]] - f[c[i]].  The expected rows come from scalar code; the
+    alternatives that a slip would give (no norm, GELU after W2, no bf16 store
+    of the GELU output, a transposed W1) differ from it."""
+    d, F, n = 64, 96, 6
+    rng = np.random.default_rng(77)
+    h = O.round_store(rng.standard_normal((n, d)) * 3.0, "bf16")
+    a = rng.permutation(d)
+    b = rng.permutation(d)
+    c = (b + 1 + rng.integers(0, d - 1, d)) % d          # c[i] != b[i]
+    w1 = np.zeros((F, d))
+    w1[np.arange(d), a] = 1.0
+    w2 = np.zeros((d, F))
+    w2[np.arange(d), b] = 2.0
+    w2[np.arange(d), c] = -1.0
+    got = O.ffn(h, w1, w2, "bf16", eps=1e-6)
+
+    def expect(norm=True, store=True, gelu_after=False, w1_t=False):
+        out = np.zeros((n, d))
+        pick = np.argsort(a) if w1_t else a
+        for r in range(n):
+            row = [float(x) for x in h[r]]
+            scale = 1.0 / math.sqrt(math.fsum(x * x for x in row) / d + 1e-6) if norm else 1.0
+            x1 = [scale * row[pick[j]] for j in range(d)]     # W1 . (norm h), first d rows
+            if gelu_after:
+                f = [2.0 * x1[b[i]] - x1[c[i]] for i in range(d)]
+                out[r] = [_bf16_rne(row[i] + _gelu_erf(f[i])) for i in range(d)]
+                continue
+            g = [_gelu_erf(v) for v in x1]
+            g = [_bf16_rne(v) for v in g] if store else g
+            out[r] = [_bf16_rne(row[i] + 2.0 * g[b[i]] - g[c[i]]) for i in range(d)]
+        return out
+
+    want = expect()
+    assert np.array_equal(got, want)
+    for slip in (dict(norm=False), dict(store=False), dict(gelu_after=True), dict(w1_t=True)):
+        assert not np.array_equal(expect(**slip), want), slip
+
+
+def test_bf16_scalar_rounding_agrees_with_the_oracle():
+    x = RNG.standard_normal(2000) * np.exp(RNG.uniform(-10, 10, 2000))
+    assert np.array_equal(O.round_store(x, "bf16"), np.array([_bf16_rne(float(v)) for v in x]))
+
+
 # --- LM head confidence ----------------------------------------------------------------------
 def test_lm_head_uniform_logits():
     V = 50
@@ -302,8 +361,35 @@ def test_refresh_rows_composition():
     version[0, 0, 11] = 7                # expired at t=10 with expiry 2
     rows = O.refresh_rows(stable, tok, tok_w, version, 4, 4, 1, 10, 2)
     assert list(rows) == [4, 5, 6, 11, 12 + 1]
-    rows_all = O.refresh_rows(stable, tok, tok_w, version, 4, 4, 1, 10, 2, refresh_active=True)
-    assert list(rows_all) == [4, 5, 6, 7, 11, 12 + 1, 12 + 4, 12 + 5, 12 + 6, 12 + 7]
+
+
+def test_multilayer_queries_and_kv_gate():
+    """Multi-layer denoiser: the rows that pass through the layers are the
+    refresh set plus the active block, and only refresh-set rows rewrite K/V
+    and versions; an active row that is stable and outside the refresh set
+    queries every layer but leaves its cached K/V and version untouched."""
+    w, W, tok0 = _load("mid_multi_sharp")
+    tr = O.run_dense(w, W, tok0, mode="cached", keep_pre=True)
+    B, L, blk, H, dh = w.batch, w.seq_len, w.block_len, w.n_heads, w.head_dim
+    gated = 0
+    for r in tr:
+        ac = (np.arange(B)[:, None] * L + r["q0"] + np.arange(blk)[None, :]).reshape(-1)
+        assert np.array_equal(r["queries"], np.union1d(r["rows"], ac))
+        quiet = np.setdiff1d(ac, r["rows"])             # query-only rows of this step
+        if r["s"] == 0 or not len(quiet):
+            continue
+        nxt = next((x for x in tr if x["t"] == r["t"] + 1), None)
+        if nxt is None:
+            continue
+        pre, post = r["pre"], nxt["pre"]
+        for f in (1, 2):                                 # K and V
+            a = pre["caches"][f].reshape(w.n_layers, B * L, H, dh)[:, quiet]
+            bq = post["caches"][f].reshape(w.n_layers, B * L, H, dh)[:, quiet]
+            assert np.array_equal(a, bq)
+        assert np.array_equal(pre["version"].reshape(w.n_layers, -1)[:, quiet],
+                              r["version"].reshape(w.n_layers, -1)[:, quiet])
+        gated += len(quiet)
+    assert gated > 0
 
 
 # --- whole-loop pins (refresh-all == recompute; unchanged => identical K/V) ---------------

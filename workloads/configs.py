@@ -36,7 +36,8 @@ class Workload:
     tokens: str = "zipf"  # "uniform255" or "zipf" (Zipf(1.1) over ids 1..V-1)
     zipf_a: float = 1.1
     lm_scale: float = 1.0  # multiplies W_lm ("sharp" variants make SWD fire)
-    refresh_active: int = 0  # 1: every active-block row joins the refresh set
+    active_queries: int = 0  # 1: every active-block row passes through the layers as a query
+    #                          (only the refresh set rewrites K/V; multi-layer denoiser)
     # attention-sink stream (sink > 0 selects streaming mode)
     sink: int = 0
     window: int = 0
@@ -88,9 +89,13 @@ TWELVE_LAYER = Workload(
     name="twelve_layer", dtype="bf16", n_layers=12, batch=16, seq_len=2048,
     n_prompt=1536, block_len=64, steps_per_block=64, d_model=1024, n_heads=16,
     head_dim=64, vocab=32000, ffn=4096, swd_K=3, swd_tau=0.9, swd_R=2, expiry=2,
-    seed=4, refresh_active=1)
+    seed=4, active_queries=1)
 
 NAMED = {w.name: w for w in (TINY_FP32, BF16_D2048, LAYER_8B, SINK_RING, TWELVE_LAYER)}
+
+# The 12-layer shape with W_lm scaled so that positions stabilise and commit
+# inside a block (the stability mask then gates the per-layer refresh).
+TWELVE_LAYER_SHARP = replace(TWELVE_LAYER, name="twelve_layer_sharp", lm_scale=40.0)
 
 # --- small shapes for element-by-element parity ------------------------------
 # Ragged on purpose: 320 rows (2.5 row tiles of 128), vocab 1000 (7 column
@@ -124,7 +129,7 @@ MID_MULTI = Workload(
     name="mid_multi", dtype="bf16", n_layers=3, batch=2, seq_len=160, n_prompt=128,
     block_len=16, steps_per_block=6, d_model=256, n_heads=4, head_dim=64,
     vocab=1000, ffn=512, swd_K=3, swd_tau=0.9, swd_R=2, expiry=2, seed=14,
-    refresh_active=1)
+    active_queries=1)
 
 MID_MULTI_SHARP = replace(MID_MULTI, name="mid_multi_sharp", lm_scale=40.0, steps_per_block=10, seed=18)
 
@@ -136,7 +141,7 @@ BIG_ROWS_DH64 = replace(MID_BF16_DH64, name="big_rows_dh64", batch=3, seq_len=30
 
 ALL = dict(NAMED)
 for _w in (MID_BF16, MID_BF16_DH64, TINY_FP32_SHARP, MID_BF16_SHARP, MID_SINK, TINY_SINK_F32, MID_MULTI,
-           MID_MULTI_SHARP, BIG_ROWS, BIG_ROWS_DH64):
+           MID_MULTI_SHARP, BIG_ROWS, BIG_ROWS_DH64, TWELVE_LAYER_SHARP):
     ALL[_w.name] = _w
 
 
