@@ -23,7 +23,7 @@ class CacheCfg(ctypes.Structure):
         ("sink", ctypes.c_int), ("window", ctypes.c_int), ("expiry", ctypes.c_int),
         ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float), ("swd_K", ctypes.c_int),
         ("swd_tau", ctypes.c_float), ("swd_R", ctypes.c_int), ("block_len", ctypes.c_int),
-        ("mask_id", ctypes.c_int), ("refresh_active", ctypes.c_int), ("vocab", ctypes.c_int),
+        ("mask_id", ctypes.c_int), ("active_queries", ctypes.c_int), ("vocab", ctypes.c_int),
         ("max_pos", ctypes.c_int), ("ffn", ctypes.c_int),
     ]
 
@@ -53,7 +53,7 @@ _SIGS = {
     "dllm_profile_events": [_VP, _I, _VP, _VP],
     "lmhead_conf_noalloc": [_VP, _VP, _I, _I, _I, _I, _I, ctypes.c_float, _VP, _VP, _VP, _VP],
 }
-PROF_QKV_GEMM, PROF_ATTN, PROF_LM_GEMM = 1, 2, 3
+PROF_QKV_GEMM, PROF_ATTN, PROF_LM_GEMM, PROF_OUT_GEMM, PROF_FFN = 1, 2, 3, 4, 5
 EXPORTS = list(_SIGS) + ["dllm_last_error"]
 
 _lib = None
@@ -99,7 +99,7 @@ def make_cfg(w, vocab=None):
     c.sink, c.window, c.expiry = w.sink, w.window, w.expiry
     c.rope_theta, c.rms_eps = w.rope_theta, w.rms_eps
     c.swd_K, c.swd_tau, c.swd_R = w.swd_K, w.swd_tau, w.swd_R
-    c.block_len, c.mask_id, c.refresh_active = w.block_len, w.mask_id, w.refresh_active
+    c.block_len, c.mask_id, c.active_queries = w.block_len, w.mask_id, w.active_queries
     c.vocab = w.vocab if vocab is None else vocab
     c.max_pos = w.stream_len if w.streaming else 0
     c.ffn = w.ffn

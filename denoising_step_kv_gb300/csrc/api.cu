@@ -384,6 +384,7 @@ dllm_status attn_out(dllm_cache* c, const void* o_dev, const void* w_o_dev, cons
   if (!aligned16(o_dev) || !aligned16(w_o_dev) || !aligned16(h_dev))
     return fail(DLLM_EINVAL, "attn_out: pointers must be 16-byte aligned");
   const int M = g.batch * std::max(q_len, 1);
+  ProfScope prof(c, DLLM_PROF_OUT_GEMM, static_cast<cudaStream_t>(stream));
   DLLM_LAUNCH(gemm_resid(c, o_dev, w_o_dev, M, c->seq_rows, m_dev, c->d, c->d, x_res_dev, tok_dev, embed_dev,
                          q_start, std::max(q_len, 1), h_dev, static_cast<cudaStream_t>(stream)),
               "attn_out");
@@ -398,6 +399,7 @@ dllm_status ffn_gelu(dllm_cache* c, const void* h_dev, const void* w1_dev, const
   if (!m_dev && (M < 0 || M > c->seq_rows)) return fail(DLLM_EINVAL, "ffn_gelu: M outside [0, B*L]");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int cap = m_dev ? c->seq_rows : M;
+  ProfScope prof(c, DLLM_PROF_FFN, st);
   DLLM_LAUNCH(launch_rownorm(c, h_dev, cap, m_dev, c->d, c->rs, st), "ffn_gelu: norm");
   DLLM_LAUNCH(gemm_gelu(c, h_dev, w1_dev, M, c->seq_rows, m_dev, F, c->d, c->rs, c->ffn_buf, st), "ffn_gelu: W1");
   DLLM_LAUNCH(gemm_resid(c, c->ffn_buf, w2_dev, M, c->seq_rows, m_dev, c->d, F, h_dev, nullptr, nullptr, 0, 1,
@@ -446,7 +448,7 @@ dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p
 
 dllm_status dllm_profile_events(dllm_cache* c, int kernel, void* ev_begin, void* ev_end) {
   DLLM_CHECK_HANDLE(c);
-  if (kernel < DLLM_PROF_QKV_GEMM || kernel > DLLM_PROF_LM_GEMM)
+  if (kernel < DLLM_PROF_QKV_GEMM || kernel > DLLM_PROF_FFN)
     return fail(DLLM_EINVAL, "dllm_profile_events: unknown kernel");
   if (!ev_begin != !ev_end) return fail(DLLM_EINVAL, "dllm_profile_events: give both events or neither");
   c->prof_begin[kernel] = static_cast<cudaEvent_t>(ev_begin);

@@ -61,7 +61,13 @@ struct EpiQKV {
   uint8_t* v;           // layer base pointers (tiled layout)
   KvLayout kv;
   const float2* rope;   // [DH/2] frequencies theta^(-2i/DH) as (hi, lo)
-  int L, d, rows_cap, streaming, S, W, max_pos;
+  const uint32_t* gate; // refresh-set flag words [B][Lw] (null: every row writes K/V)
+  int L, d, rows_cap, streaming, S, W, max_pos, Lw;
+
+  // does row (b, pos) rewrite its K and V (a query-only row stores Q alone)
+  __device__ __forceinline__ bool writes_kv(int b, int pos) const {
+    return !gate || ((gate[b * Lw + (pos >> 5)] >> (pos & 31)) & 1u);
+  }
 
   // where row m goes; false: store nothing
   __device__ __forceinline__ bool locate(int m, int M, int& b, int& slot, int& pos, float& sc) const {
@@ -89,9 +95,10 @@ struct EpiQKV {
   __device__ __forceinline__ void run_part(int m, int n0, int p, int M, int N, const LD& ld) const {
     int b, slot, pos;
     float sc;
-    const bool ok = locate(m, M, b, slot, pos, sc);
+    const bool ok_row = locate(m, M, b, slot, pos, sc);
     const int part = n0 / d, c0 = n0 - part * d;   // c0: first column inside q, k or v
     uint8_t* base = part == 0 ? q : part == 1 ? k : v;
+    const bool ok = ok_row && (part == 0 || writes_kv(b, pos));
     auto put = [&](int col, const float* vals) {    // col: column inside the part
       const int h = col / DH;
       store_kv32<T>(base, kv, b, h, slot, col - h * DH, vals);
@@ -141,8 +148,9 @@ struct EpiQKV {
     } else {   // DH == 32: both halves of a head sit in one 32-column chunk
       int b, slot, pos;
       float sc;
-      const bool ok = locate(m, M, b, slot, pos, sc);
+      const bool ok_row = locate(m, M, b, slot, pos, sc);
       const int part = n0 / d, c0 = n0 - part * d;
+      const bool ok = ok_row && (part == 0 || writes_kv(b, pos));
       uint8_t* base = part == 0 ? q : part == 1 ? k : v;
       float a[32];
 #pragma unroll 1

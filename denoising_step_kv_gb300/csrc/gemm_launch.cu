@@ -194,6 +194,8 @@ EpiQKV<T, DH> make_qkv(dllm_cache* c, int layer, const int* rows) {
   e.S = c->cfg.sink;
   e.W = c->cfg.window;
   e.max_pos = c->max_pos;
+  e.gate = kv_gate(c);
+  e.Lw = c->Lw;
   return e;
 }
 

@@ -45,8 +45,8 @@ struct dllm_cache {
   void* ffn_buf = nullptr;  // [seq_rows][ffn]
   int ffn_cap = 0;
   // measurement hook: events bracketing a kernel (index = dllm_prof_kernel)
-  cudaEvent_t prof_begin[4] = {nullptr, nullptr, nullptr, nullptr};
-  cudaEvent_t prof_end[4] = {nullptr, nullptr, nullptr, nullptr};
+  cudaEvent_t prof_begin[8] = {};
+  cudaEvent_t prof_end[8] = {};
 };
 
 namespace dllm {
@@ -74,6 +74,12 @@ struct ProfScope {
     if (end) record_event(end, st);
   }
 };
+
+// Refresh-set flag words that gate K/V writes: with active queries the row
+// list of a step also holds query-only rows (dense mode only).
+inline const uint32_t* kv_gate(const dllm_cache* c) {
+  return (c->cfg.sink == 0 && c->cfg.active_queries) ? c->words : nullptr;
+}
 
 // tensor maps (driver entry point resolved once)
 bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,

@@ -25,6 +25,9 @@ __device__ __forceinline__ float warp_sum(float x) {
 // input into the compact buffer X (layer-0 embedding rows; a caller-given
 // input is used in place), compute the RMSNorm scale, and stamp the row's
 // version and token-at-write.
+//
+// gate (may be null): refresh-set flag words [B][Lw]; a listed row whose flag
+// is clear only queries, so its version and token-at-write stay as they are.
 template <typename T>
 __global__ void __launch_bounds__(256) gather_kernel(const int* __restrict__ rows, const int* __restrict__ n_rows,
                                                      int n_host, const T* __restrict__ x, const int* __restrict__ tok,
@@ -32,6 +35,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const int* __restrict__ row
                                                      float* __restrict__ rs, int* __restrict__ tok_w,
                                                      int* __restrict__ version, int t, int d, int rows_cap,
                                                      int max_pos, int streaming, int vocab, float eps, int x_cap,
+                                                     const uint32_t* __restrict__ gate, int L, int Lw,
                                                      unsigned* err) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * 8 + warp;
@@ -86,8 +90,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const int* __restrict__ row
   if (lane == 0) {
     rs[i] = rsqrtf(ss / static_cast<float>(d) + eps);
     if (!streaming) {
-      if (version) version[row] = t;
-      if (tok_w && token >= 0) tok_w[row] = token;
+      const int b = row / L, pos = row - b * L;
+      const bool writes = !gate || ((gate[b * Lw + (pos >> 5)] >> (pos & 31)) & 1u);
+      if (version && writes) version[row] = t;
+      if (tok_w && token >= 0 && writes) tok_w[row] = token;
     }
   }
 }
@@ -158,8 +164,8 @@ __global__ void __launch_bounds__(MERGE_THREADS) lm_merge_kernel(const LMPart* _
   }
 }
 
-__device__ void compact_words(const uint32_t* __restrict__ words, int nw, int L, int Lw, int* __restrict__ rows,
-                              int* __restrict__ n_rows);
+__device__ void compact_words(const uint32_t* __restrict__ words, int nw, int L, int Lw, int q0, int nac,
+                              int* __restrict__ rows, int* __restrict__ n_rows);
 
 // Stable-Window-Decoding update of the active block of sequence blockIdx.x,
 // then one flag bit per position for the next step's refresh set.
@@ -168,7 +174,7 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
     uint8_t* __restrict__ stable, int* __restrict__ hist_tok, float* __restrict__ hist_p, int* __restrict__ hist_n,
     const int* __restrict__ tok_w, const int* __restrict__ version, uint32_t* __restrict__ words, int L, int Lw,
     int seq_rows, int n_layers, int blk, int K, float tau, int R, int q0, int t, int last, int expiry,
-    int refresh_active, unsigned* __restrict__ ticket, int* __restrict__ rows, int* __restrict__ n_rows) {
+    int active_queries, unsigned* __restrict__ ticket, int* __restrict__ rows, int* __restrict__ n_rows) {
   __shared__ uint8_t s_unst[64];
   __shared__ int s_last;
   const int b = blockIdx.x;
@@ -255,7 +261,6 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
           for (int l = 0; l < n_layers; ++l) vmin = min(vmin, version[l * seq_rows + r]);
         const int lo = max(p - R, q0), hi = min(p + R, q0 + nac - 1);
         for (int u = lo; u <= hi; ++u) f |= s_unst[u - q0] != 0;
-        if (refresh_active && p >= q0 && p < q0 + nac) f = true;
         f |= tk != tw;
         if (expiry >= 0) f |= (t + 1) - vmin > expiry;
       }
@@ -271,15 +276,26 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  compact_words(words, gridDim.x * Lw, L, Lw, rows, n_rows);
+  // the row list: the refresh set, plus every active row when they all query
+  compact_words(words, gridDim.x * Lw, L, Lw, q0, active_queries && !last ? nac : 0, rows, n_rows);
   if (threadIdx.x == 0) *ticket = 0u;
 }
 
-// Compact the flag words into ascending row ids b * L + pos (block-wide
-// exclusive scan of the per-word popcounts, one word per thread per pass).
-// Run by one whole block of blockDim.x (a multiple of 32, <= 1024) threads.
-__device__ void compact_words(const uint32_t* __restrict__ words, int nw, int L, int Lw, int* __restrict__ rows,
-                              int* __restrict__ n_rows) {
+// Bits [lo, hi) of a 32-bit word (clipped to [0, 32)).
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi) {
+  lo = max(lo, 0);
+  hi = min(hi, 32);
+  if (hi <= lo) return 0u;
+  const uint32_t up = hi == 32 ? 0xffffffffu : ((1u << hi) - 1u);
+  return up & ~((1u << lo) - 1u);
+}
+
+// Compact the flag words, OR the positions [q0, q0 + nac) of every sequence,
+// into ascending row ids b * L + pos (block-wide exclusive scan of the
+// per-word popcounts, one word per thread per pass).  Run by one whole block
+// of blockDim.x (a multiple of 32, <= 1024) threads.
+__device__ void compact_words(const uint32_t* __restrict__ words, int nw, int L, int Lw, int q0, int nac,
+                              int* __restrict__ rows, int* __restrict__ n_rows) {
   __shared__ int s_warp[32];
   __shared__ int s_base;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -287,7 +303,7 @@ __device__ void compact_words(const uint32_t* __restrict__ words, int nw, int L,
   __syncthreads();
   for (int base = 0; base < nw; base += blockDim.x) {
     const int w = base + tid;
-    uint32_t word = w < nw ? words[w] : 0u;
+    uint32_t word = w < nw ? words[w] | range_bits(q0 - (w % Lw) * 32, q0 + nac - (w % Lw) * 32) : 0u;
     const int cnt = __popc(word);
     int incl = cnt;
 #pragma unroll
@@ -323,9 +339,12 @@ __device__ void compact_words(const uint32_t* __restrict__ words, int nw, int L,
   if (tid == 0) *n_rows = s_base;
 }
 
-// Every refresh row 0 .. n-1 (the block-start full refresh).
-__global__ void __launch_bounds__(256) all_rows_kernel(int* __restrict__ rows, int* __restrict__ n_rows, int n) {
+// Every refresh row 0 .. n-1 (the block-start full refresh), every refresh
+// flag set.
+__global__ void __launch_bounds__(256) all_rows_kernel(int* __restrict__ rows, int* __restrict__ n_rows, int n,
+                                                       uint32_t* __restrict__ words, int nw) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) rows[i] = i;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nw; i += gridDim.x * blockDim.x) words[i] = 0xffffffffu;
   if (blockIdx.x == 0 && threadIdx.x == 0) *n_rows = n;
 }
 
@@ -390,13 +409,16 @@ cudaError_t launch_gather(dllm_cache* c, int layer, const int* rows, const int* 
   const dim3 grid(cdiv(cap, 8));
   const int* nr = rows ? n_rows : nullptr;
   const int streaming = dense ? 0 : 1;
+  const uint32_t* gate = kv_gate(c);
+  const int L = dense ? c->cfg.seq_len : 1;
   if (c->cfg.dtype == DLLM_BF16)
     return launch_ex(gather_kernel<bf16>, grid, dim3(256), 0, st, 0, rows, nr, n_host, static_cast<const bf16*>(x), tok,
                      static_cast<const bf16*>(embed), static_cast<bf16*>(c->X), c->rs, tok_w, version, t, c->d,
-                     c->rows, c->max_pos, streaming, c->cfg.vocab, c->cfg.rms_eps, c->seq_rows, c->err);
+                     c->rows, c->max_pos, streaming, c->cfg.vocab, c->cfg.rms_eps, c->seq_rows, gate, L, c->Lw,
+                     c->err);
   return launch_ex(gather_kernel<float>, grid, dim3(256), 0, st, 0, rows, nr, n_host, static_cast<const float*>(x), tok,
                    static_cast<const float*>(embed), static_cast<float*>(c->X), c->rs, tok_w, version, t, c->d,
-                   c->rows, c->max_pos, streaming, c->cfg.vocab, c->cfg.rms_eps, c->seq_rows, c->err);
+                   c->rows, c->max_pos, streaming, c->cfg.vocab, c->cfg.rms_eps, c->seq_rows, gate, L, c->Lw, c->err);
 }
 
 cudaError_t launch_rownorm(dllm_cache* c, const void* h, int M, const int* M_dev, int d, float* rs,
@@ -421,14 +443,14 @@ cudaError_t launch_stab(dllm_cache* c, const int* argmax, const float* p1, int* 
   const dllm_cache_cfg& g = c->cfg;
   return launch_ex(swd_kernel, dim3(g.batch), dim3(1024), 0, st, 0, argmax, p1, tok, c->stable, c->hist_tok, c->hist_p,
                    c->hist_n, c->tok_w, c->version, c->words, g.seq_len, c->Lw, c->seq_rows, g.n_layers, g.block_len,
-                   g.swd_K, g.swd_tau, g.swd_R, q_start, t, last, g.expiry, g.refresh_active, c->ticket, rows,
+                   g.swd_K, g.swd_tau, g.swd_R, q_start, t, last, g.expiry, g.active_queries, c->ticket, rows,
                    n_rows);
 }
 
 cudaError_t launch_refresh_all(dllm_cache* c, int q_start, int* rows, int* n_rows, cudaStream_t st) {
   (void)q_start;
   const int n = c->seq_rows;
-  all_rows_kernel<<<std::min(cdiv(n, 256), 256), 256, 0, st>>>(rows, n_rows, n);
+  all_rows_kernel<<<std::min(cdiv(n, 256), 256), 256, 0, st>>>(rows, n_rows, n, c->words, c->cfg.batch * c->Lw);
   return cudaGetLastError();
 }
 

@@ -185,13 +185,19 @@ class LayerStackGenerator:
     __del__ = DenseGenerator.__del__
     schedule = DenseGenerator.schedule
 
-    def step(self, t, q0, s, stream=None):
+    def step(self, t, q0, s, stream=None, prof=None):
+        """One denoising step.  prof: {kernel id: [(begin, end) per layer]}
+        events recorded around that kernel's launch in each layer (the LM
+        head's list has one pair)."""
         w, c, W = self.w, self.cache, self.W
         blk = w.block_len
         if t == 0:
             K.refresh_all(c, q0, self.rows, self.n_rows, stream)
         x = None                       # layer 0: embeddings of the rows, gathered by kv_refresh
         for l in range(w.n_layers):
+            if prof:
+                for k, pairs in prof.items():
+                    K.dllm_profile_events(c, k, *pairs[min(l, len(pairs) - 1)])
             K.kv_refresh(c, l, x, self.tok, W["embed"], W["w_qkv"][l], self.rows, self.n_rows, t, stream)
             K.block_attn_rows(c, l, self.rows, self.n_rows, self.O, stream)
             h = self.H[l % 2]
@@ -205,23 +211,44 @@ class LayerStackGenerator:
         K.stab_update(c, self.argmax, self.p1, self.tok, q0, t, s == w.steps_per_block - 1, self.rows,
                       self.n_rows, stream)
 
-    def run(self, stream=None, on_step=None, n_steps=None):
+    def make_prof_events(self, kernels, n_steps):
+        """{kernel id: [[(begin, end) per layer] per step]} CUDA event pairs
+        for the first n_steps steps (the LM head: one pair per step)."""
+        ev = {}
+        for k in kernels:
+            per_step = []
+            for _ in range(n_steps):
+                layers = []
+                for _ in range(1 if k == K.PROF_LM_GEMM else self.w.n_layers):
+                    pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    pair[0].record()
+                    pair[1].record()
+                    layers.append(pair)
+                per_step.append(layers)
+            ev[k] = per_step
+        return ev
+
+    def run(self, stream=None, on_step=None, n_steps=None, prof=None):
         K.dllm_cache_reset(self.cache, stream)
         self.tok.copy_(self.tok_in)
         for t, q0, s in self.schedule():
             if n_steps is not None and t >= n_steps:
                 break
-            self.step(t, q0, s, stream)
+            step_prof = {k: v[t] for k, v in prof.items()} if prof and t < len(next(iter(prof.values()))) else None
+            self.step(t, q0, s, stream, step_prof)
+            if prof:
+                for k in prof:
+                    K.dllm_profile_events(self.cache, k, None, None)
             if on_step is not None:
                 on_step(t, q0, s)
         return self.tok
 
-    def capture(self, n_steps=None):
+    def capture(self, n_steps=None, prof=None):
         self.run(n_steps=n_steps)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.run(n_steps=n_steps)
+            self.run(n_steps=n_steps, prof=prof)
         self.graph = g
         return g
 
@@ -268,18 +295,40 @@ class StreamGenerator:
         K.kv_refresh(c, 0, None, self.tok, W["embed"], W["w_qkv"][0], self.pos[n:n + 1], self.one, n, stream)
         K.block_attn(c, 0, n, 1, self.out[n:n + 1], stream)
 
-    def run(self, n_tokens=None, stream=None):
+    def make_prof_events(self, kernels, n0, n1):
+        """{kernel id: [(begin, end) per token n0 .. n1-1]} CUDA event pairs."""
+        ev = {}
+        for k in kernels:
+            ev[k] = []
+            for _ in range(n0, n1):
+                pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                pair[0].record()
+                pair[1].record()
+                ev[k].append(pair)
+        return ev
+
+    def run(self, n_tokens=None, stream=None, prof=None, prof_from=0):
+        """Run the stream; prof (from make_prof_events(kernels, prof_from, ..))
+        brackets both kernels of tokens prof_from onwards."""
         K.dllm_cache_reset(self.cache, stream)
+        n_prof = len(next(iter(prof.values()))) if prof else 0
         for n in range(self.w.stream_len if n_tokens is None else n_tokens):
+            on = prof_from <= n < prof_from + n_prof
+            if on:
+                for k, pairs in prof.items():
+                    K.dllm_profile_events(self.cache, k, *pairs[n - prof_from])
             self.step(n, stream)
+            if on:
+                for k in prof:
+                    K.dllm_profile_events(self.cache, k, None, None)
         return self.out
 
-    def capture(self, n_tokens=None):
+    def capture(self, n_tokens=None, prof=None, prof_from=0):
         self.run(n_tokens)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.run(n_tokens)
+            self.run(n_tokens, prof=prof, prof_from=prof_from)
         self.graph = g
         return g
 

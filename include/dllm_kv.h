@@ -93,8 +93,11 @@ typedef struct {
   int swd_R;         /* dilation radius of unstable positions */
   int block_len;     /* active block length (<= 64) */
   int mask_id;       /* id of the mask token */
-  int refresh_active;/* 1: the active block always joins the refresh set,
-                        listed first (multi-layer denoiser) */
+  int active_queries;/* 1 (multi-layer denoiser): every active-block row
+                        passes through the layers as a query; the row list
+                        stab_update writes is the refresh set plus the active
+                        block, and kv_refresh rewrites K/V, version and
+                        token-at-write only for refresh-set rows */
   int vocab;         /* V: token ids are checked against it; sizes the
                         LM-head workspace */
   int max_pos;       /* RoPE positions (streaming: stream length); 0 = L */
@@ -255,8 +258,9 @@ dllm_status lmhead_conf(dllm_cache* c, const void* h_dev, const void* w_lm_dev, 
      the history is cleared, and the next refresh set is the full set of the
      next block (as refresh_all(q_start + block_len)).
      Otherwise rows = dilate_R(unstable active) U {tok != token-at-write}
-       U {(t + 1) - version > expiry} (U the active block if refresh_active),
-     ascending b * L + pos.
+       U {(t + 1) - version > expiry}, ascending b * L + pos; with
+     active_queries the list also holds every active row (the refresh set
+     itself stays in the handle and gates kv_refresh's K/V writes).
    argmax_dev / p_top1_dev: [B * block_len] device; tok_dev [B][L] device,
    updated in place; rows_dev [B * L], n_rows_dev [1] device outputs. */
 dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p_top1_dev,
@@ -291,7 +295,9 @@ dllm_status lmhead_conf_noalloc(const void* h_dev, const void* w_lm_dev, int M, 
 typedef enum {
   DLLM_PROF_QKV_GEMM = 1,   /* projection GEMM of kv_refresh */
   DLLM_PROF_ATTN = 2,       /* attention kernel of block_attn */
-  DLLM_PROF_LM_GEMM = 3     /* fused LM-head GEMM of lmhead_conf */
+  DLLM_PROF_LM_GEMM = 3,    /* fused LM-head GEMM of lmhead_conf */
+  DLLM_PROF_OUT_GEMM = 4,   /* output-projection GEMM of attn_out */
+  DLLM_PROF_FFN = 5         /* row norm and both GEMMs of ffn_gelu */
 } dllm_prof_kernel;
 
 /* Record the CUDA events ev_begin / ev_end (cudaEvent_t, created by the

@@ -57,16 +57,6 @@ def close(a, b, w):
     return np.allclose(a, b, rtol=rtol, atol=atol)
 
 
-def close_rows(a, b, rtol=BF16_RTOL):
-    """Row-wise max-norm comparison: every row's largest error within rtol of
-    the row's largest magnitude.  Used for hidden states deep in a bf16 layer
-    stack, where each layer's storage rounding depends on its inputs' last
-    bit and element-wise relative errors near zero crossings grow."""
-    a = np.asarray(a, np.float64).reshape(-1, np.shape(a)[-1])
-    b = np.asarray(b, np.float64).reshape(-1, np.shape(b)[-1])
-    return bool(np.all(np.max(np.abs(a - b), axis=1) <= rtol * np.maximum(np.max(np.abs(b), axis=1), 1e-30)))
-
-
 def worst(a, b, w):
     """(count over tolerance, got, want) at the element farthest past it."""
     rtol, atol = tol(w)

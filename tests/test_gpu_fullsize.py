@@ -1,10 +1,10 @@
-"""Full-size workloads (GPU) on sampled outputs: the 2048-wide layer (batch 4,
-L 1024), the 8B-shaped layer (batch 8, L 4096, vocab 126464) and the
-12-layer denoiser (batch 16, L 2048) run their first two denoising steps
-(a full refresh, then a partial one) at full batch in the launch
-configuration of the benchmark; the oracle recomputes sampled sequences on
-their own (sequences are independent) and every output of those sequences
-is compared."""
+"""Full-size single-layer workloads (GPU) on sampled outputs: the 2048-wide
+layer (batch 4, L 1024) and the 8B-shaped layer (batch 8, L 4096, vocab
+126464) run their first two denoising steps (a full refresh, then a partial
+one) at full batch in the launch configuration of the benchmark; the oracle
+recomputes sampled sequences on their own (sequences are independent) and
+every output of those sequences is compared.  (The 12-layer denoiser's
+full-size check, layer by layer over a whole block, is test_gpu_layers.)"""
 from dataclasses import replace
 
 import numpy as np
@@ -14,7 +14,7 @@ import torch
 import oracle as O
 from denoising_step_kv_gb300 import _lib as K
 from denoising_step_kv_gb300 import loop
-from gpu_util import close, close_rows, max_err, read_field, read_kv, tol, worst
+from gpu_util import close, read_field, read_kv, tol, worst
 from workloads import configs as C
 from workloads import generate as G
 
@@ -51,20 +51,18 @@ def _qkv_worst(got, want):
     return int(bad.sum()), i, float(got[i]), float(want[i])
 
 
-@pytest.mark.parametrize("name,sample", [("bf16_d2048", [0, 3]), ("8b_shaped", [5]), ("twelve_layer", [13])])
+@pytest.mark.parametrize("name,sample", [("bf16_d2048", [0, 3]), ("8b_shaped", [5])])
 def test_full_size_sampled(name, sample):
     """Each step's outputs of the sampled sequences, kernel by kernel against
     the oracle on the same inputs (the GPU's own caches and hidden states):
     projection into the cache, attention, W_o + residual, LM head and
     confidences; the sequence's tokens and stability against the oracle's
-    trajectory.  The 12-layer model is compared end to end (row max-norm)."""
+    trajectory."""
     w = C.get(name)
     m = G.model(w)
     tok0 = G.prompt_tokens(w)
     B, L, blk, d, H, dh = w.batch, w.seq_len, w.block_len, w.d_model, w.n_heads, w.head_dim
-    stacked = w.n_layers > 1 or bool(w.ffn)
-    cls = loop.LayerStackGenerator if stacked else loop.DenseGenerator
-    gen = cls(w, {k: loop.to_device(v) for k, v in m.items()})
+    gen = loop.DenseGenerator(w, {k: loop.to_device(v) for k, v in m.items()})
     got = []
 
     def grab(t, q0, s):
@@ -73,8 +71,7 @@ def test_full_size_sampled(name, sample):
                    o=gen.o.float().cpu().numpy().reshape(B, blk, d),
                    h=gen.h.float().cpu().numpy().reshape(B, blk, d),
                    stable=read_field(gen.cache, K.FIELD_STABLE, 0, (B, L), "u8").astype(bool))
-        if not stacked:
-            rec["qkv"] = [read_kv(gen.cache, f, 0, w)[sample] for f in (K.FIELD_Q, K.FIELD_K, K.FIELD_V)]
+        rec["qkv"] = [read_kv(gen.cache, f, 0, w)[sample] for f in (K.FIELD_Q, K.FIELD_K, K.FIELD_V)]
         got.append(rec)
 
     gen.tok_in.copy_(torch.from_numpy(tok0))
@@ -93,21 +90,17 @@ def test_full_size_sampled(name, sample):
         for t, g in enumerate(got):
             rec = trace[t]
             q0 = rec["q0"]
-            if stacked:
-                assert close_rows(g["o"][b], rec["o"][0]), (name, b, t, "o", max_err(g["o"][b], rec["o"][0]))
-                assert close_rows(g["h"][b], rec["h"][0]), (name, b, t, "h", max_err(g["h"][b], rec["h"][0]))
-            else:
-                # projection: the caches after this step
-                qg, kg, vg = (a[si] for a in g["qkv"])
-                for nm, a, r in zip("qkv", (qg, kg, vg), trace[t + 1]["pre"]["caches"]):
-                    assert _qkv_close(a, r[0][0]), (name, b, t, nm, _qkv_worst(a, r[0][0]))
-                # attention, W_o + residual on the GPU's own inputs
-                o_want = O.round_store(O.attention(qg[q0:q0 + blk], kg, vg).reshape(blk, d), w.dtype)
-                assert close(g["o"][b], o_want, w), (name, b, t, "o", worst(g["o"][b], o_want, w))
-                tok_in = got[t - 1]["tok"][b] if t else tok0[b]          # tokens when the step began
-                x = W64["embed"][tok_in[q0:q0 + blk]]
-                h_want = O.out_proj(g["o"][b].astype(np.float64), W64["w_o"][0], x, w.dtype)
-                assert close(g["h"][b], h_want, w), (name, b, t, "h", worst(g["h"][b], h_want, w))
+            # projection: the caches after this step
+            qg, kg, vg = (a[si] for a in g["qkv"])
+            for nm, a, r in zip("qkv", (qg, kg, vg), trace[t + 1]["pre"]["caches"]):
+                assert _qkv_close(a, r[0][0]), (name, b, t, nm, _qkv_worst(a, r[0][0]))
+            # attention, W_o + residual on the GPU's own inputs
+            o_want = O.round_store(O.attention(qg[q0:q0 + blk], kg, vg).reshape(blk, d), w.dtype)
+            assert close(g["o"][b], o_want, w), (name, b, t, "o", worst(g["o"][b], o_want, w))
+            tok_in = got[t - 1]["tok"][b] if t else tok0[b]          # tokens when the step began
+            x = W64["embed"][tok_in[q0:q0 + blk]]
+            h_want = O.out_proj(g["o"][b].astype(np.float64), W64["w_o"][0], x, w.dtype)
+            assert close(g["h"][b], h_want, w), (name, b, t, "h", worst(g["h"][b], h_want, w))
             # LM head and confidences on the GPU's hidden states
             am, p1, ent, margin = O.lm_head_conf(g["h"][b].astype(np.float64), W64["w_lm"], w.mask_id, w.rms_eps)
             assert np.allclose(g["p1"][b], p1, rtol=rtol, atol=atol), (name, b, t, "p1")

@@ -317,8 +317,10 @@ def test_stab_update_random_state(name, last, seed):
     if last:
         rows_o = np.arange(B * L)
     else:
-        rows_o = O.refresh_rows(stable_o, tok_o, tok_w, version, q0, blk, w.swd_R, t + 1, w.expiry,
-                                bool(w.refresh_active))
+        rows_o = O.refresh_rows(stable_o, tok_o, tok_w, version, q0, blk, w.swd_R, t + 1, w.expiry)
+        if w.active_queries:             # the row list also holds every active row
+            ac = (np.arange(B)[:, None] * L + q0 + np.arange(blk)[None, :]).reshape(-1)
+            rows_o = np.union1d(rows_o, ac).astype(np.int32)
     # GPU
     c = _fresh(w)
     try:

@@ -1,6 +1,7 @@
 """The multi-layer denoiser (GPU) against the oracle: attention for a row
-list, the active-row gather, the FFN, and whole generations of a 3-layer
-model with the stability mask gating every layer's refresh."""
+list, the active-row gather, the FFN, and free-running generations of a
+3-layer model with the stability mask gating every layer's refresh (the
+per-layer element-wise comparison runs teacher-forced in test_gpu_layers)."""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +10,7 @@ import oracle as O
 from denoising_step_kv_gb300 import _lib as K
 from denoising_step_kv_gb300 import loop
 from denoising_step_kv_gb300.loop import to_device
-from gpu_util import close, close_rows, i32, max_err, read_field, tol, write_kv
+from gpu_util import close, i32, max_err, read_field, tol, write_kv
 from workloads import configs as C
 from workloads import generate as G
 
@@ -105,7 +106,10 @@ def test_ffn_gelu(n):
         K.dllm_cache_free(c)
 
 
-def _ambiguous(rec, w, p_band):
+P_BAND = 1e-3      # the probability tolerance: stability decisions this close to tau may differ
+
+
+def _ambiguous(rec, w, p_band=P_BAND):
     """Active positions whose argmax (top-2 margin <= 1e-2) or stability
     decision (mean top-1 probability within p_band of tau) may differ."""
     amb = rec["margin"] <= 1e-2
@@ -119,11 +123,11 @@ def _ambiguous(rec, w, p_band):
 
 @pytest.mark.parametrize("name", ["mid_multi", "mid_multi_sharp"])
 def test_layer_stack_generation(name):
-    """Free-running generation of the 3-layer model: every step's last-layer
-    attention output and hidden state of the active rows (row max-norm), the
-    confidences, and - until an ambiguous position could part the
-    trajectories - tokens, stability, refresh rows and every layer's
-    versions."""
+    """Free-running generation of the 3-layer model: every step's confidences
+    (the oracle's LM head on the GPU's hidden states, element-wise) and,
+    until a position whose argmax margin is <= 1e-2 or whose mean top-1
+    probability lies within 1e-3 of tau could part the trajectories, tokens,
+    stability, the row list and every layer's versions, bit for bit."""
     w = C.get(name)
     m = G.model(w)
     tok0 = G.prompt_tokens(w)
@@ -151,10 +155,6 @@ def test_layer_stack_generation(name):
     compared = 0
     for rec, g in zip(trace, got):
         t = rec["t"]
-        # the layer stack: after several bf16 layers the hidden states carry
-        # storage-rounding differences, compared in the row max-norm
-        assert close_rows(g["o"], rec["o"]), (name, t, "o", max_err(g["o"], rec["o"]))
-        assert close_rows(g["h"], rec["h"]), (name, t, "h", max_err(g["h"], rec["h"]))
         # the LM head and confidences: the oracle's on the GPU's own hidden states
         am, p1, ent, margin = O.lm_head_conf(g["h"].reshape(B * blk, d).astype(np.float64), W64["w_lm"],
                                              w.mask_id, w.rms_eps)
@@ -162,11 +162,8 @@ def test_layer_stack_generation(name):
         assert np.allclose(g["ent"].reshape(-1), ent, rtol=rtol, atol=atol), (name, t, "ent")
         sure = margin > 1e-2
         assert np.array_equal(g["argmax"].reshape(-1)[sure], am[sure]), (name, t, "argmax")
-        # the trajectory, while no decision hangs on the stack's rounding: a
-        # position is ambiguous when its argmax margin is small or its mean
-        # top-1 probability is closer to tau than the two sides' p1 differ
-        band = float(np.max(np.abs(g["p1"] - rec["p1"]))) + 1e-3
-        amb = _ambiguous(rec, w, band)
+        # the trajectory, while no decision hangs on the stack's rounding
+        amb = _ambiguous(rec, w)
         if np.any(g["argmax"] != rec["argmax"]):
             assert np.all(amb[g["argmax"] != rec["argmax"]]), (name, t, "argmax against the trajectory")
             break
@@ -180,4 +177,5 @@ def test_layer_stack_generation(name):
         assert np.array_equal(g["rows"], rec["rows_next"]), (name, t, "rows")
         assert np.array_equal(g["version"], rec["version"]), (name, t, "version")
         compared += 1
-    assert compared >= 1, (name, compared)
+    # the trajectories agree through the first block at least
+    assert compared >= w.steps_per_block, (name, compared)
