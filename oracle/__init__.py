@@ -11,13 +11,13 @@ fp32) exactly where the GPU path stores them (Q/K/V cache rows, attention
 output O, residual stream h, FFN intermediate).
 """
 from .model import (bf16_bits_to_f64, round_store, rms_scale, rope, project_qkv,
-                    attention, out_proj, ffn, lm_head_conf, gelu)
-from .swd import SWDState, swd_update, dilate, refresh_rows, expired_rows
+                    attention, attention_partial, merge_partials, out_proj, ffn, lm_head_conf, gelu)
+from .swd import SWDState, swd_update, dilate, refresh_rows, expired_rows, radius_at, full_refresh_at
 from .run import run_dense, run_stream, weights_f64, ring_positions, RingSim, NEVER
 
 __all__ = [
     "bf16_bits_to_f64", "round_store", "rms_scale", "rope", "project_qkv",
-    "attention", "out_proj", "ffn", "lm_head_conf", "gelu", "SWDState",
-    "swd_update", "dilate", "refresh_rows", "expired_rows", "run_dense",
+    "attention", "attention_partial", "merge_partials", "out_proj", "ffn", "lm_head_conf", "gelu", "SWDState",
+    "swd_update", "dilate", "refresh_rows", "expired_rows", "radius_at", "full_refresh_at", "run_dense",
     "run_stream", "weights_f64", "ring_positions", "RingSim", "NEVER",
 ]

@@ -116,6 +116,42 @@ def attention(q, k, v):
     return np.einsum("hqk,khd->qhd", p, v)
 
 
+def attention_partial(q, k, v):
+    """Online-softmax state of queries q over the keys k, v ([LaCache] LSM,
+    FACache: the running maximum m, the normaliser l and the unnormalised
+    accumulator O~ of a FlashAttention pass over those keys).
+
+    q: [nq, H, dh]; k, v: [nk, H, dh] (nk may be 0).  Returns
+    (m [H, nq], l [H, nq], O~ [nq, H, dh]) with O~ = sum_k e^(s_k - m) v_k,
+    l = sum_k e^(s_k - m), s = q.k / sqrt(dh); an empty key set gives
+    m = -inf, l = 0, O~ = 0.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    nq, H, dh = q.shape
+    if len(k) == 0:
+        return np.full((H, nq), -np.inf), np.zeros((H, nq)), np.zeros((nq, H, dh))
+    s = np.einsum("qhd,khd->hqk", q, k) / np.sqrt(dh)
+    m = s.max(axis=-1)
+    p = np.exp(s - m[..., None])
+    return m, p.sum(axis=-1), np.einsum("hqk,khd->qhd", p, v)
+
+
+def merge_partials(parts):
+    """Combine online-softmax states of one set of queries over disjoint key
+    sets into the attention output over their union:
+    O = sum_i e^(m_i - M) O~_i / sum_i e^(m_i - M) l_i, M = max_i m_i."""
+    M = np.max(np.stack([m for m, _, _ in parts]), axis=0)             # [H, nq]
+    num = 0.0
+    den = 0.0
+    for m, l, o in parts:
+        w = np.where(np.isneginf(m), 0.0, np.exp(m - np.where(np.isneginf(M), 0.0, M)))
+        den = den + w * l
+        num = num + np.transpose(w)[:, :, None] * o
+    return num / np.transpose(den)[:, :, None]
+
+
 def out_proj(o, w_o, x, dtype):
     """Residual stream after attention: h = x + O . W_o^T (O stored first)."""
     o = round_store(np.asarray(o, dtype=np.float64).reshape(len(x), -1), dtype)

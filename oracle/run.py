@@ -29,7 +29,7 @@ from collections import deque
 import numpy as np
 
 from . import model as M
-from .swd import SWDState, swd_update, refresh_rows
+from .swd import SWDState, swd_update, refresh_rows, radius_at, full_refresh_at
 
 NEVER = -(1 << 30)     # version of a cache entry that was never written
 
@@ -72,13 +72,19 @@ def _layer_stack(w, W, x, pos_rows, rows_flat, caches, write_kv=None):
     return o_last, x
 
 
-def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre=False):
+def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre=False, facache=False):
     """Run the SAR step loop.  Returns a list of per-step records.
 
     W: fp64 weights (``weights_f64``); tok0: [B, L] int32 initial tokens.
     mode: "cached" or "recompute"; force_all: refresh every row every step.
     keep_pre: record the pre-step state (including caches) of every step.
     n_steps caps the number of steps run.
+    facache (single-layer cached mode): [LaCache] LSM, FACache - the
+    online-softmax state of the active queries over the keys outside the
+    block's window [q0 - R, q0 + blk + R) is kept per sequence with the
+    block start and the queries' token-at-write, and reused (merged with the
+    window's fresh state) while they are unchanged; the record's
+    "fa_rebuilt" lists the sequences whose state was recomputed.
     """
     B, L, H, dh, d = w.batch, w.seq_len, w.n_heads, w.head_dim, w.d_model
     nl, blk = w.n_layers, w.block_len
@@ -93,6 +99,7 @@ def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre
     trace = []
     t = 0
     rows_next = None
+    fa_key, fa_state = {}, {}
     total = w.n_steps if n_steps is None else min(n_steps, w.n_steps)
     for bi in range(w.n_blocks):
         q0 = w.n_prompt + bi * blk
@@ -120,9 +127,22 @@ def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre
                 for c, val in zip(caches, (q, k, v)):
                     c[0].reshape(B * L, H, dh)[rows] = val
                 o = np.zeros((B * blk, H, dh))
+                rec["fa_rebuilt"] = []
                 for b in range(B):
                     qa = caches[0][0][b, q0:q0 + blk]
-                    o[b * blk:(b + 1) * blk] = M.attention(qa, caches[1][0][b], caches[2][0][b])
+                    kb, vb = caches[1][0][b], caches[2][0][b]
+                    if not facache:
+                        o[b * blk:(b + 1) * blk] = M.attention(qa, kb, vb)
+                        continue
+                    win = np.arange(max(0, q0 - w.swd_R), min(L, q0 + blk + w.swd_R))
+                    unch = np.setdiff1d(np.arange(L), win)
+                    key = (q0, tuple(int(x) for x in tok_w[b, q0:q0 + blk]))
+                    if fa_key.get(b) != key:
+                        fa_state[b] = M.attention_partial(qa, kb[unch], vb[unch])
+                        fa_key[b] = key
+                        rec["fa_rebuilt"].append(b)
+                    o[b * blk:(b + 1) * blk] = M.merge_partials(
+                        [fa_state[b], M.attention_partial(qa, kb[win], vb[win])])
                 o_ac = M.round_store(o.reshape(B * blk, d), w.dtype)
                 h_ac = M.out_proj(o_ac, W["w_o"][0], x_emb[ac_flat], w.dtype)
             else:
@@ -141,8 +161,11 @@ def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre
             if last:
                 swd.reset()
                 rows_next = flat_all
+            elif full_refresh_at(s + 1, w.full_every):
+                rows_next = flat_all
             else:
-                rows_next = refresh_rows(stable, tok, tok_w, version, q0, blk, w.swd_R, t + 1, w.expiry)
+                R_next = radius_at(s + 1, w.steps_per_block, w.swd_R, w.swd_R_min)
+                rows_next = refresh_rows(stable, tok, tok_w, version, q0, blk, R_next, t + 1, w.expiry)
             # the row list the next step runs on: Rf, plus the active block
             # when every active row queries (the next step is in this block
             # unless this was its last step, and then Rf is every row)

@@ -29,6 +29,11 @@ Readings (also listed in the design notes):
   * t is the global step counter; refresh set for step t+1 =
       dilate_R(unstable) U {p : tok[p] != token the entry was computed from}
       U {p : (t+1) - version[p] > expiry}.
+  * schedules ([SWD] 4.4: R may grow along the sampling steps, small or 0
+    early and larger late; [FlashdLLM] 5.1: a full refresh every few steps,
+    incremental updates between): radius_at gives R at block-local step s
+    rising in equal stages from R_min to R; full_refresh_at marks the steps
+    s % every == 0 whose refresh set is every row.
 """
 import numpy as np
 
@@ -113,6 +118,20 @@ def expired_rows(version, t, expiry):
     if expiry < 0:
         return np.zeros(version.shape[1:], dtype=bool)
     return np.any(t - version > expiry, axis=0)
+
+
+def radius_at(s, steps, R, R_min):
+    """Dilation radius at block-local step s of a block of `steps` steps:
+    R when R_min < 0, else R_min + floor((R - R_min + 1) * s / steps)
+    (R_min at s = 0, R over the last stage)."""
+    if R_min < 0:
+        return R
+    return R_min + ((R - R_min + 1) * s) // steps
+
+
+def full_refresh_at(s, every):
+    """Is block-local step s a scheduled refresh of every row?"""
+    return every > 0 and s % every == 0
 
 
 def refresh_rows(stable, tok, tok_w, version, q0, blk, R, t_next, expiry):

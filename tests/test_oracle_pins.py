@@ -363,6 +363,38 @@ def test_refresh_rows_composition():
     assert list(rows) == [4, 5, 6, 11, 12 + 1]
 
 
+def test_radius_schedule_and_full_refresh_steps():
+    # fixed radius unless a starting radius is given
+    assert [O.radius_at(s, 32, 2, -1) for s in (0, 15, 31)] == [2, 2, 2]
+    # 0 -> 2 over 32 steps in three equal stages; monotone, ends at R
+    rs = [O.radius_at(s, 32, 2, 0) for s in range(32)]
+    assert rs[0] == 0 and rs[-1] == 2 and all(a <= b for a, b in zip(rs, rs[1:]))
+    assert [rs.count(r) for r in (0, 1, 2)] == [11, 11, 10]
+    assert [O.radius_at(s, 10, 3, 1) for s in range(10)] == [1, 1, 1, 1, 2, 2, 2, 3, 3, 3]
+    assert [s for s in range(12) if O.full_refresh_at(s, 4)] == [0, 4, 8]
+    assert not any(O.full_refresh_at(s, 0) for s in range(12))
+
+
+def test_schedules_shape_the_refresh_sets():
+    """mid_bf16_sched: every 4th step of a block refreshes every row; the
+    other steps dilate the unstable rows by the scheduled radius."""
+    w, W, tok0 = _load("mid_bf16_sched")
+    tr = O.run_dense(w, W, tok0, mode="cached")
+    full = w.batch * w.seq_len
+    saw_partial = 0
+    for prev, r in zip(tr[:-1], tr[1:]):
+        s = r["s"]
+        if s == 0 or s % w.full_every == 0:
+            assert len(r["rows"]) == full, (r["t"], s)
+            continue
+        R = O.radius_at(s, w.steps_per_block, w.swd_R, w.swd_R_min)
+        want = O.refresh_rows(prev["stable"], prev["tok"], prev["tok_w"], prev["version"], r["q0"], w.block_len, R,
+                              r["t"], w.expiry)
+        assert np.array_equal(r["rows"], want), (r["t"], s)
+        saw_partial += len(r["rows"]) < full
+    assert saw_partial > 0
+
+
 def test_multilayer_queries_and_kv_gate():
     """Multi-layer denoiser: the rows that pass through the layers are the
     refresh set plus the active block, and only refresh-set rows rewrite K/V
@@ -390,6 +422,54 @@ def test_multilayer_queries_and_kv_gate():
                               r["version"].reshape(w.n_layers, -1)[:, quiet])
         gated += len(quiet)
     assert gated > 0
+
+
+def test_split_kv_merge_equals_single_pass():
+    """The online-softmax states over disjoint key sets merge into the plain
+    attention over their union (the split-KV identity FACache rests on); an
+    empty part contributes nothing; one key gives m = s, l = 1, O~ = v."""
+    q = RNG.standard_normal((5, 3, 16))
+    k = RNG.standard_normal((40, 3, 16)) * 2.0
+    v = RNG.standard_normal((40, 3, 16))
+    want = O.attention(q, k, v)
+    for cut in ([0, 40], [0, 1, 40], [0, 13, 13, 29, 40], [0, 39, 40]):
+        parts = [O.attention_partial(q, k[a:b], v[a:b]) for a, b in zip(cut[:-1], cut[1:])]
+        assert np.allclose(O.merge_partials(parts), want, rtol=1e-13, atol=1e-14), cut
+    idx = RNG.permutation(40)                                   # not contiguous
+    parts = [O.attention_partial(q, k[idx[:17]], v[idx[:17]]), O.attention_partial(q, k[idx[17:]], v[idx[17:]])]
+    assert np.allclose(O.merge_partials(parts), want, rtol=1e-13, atol=1e-14)
+    m, l, o = O.attention_partial(q[:1], k[:1], v[:1])
+    assert np.allclose(m[:, 0], np.einsum("hd,hd->h", q[0], k[0]) / 4.0)
+    assert np.array_equal(l, np.ones_like(l)) and np.allclose(o[0], v[0])
+
+
+@pytest.mark.parametrize("name", ["mid_bf16", "mid_bf16_sharp", "mid_bf16_dh64"])
+def test_facache_loop_equals_the_plain_loop(name):
+    """Reusing the kept softmax state changes nothing but rounding order:
+    the same tokens, argmaxes and stability at every step, outputs to 1e-6;
+    the state is rebuilt for every sequence at each block start and
+    otherwise only after one of its block's tokens changed."""
+    w, W, tok0 = _load(name)
+    a = O.run_dense(w, W, tok0, mode="cached")
+    b = O.run_dense(w, W, tok0, mode="cached", facache=True)
+    for ra, rb in zip(a, b):
+        for key in ("argmax", "tok", "stable"):
+            assert np.array_equal(ra[key], rb[key]), (name, ra["t"], key)
+        assert np.allclose(ra["o"], rb["o"], rtol=1e-6, atol=1e-9)
+        assert np.allclose(ra["p1"], rb["p1"], rtol=1e-9)
+    for prev, rb in zip(b[:-1], b[1:]):
+        q0, blk = rb["q0"], w.block_len
+        if rb["s"] == 0:
+            assert rb["fa_rebuilt"] == list(range(w.batch))
+        else:      # the key: the active rows' token-at-write when the attention ran
+            changed = [bb for bb in range(w.batch)
+                       if not np.array_equal(rb["tok_w"][bb, q0:q0 + blk], prev["tok_w"][bb, q0:q0 + blk])]
+            assert rb["fa_rebuilt"] == changed, (name, rb["t"])
+    assert b[0]["fa_rebuilt"] == list(range(w.batch))
+    if name == "mid_bf16":                          # nothing commits inside a block
+        assert all(rb["fa_rebuilt"] == [] for rb in b if rb["s"] > 0)
+    if name == "mid_bf16_sharp":
+        assert any(rb["fa_rebuilt"] for rb in b if rb["s"] > 0)
 
 
 # --- whole-loop pins (refresh-all == recompute; unchanged => identical K/V) ---------------

@@ -28,6 +28,8 @@ class Workload:
     swd_K: int = 3
     swd_tau: float = 0.9
     swd_R: int = 2
+    swd_R_min: int = -1   # dilation radius at a block's first step (growing to swd_R); -1 = fixed swd_R
+    full_every: int = 0   # refresh every row at block-local steps s with s % full_every == 0 (0 = never)
     expiry: int = -1      # reject t - version > expiry; -1 = no expiry
     mask_id: int = 0
     rope_theta: float = 10000.0
@@ -114,6 +116,12 @@ TINY_FP32_SHARP = replace(TINY_FP32, name="tiny_fp32_sharp", lm_scale=60.0)
 MID_BF16_SHARP = replace(MID_BF16, name="mid_bf16_sharp", lm_scale=40.0,
                          steps_per_block=10)
 
+# The schedules of the refresh set: a dilation radius that grows from 0 at a
+# block's first step to R = 3 at its last, and a full refresh every 4th step
+# of a block (no version expiry, so only the schedule refreshes the prompt).
+MID_BF16_SCHED = replace(MID_BF16_SHARP, name="mid_bf16_sched", swd_R=3, swd_R_min=0, full_every=4, expiry=-1,
+                         seed=19)
+
 MID_SINK = Workload(
     name="mid_sink", dtype="bf16", n_layers=1, batch=1, seq_len=0, n_prompt=0,
     block_len=1, steps_per_block=1, d_model=256, n_heads=2, head_dim=128,
@@ -141,7 +149,7 @@ BIG_ROWS_DH64 = replace(MID_BF16_DH64, name="big_rows_dh64", batch=3, seq_len=30
 
 ALL = dict(NAMED)
 for _w in (MID_BF16, MID_BF16_DH64, TINY_FP32_SHARP, MID_BF16_SHARP, MID_SINK, TINY_SINK_F32, MID_MULTI,
-           MID_MULTI_SHARP, BIG_ROWS, BIG_ROWS_DH64, TWELVE_LAYER_SHARP):
+           MID_MULTI_SHARP, BIG_ROWS, BIG_ROWS_DH64, TWELVE_LAYER_SHARP, MID_BF16_SCHED):
     ALL[_w.name] = _w
 
 
