@@ -11,7 +11,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdllmkv.so")
 
 DLLM_F32, DLLM_BF16 = 0, 1
-FIELD_Q, FIELD_K, FIELD_V, FIELD_VERSION, FIELD_TOK_W, FIELD_STABLE, FIELD_HIST_TOK, FIELD_HIST_P, FIELD_HIST_N = range(9)
+(FIELD_Q, FIELD_K, FIELD_V, FIELD_VERSION, FIELD_TOK_W, FIELD_STABLE, FIELD_HIST_TOK, FIELD_HIST_P, FIELD_HIST_N,
+ FIELD_FA_REBUILT) = range(10)
 ERR_ROW, ERR_TOKEN, ERR_TIMEOUT, ERR_POS = 1, 2, 4, 8
 STATUS = {0: "OK", 1: "EINVAL", 2: "ENOMEM", 3: "ECUDA", 4: "EDEVICE", 5: "EUNSUPPORTED"}
 
@@ -24,7 +25,8 @@ class CacheCfg(ctypes.Structure):
         ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float), ("swd_K", ctypes.c_int),
         ("swd_tau", ctypes.c_float), ("swd_R", ctypes.c_int), ("block_len", ctypes.c_int),
         ("mask_id", ctypes.c_int), ("active_queries", ctypes.c_int), ("vocab", ctypes.c_int),
-        ("max_pos", ctypes.c_int), ("ffn", ctypes.c_int),
+        ("max_pos", ctypes.c_int), ("ffn", ctypes.c_int), ("swd_R_min", ctypes.c_int),
+        ("steps_per_block", ctypes.c_int), ("full_every", ctypes.c_int), ("facache", ctypes.c_int),
     ]
 
 
@@ -49,9 +51,10 @@ _SIGS = {
     "attn_out": [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _VP],
     "ffn_gelu": [_VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _VP],
     "lmhead_conf": [_VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP],
-    "stab_update": [_VP, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _VP],
+    "stab_update": [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP],
     "dllm_profile_events": [_VP, _I, _VP, _VP],
     "lmhead_conf_noalloc": [_VP, _VP, _I, _I, _I, _I, _I, ctypes.c_float, _VP, _VP, _VP, _VP],
+    "dllm_wait_selftest": [_VP, ctypes.c_uint64, _VP],
 }
 PROF_QKV_GEMM, PROF_ATTN, PROF_LM_GEMM, PROF_OUT_GEMM, PROF_FFN = 1, 2, 3, 4, 5
 EXPORTS = list(_SIGS) + ["dllm_last_error"]
@@ -90,9 +93,10 @@ def _check(name, status):
         raise DllmError(name, status, lib().dllm_last_error().decode())
 
 
-def make_cfg(w, vocab=None):
+def make_cfg(w, vocab=None, facache=False):
     """CacheCfg of a workload (see workloads.configs.Workload)."""
     c = CacheCfg()
+    c.facache = 1 if facache else 0
     c.n_layers, c.batch, c.seq_len = w.n_layers, w.batch, w.seq_len
     c.n_heads, c.head_dim = w.n_heads, w.head_dim
     c.dtype = DLLM_BF16 if w.dtype == "bf16" else DLLM_F32
@@ -103,6 +107,7 @@ def make_cfg(w, vocab=None):
     c.vocab = w.vocab if vocab is None else vocab
     c.max_pos = w.stream_len if w.streaming else 0
     c.ffn = w.ffn
+    c.swd_R_min, c.steps_per_block, c.full_every = w.swd_R_min, w.steps_per_block, w.full_every
     return c
 
 
@@ -192,8 +197,8 @@ def lmhead_conf(c, h, w_lm, M, V, d, mask_id, argmax, p_top1, entropy, stream=No
                                             _p(entropy), _s(stream)))
 
 
-def stab_update(c, argmax, p_top1, tok, q_start, t, last_step, rows, n_rows, stream=None):
-    _check("stab_update", lib().stab_update(c, _p(argmax), _p(p_top1), _p(tok), q_start, t,
+def stab_update(c, argmax, p_top1, tok, q_start, t, step_in_block, last_step, rows, n_rows, stream=None):
+    _check("stab_update", lib().stab_update(c, _p(argmax), _p(p_top1), _p(tok), q_start, t, step_in_block,
                                             1 if last_step else 0, _p(rows), _p(n_rows), _s(stream)))
 
 
@@ -211,3 +216,8 @@ def lmhead_conf_noalloc(h, w_lm, M, V, d, dtype, mask_id, rms_eps, argmax, p_top
     _check("lmhead_conf_noalloc", lib().lmhead_conf_noalloc(_p(h), _p(w_lm), M, V, d, dtype, mask_id,
                                                             ctypes.c_float(rms_eps), _p(argmax), _p(p_top1),
                                                             _p(entropy), _s(stream)))
+
+
+def dllm_wait_selftest(c, limit_ns, stream=None):
+    """One bounded wait on a barrier nothing arrives on (sets ERR_TIMEOUT)."""
+    _check("dllm_wait_selftest", lib().dllm_wait_selftest(c, ctypes.c_uint64(limit_ns), _s(stream)))

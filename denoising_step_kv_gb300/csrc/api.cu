@@ -59,7 +59,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 void free_all(dllm_cache* c) {
   void* bufs[] = {c->q, c->k, c->v, c->version, c->tok_w, c->stable, c->hist_tok, c->hist_p, c->hist_n, c->words,
-                  c->rope, c->err, c->ticket, c->X, c->rs, c->lm_part, c->lm_rs, c->ffn_buf};
+                  c->rope, c->err, c->ticket, c->X, c->rs, c->lm_part, c->lm_rs, c->ffn_buf,
+                  c->fa_state, c->fa_key, c->fa_rebuilt, c->sk_acc, c->sk_tickets};
   for (void* b : bufs)
     if (b) cudaFree(b);
 }
@@ -110,6 +111,9 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
       return fail(DLLM_EINVAL, "dllm_cache_init: need 1 <= block_len <= min(64, seq_len)");
     if (g.swd_K < 1 || g.swd_K > 8 || g.swd_R < 0)
       return fail(DLLM_EINVAL, "dllm_cache_init: need 1 <= swd_K <= 8 and swd_R >= 0");
+    if (g.swd_R_min > g.swd_R || g.full_every < 0 || (g.swd_R_min >= 0 && g.steps_per_block < 1))
+      return fail(DLLM_EINVAL, "dllm_cache_init: need swd_R_min <= swd_R, full_every >= 0 and, with a radius "
+                               "schedule, steps_per_block >= 1");
     if (static_cast<long long>(g.batch) * g.seq_len > (1LL << 26))
       return fail(DLLM_EUNSUPPORTED, "dllm_cache_init: batch * seq_len above 2^26");
   }
@@ -125,6 +129,8 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
     if (g.ffn % 32 != 0) return fail(DLLM_EUNSUPPORTED, "dllm_cache_init: fp32 needs ffn % 32 == 0");
   }
   if (!(g.rope_theta > 0.f) || !(g.rms_eps >= 0.f)) return fail(DLLM_EINVAL, "dllm_cache_init: bad theta/eps");
+  if (g.facache && (streaming || g.dtype != DLLM_BF16 || g.n_layers != 1))
+    return fail(DLLM_EUNSUPPORTED, "dllm_cache_init: facache needs a dense bf16 single-layer cache");
 
   dllm_cache* c = new dllm_cache();
   c->cfg = g;
@@ -162,6 +168,19 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
             dalloc(&c->lm_part, static_cast<size_t>(c->lm_rows_cap) * c->lm_tiles_cap * 16) &&
             dalloc(&c->lm_rs, static_cast<size_t>(c->lm_rows_cap) * sizeof(float)) &&
             dalloc(&c->ffn_buf, sr * static_cast<size_t>(g.ffn) * c->elem);
+  if (ok && g.dtype == DLLM_BF16) {   // stream-K accumulators: the widest projection (q k v, W_o, FFN)
+    c->sk_max_n = std::max(3 * d, std::max(d, g.ffn));
+    const size_t tiles = static_cast<size_t>(cdiv(c->sk_max_n, 128));
+    ok = dalloc(&c->sk_acc, tiles * 512 * 128 * sizeof(float)) && dalloc(&c->sk_tickets, tiles * sizeof(unsigned));
+    if (ok)
+      ok = cudaMemset(c->sk_acc, 0, tiles * 512 * 128 * sizeof(float)) == cudaSuccess &&
+           cudaMemset(c->sk_tickets, 0, tiles * sizeof(unsigned)) == cudaSuccess;
+  }
+  if (ok && g.facache) {
+    const size_t bh = static_cast<size_t>(g.batch) * g.n_heads;
+    ok = dalloc(&c->fa_state, bh * 64 * (g.head_dim + 4) * sizeof(float)) &&
+         dalloc(&c->fa_key, bh * 66 * sizeof(int)) && dalloc(&c->fa_rebuilt, sizeof(int));
+  }
   if (!ok) {
     free_all(c);
     delete c;
@@ -266,6 +285,10 @@ dllm_status dllm_state_copy(dllm_cache* c, int field, int layer, void* host, siz
   } else if (field == DLLM_FIELD_HIST_N) {
     ptr = c->hist_n;
     size = g.batch * blk * sizeof(int);
+  } else if (field == DLLM_FIELD_FA_REBUILT) {
+    if (!c->fa_rebuilt) return fail(DLLM_EINVAL, "dllm_state_copy: the cache keeps no attention state");
+    ptr = c->fa_rebuilt;
+    size = sizeof(int);
   } else {
     return fail(DLLM_EINVAL, "dllm_state_copy: unknown field");
   }
@@ -333,6 +356,10 @@ dllm_status block_attn(dllm_cache* c, int layer, int q_start, int q_len, void* o
     return fail(DLLM_EINVAL, "block_attn: query range outside the sequence");
   if (g.dtype == DLLM_BF16 && q_len > 64) return fail(DLLM_EUNSUPPORTED, "block_attn: q_len > 64");
   ProfScope prof(c, DLLM_PROF_ATTN, st);
+  if (g.facache && layer == 0) {
+    DLLM_LAUNCH(attn_facache(c, q_start, q_len, out_dev, st), "block_attn");
+    return DLLM_OK;
+  }
   DLLM_LAUNCH(attn_dense(c, layer, q_start, q_len, g.seq_len, g.batch, out_dev, st), "block_attn");
   return DLLM_OK;
 }
@@ -427,12 +454,13 @@ dllm_status lmhead_conf(dllm_cache* c, const void* h_dev, const void* w_lm_dev, 
     DLLM_LAUNCH(gemm_lm(c, h_dev, w_lm_dev, M, V, d, c->lm_rs, mask_id, c->lm_part, n_tiles, st),
                 "lmhead_conf: gemm");
   }
-  DLLM_LAUNCH(launch_lm_merge(c->lm_part, M, n_tiles, argmax_dev, p_top1_dev, entropy_dev, st), "lmhead_conf: merge");
+  DLLM_LAUNCH(launch_lm_merge(c->lm_part, M, n_tiles, argmax_dev, p_top1_dev, entropy_dev, nullptr, st), "lmhead_conf: merge");
   return DLLM_OK;
 }
 
 dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p_top1_dev, int32_t* tok_dev,
-                        int q_start, int t, int last_step, int32_t* rows_dev, int32_t* n_rows_dev, void* stream) {
+                        int q_start, int t, int step_in_block, int last_step, int32_t* rows_dev, int32_t* n_rows_dev,
+                        void* stream) {
   DLLM_CHECK_HANDLE(c);
   const dllm_cache_cfg& g = c->cfg;
   if (g.sink > 0) return fail(DLLM_EINVAL, "stab_update: dense mode only");
@@ -440,9 +468,24 @@ dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p
     return fail(DLLM_EINVAL, "stab_update: null pointer");
   if (q_start < 0 || q_start + g.block_len > g.seq_len)
     return fail(DLLM_EINVAL, "stab_update: active block outside the sequence");
-  DLLM_LAUNCH(launch_stab(c, argmax_dev, p_top1_dev, tok_dev, q_start, t, last_step ? 1 : 0, rows_dev, n_rows_dev,
-                          static_cast<cudaStream_t>(stream)),
+  if (step_in_block < 0) return fail(DLLM_EINVAL, "stab_update: step_in_block < 0");
+  // the schedules of the next step's refresh set
+  const int s1 = step_in_block + 1;
+  int R_next = g.swd_R;
+  if (g.swd_R_min >= 0 && g.steps_per_block > 0)
+    R_next = std::min(g.swd_R, g.swd_R_min + ((g.swd_R - g.swd_R_min + 1) * s1) / g.steps_per_block);
+  const int full_next = (g.full_every > 0 && s1 % g.full_every == 0) ? 1 : 0;
+  DLLM_LAUNCH(launch_stab(c, argmax_dev, p_top1_dev, tok_dev, q_start, t, last_step ? 1 : 0, R_next, full_next,
+                          rows_dev, n_rows_dev, static_cast<cudaStream_t>(stream)),
               "stab_update");
+  return DLLM_OK;
+}
+
+dllm_status dllm_wait_selftest(dllm_cache* c, uint64_t limit_ns, void* stream) {
+  DLLM_CHECK_HANDLE(c);
+  if (limit_ns < 1000 || limit_ns > 2000000000ull)
+    return fail(DLLM_EINVAL, "dllm_wait_selftest: limit_ns outside [1e3, 2e9]");
+  DLLM_LAUNCH(launch_wait_selftest(c, limit_ns, static_cast<cudaStream_t>(stream)), "dllm_wait_selftest");
   return DLLM_OK;
 }
 

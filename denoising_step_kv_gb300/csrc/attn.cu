@@ -5,6 +5,7 @@
 #include <algorithm>
 
 #include "attn_tc.cuh"
+#include "attn_fa.cuh"
 #include "attn_rows.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -61,11 +62,10 @@ cudaError_t launch_tc_r(dllm_cache* c, const uint8_t* Ql, const uint8_t* Kl, con
   const int per = cdiv(tiles, n_split);
   n_split = cdiv(tiles, per);
   const int keys_per_split = per * attn_tc::KT;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(attn_tc::attn_tc_kernel<DH, R>, S::SMEM);
+  static PerDeviceOnce attr;
+  {
+    const cudaError_t e = set_smem_once(attr, attn_tc::attn_tc_kernel<DH, R>, S::SMEM);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(DH));
   return launch_ex(attn_tc::attn_tc_kernel<DH, R>, dim3(n_split, H, n_seq), dim3(192), S::SMEM, st, n_split, Ql, Kl,
@@ -87,11 +87,10 @@ template <int DH>
 cudaError_t launch_rows(dllm_cache* c, const uint8_t* Ql, const uint8_t* Kl, const uint8_t* Vl, const int* rows,
                         const int* n_rows, bf16* out, cudaStream_t st) {
   using S = attn_rows::Shape<DH>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(attn_rows::attn_rows_kernel<DH>, S::SMEM);
+  static PerDeviceOnce attr;
+  {
+    const cudaError_t e = set_smem_once(attr, attn_rows::attn_rows_kernel<DH>, S::SMEM);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(DH));
   return launch_ex(attn_rows::attn_rows_kernel<DH>, dim3(c->num_sms), dim3(192), S::SMEM, st, 0, Ql, Kl, Vl, c->kv,
@@ -107,6 +106,41 @@ cudaError_t attn_rows_dense(dllm_cache* c, int layer, const int* rows, const int
   bf16* o = static_cast<bf16*>(out);
   if (c->cfg.head_dim == 128) return launch_rows<128>(c, Ql, Kl, Vl, rows, n_rows, o, st);
   if (c->cfg.head_dim == 64) return launch_rows<64>(c, Ql, Kl, Vl, rows, n_rows, o, st);
+  return cudaErrorInvalidValue;
+}
+
+template <int DH, int R>
+cudaError_t launch_fa_r(dllm_cache* c, int q_pos0, int q_len, bf16* out, cudaStream_t st) {
+  using S = attn_fa::Shape<DH, R>;
+  static PerDeviceOnce attr;
+  {
+    const cudaError_t e = set_smem_once(attr, attn_fa::attn_fa_kernel<DH, R>, S::SMEM);
+    if (e != cudaSuccess) return e;
+  }
+  const int L = c->cfg.seq_len, Rd = c->cfg.swd_R;
+  // the window: every 64-key tile that [q0 - R, q0 + q_len + R) touches
+  const int w_lo = std::max(0, q_pos0 - Rd) / attn_tc::KT;
+  const int w_hi = (std::min(L, q_pos0 + q_len + Rd) - 1) / attn_tc::KT + 1;
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(DH));
+  const uint8_t* Ql = static_cast<const uint8_t*>(c->q);     // layer 0
+  const uint8_t* Kl = static_cast<const uint8_t*>(c->k);
+  const uint8_t* Vl = static_cast<const uint8_t*>(c->v);
+  return launch_ex(attn_fa::attn_fa_kernel<DH, R>, dim3(c->cfg.n_heads, c->cfg.batch), dim3(192), S::SMEM, st, 0, Ql,
+                   Kl, Vl, c->kv, c->d, q_pos0, q_len, L, w_lo, w_hi, scale_log2, c->tok_w, L, c->fa_state,
+                   c->fa_key, out, c->err, c->fa_rebuilt);
+}
+
+cudaError_t attn_facache(dllm_cache* c, int q_pos0, int q_len, void* out, cudaStream_t st) {
+  bf16* o = static_cast<bf16*>(out);
+  const int dh = c->cfg.head_dim;
+  if (dh == 128) {
+    if (q_len <= 32) return launch_fa_r<128, 4>(c, q_pos0, q_len, o, st);
+    return launch_fa_r<128, 2>(c, q_pos0, q_len, o, st);
+  }
+  if (dh == 64) {
+    if (q_len <= 32) return launch_fa_r<64, 4>(c, q_pos0, q_len, o, st);
+    return launch_fa_r<64, 2>(c, q_pos0, q_len, o, st);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "dllm_kv.h"
 #include "kv_layout.h"
 
@@ -23,6 +25,25 @@ inline cudaError_t set_smem(F* fn, size_t bytes) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                              static_cast<int>(cudaSharedmemCarveoutMaxShared));
+  return e;
+}
+
+// cudaFuncSetAttribute applies to the current device only: a launcher keeps
+// one of these and sets a kernel's attributes once per device (devices 64 and
+// up set them on every call).
+struct PerDeviceOnce {
+  std::atomic<uint64_t> done{0};
+};
+
+template <class F>
+inline cudaError_t set_smem_once(PerDeviceOnce& once, F* fn, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (once.done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = set_smem(fn, bytes);
+  if (e == cudaSuccess && bit) once.done.fetch_or(bit, std::memory_order_release);
   return e;
 }
 
@@ -161,22 +182,29 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase of `bar` with the given parity has completed.  Gives
-// up after kWaitLimitNs or when *abort becomes non-zero; returns false then.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          unsigned* err) {
+// up after limit_ns, setting DLLM_ERR_TIMEOUT and *abort, or when *abort
+// becomes non-zero; returns false then.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err,
+                                              uint64_t limit_ns) {
   if (mbar_try(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 0;; ++i) {
     if (mbar_try(bar, parity)) return true;
     if ((i & 63) == 63) {
       if (abort && *abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         set_err(err, DLLM_ERR_TIMEOUT);
         if (abort) *abort = 1;
         return false;
       }
     }
   }
+}
+
+// The wait every kernel uses: limit kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          unsigned* err) {
+  return mbar_wait_for(bar, parity, abort, err, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------- TMA
@@ -209,6 +237,16 @@ __device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
       : "memory");
+}
+
+// Order this thread's generic shared-memory writes before later async-proxy
+// (bulk copy) reads of them, and completed async-proxy global writes before
+// later generic accesses.
+__device__ __forceinline__ void fence_async_smem_cta() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Bring [p, p + bytes) into L2 (one prefetch per 128-byte line).

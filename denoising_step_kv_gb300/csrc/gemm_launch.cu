@@ -13,11 +13,10 @@ template <class Epi, int STAGES>
 cudaError_t launch_persistent(dllm_cache* c, const CUtensorMap& ta, const CUtensorMap& tb, int a_rows, int M_host,
                               const int* M_dev, int M_min, int N, int K, const Epi& epi, cudaStream_t st) {
   constexpr size_t smem = tc::smem_bytes<STAGES>();
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(tc::gemm_tc_kernel<Epi, STAGES>, smem);
+  static PerDeviceOnce attr;
+  {
+    const cudaError_t e = set_smem_once(attr, tc::gemm_tc_kernel<Epi, STAGES>, smem);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const int m_rows = M_dev ? a_rows : M_host;
   const int tiles = cdiv(m_rows, tc::BM) * cdiv(N, tc::BN);
@@ -31,11 +30,10 @@ template <class Epi, int STAGES>
 cudaError_t launch_pair(dllm_cache* c, const CUtensorMap& ta, const CUtensorMap& tb, int a_rows, int M_host,
                         const int* M_dev, int M_min, int N, int K, const Epi& epi, cudaStream_t st) {
   constexpr size_t smem = tc::pair_smem_bytes<STAGES>();
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(tc::gemm_pair_kernel<Epi, STAGES>, smem);
+  static PerDeviceOnce attr;
+  {
+    const cudaError_t e = set_smem_once(attr, tc::gemm_pair_kernel<Epi, STAGES>, smem);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const int m_rows = M_dev ? a_rows : M_host;
   const int pairs = cdiv(cdiv(m_rows, tc::BM), 2) * cdiv(N, tc::PBN);
@@ -48,11 +46,10 @@ template <class Epi, int STAGES, int CS, int SBN>
 cudaError_t launch_sharea(dllm_cache* c, const void* A, int M, const void* B, int N, int K, const Epi& epi,
                           cudaStream_t st) {
   constexpr size_t smem = tc::sharea_smem_bytes<STAGES, SBN>();
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(tc::gemm_sharea_kernel<Epi, STAGES, CS, SBN>, smem);
+  static PerDeviceOnce attr;
+  {
+    const cudaError_t e = set_smem_once(attr, tc::gemm_sharea_kernel<Epi, STAGES, CS, SBN>, smem);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   CUtensorMap ta, tb;
   if (!make_tmap_2d(&ta, A, K, M, static_cast<uint64_t>(K) * 2, tc::BK, tc::BM / CS, true) ||
@@ -68,11 +65,10 @@ cudaError_t launch_sharea(dllm_cache* c, const void* A, int M, const void* B, in
 template <class Epi, int S>
 cudaError_t launch_skinny(dllm_cache* c, const void* A, int a_rows, int M_host, const int* M_dev, const void* W,
                           int N, int K, const Epi& epi, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(tc::gemm_skinny_kernel<Epi, S>, tc::SKN_SMEM);
+  static PerDeviceOnce attr;
+  {
+    const cudaError_t e = set_smem_once(attr, tc::gemm_skinny_kernel<Epi, S>, tc::SKN_SMEM);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   CUtensorMap tw, tx;
   if (!make_tmap_2d(&tw, W, K, N, static_cast<uint64_t>(K) * 2, tc::BK, 128, true) ||
@@ -82,32 +78,58 @@ cudaError_t launch_skinny(dllm_cache* c, const void* A, int a_rows, int M_host, 
                    tx, M_host, M_dev, a_rows, N, K, epi, c->err);
 }
 
+template <class Epi>
+cudaError_t launch_streamk(dllm_cache* c, const void* A, int a_rows, int M_host, const int* M_dev, const void* W,
+                           int N, int K, const Epi& epi, cudaStream_t st) {
+  static PerDeviceOnce attr;
+  {
+    const cudaError_t e = set_smem_once(attr, tc::gemm_streamk_kernel<Epi>, tc::SK_SMEM);
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap tw, tx;
+  if (!make_tmap_2d(&tw, W, K, N, static_cast<uint64_t>(K) * 2, tc::BK, 128, true) ||
+      !make_tmap_2d(&tx, A, K, a_rows, static_cast<uint64_t>(K) * 2, tc::BK, tc::SKN_XBOX, true))
+    return cudaErrorInvalidValue;
+  const long long units = static_cast<long long>(cdiv(N, 128)) * cdiv(K, tc::BK);
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(c->num_sms, units)));
+  return launch_ex(tc::gemm_streamk_kernel<Epi>, dim3(grid), dim3(tc::THREADS), tc::SK_SMEM, st, 0, tw, tx, M_host,
+                   M_dev, a_rows, N, K, epi, c->sk_acc, c->sk_tickets, c->err);
+}
+
+// Epilogues that run on the stream-K kernel (the LM head keeps its own kernels).
+template <class Epi> struct StreamKOk { static constexpr bool value = true; };
+template <> struct StreamKOk<EpiLM> { static constexpr bool value = false; };
+
 // Clusters of the weight-streaming kernel (split s) that fit on the GPU at
 // once: clusters must sit inside one GPC, so this can be below num_sms / s.
 template <class Epi, int S>
 int skinny_resident(dllm_cache* c) {
-  static int n = -1;
-  if (n < 0) {
-    if (set_smem(tc::gemm_skinny_kernel<Epi, S>, tc::SKN_SMEM) != cudaSuccess) return 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(S * c->num_sms);
-    cfg.blockDim = dim3(tc::THREADS);
-    cfg.dynamicSmemBytes = tc::SKN_SMEM;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = S;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    int k = 0;
-    if (cudaOccupancyMaxActiveClusters(&k, tc::gemm_skinny_kernel<Epi, S>, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      k = 0;
-    }
-    n = k;
+  static std::atomic<int> known[64];     // per device: clusters + 1, 0 = not yet asked
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 64) {
+    const int k = known[dev].load(std::memory_order_acquire);
+    if (k > 0) return k - 1;
   }
-  return n;
+  if (set_smem(tc::gemm_skinny_kernel<Epi, S>, tc::SKN_SMEM) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S * c->num_sms);
+  cfg.blockDim = dim3(tc::THREADS);
+  cfg.dynamicSmemBytes = tc::SKN_SMEM;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = S;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int k = 0;
+  if (cudaOccupancyMaxActiveClusters(&k, tc::gemm_skinny_kernel<Epi, S>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    k = 0;
+  }
+  if (dev < 64) known[dev].store(k + 1, std::memory_order_release);
+  return k;
 }
 
 // Split of K for the weight-streaming kernel: the largest, up to 4, whose
@@ -147,6 +169,23 @@ template <class Epi>
 cudaError_t run_tc(dllm_cache* c, const void* A, int a_rows, int M_host, const int* M_dev, const void* B, int N,
                    int K, const Epi& epi, cudaStream_t st, bool wide_ok = true) {
   if (!M_dev && M_host <= 0) return cudaSuccess;
+  if (StreamKOk<Epi>::value && c->sk_acc && N <= c->sk_max_n) {
+    // up to SK_MAX_ROWS rows: stream-K weight streaming; beyond: the large-M kernels
+    const int m_rows = M_dev ? a_rows : M_host;
+    cudaError_t e = cudaSuccess;
+    if (M_dev || M_host <= tc::SK_MAX_ROWS) {
+      e = launch_streamk(c, A, a_rows, M_host, M_dev, B, N, K, epi, st);
+      if (e != cudaSuccess || m_rows <= tc::SK_MAX_ROWS) return e;
+    }
+    CUtensorMap ta, tb;
+    if (!make_tmap_2d(&ta, A, K, a_rows, static_cast<uint64_t>(K) * 2, tc::BK, tc::BM, true) ||
+        !make_tmap_2d(&tb, B, K, N, static_cast<uint64_t>(K) * 2, tc::BK, tc::BN, true))
+      return cudaErrorInvalidValue;
+    const int M_min = tc::SK_MAX_ROWS + 1;
+    if (wide_ok && N % tc::PBN == 0)
+      return launch_pair<Epi, 4>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
+    return launch_persistent<Epi, 4>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
+  }
   const int split = skinny_split<Epi>(c, N);
   const int m_rows = M_dev ? a_rows : M_host;     // most rows this call can see
   cudaError_t e = cudaSuccess;

@@ -44,6 +44,15 @@ struct dllm_cache {
   int lm_rows_cap = 0, lm_tiles_cap = 0;
   void* ffn_buf = nullptr;  // [seq_rows][ffn]
   int ffn_cap = 0;
+  // kept online-softmax state of the unchanged key tiles (cfg.facache)
+  float* fa_state = nullptr;  // [B][H][64][head_dim + 4]: O~, m (log2 domain), l
+  int* fa_key = nullptr;      // [B][H][66]: block start, block length, token-at-write of the queries
+  int* fa_rebuilt = nullptr;  // (sequence, head) states rebuilt since the last reset
+  // stream-K weight-streaming GEMM: per 128-column tile an fp32 accumulator
+  // [512][128] (kept zero between launches) and an arrival ticket
+  float* sk_acc = nullptr;
+  unsigned* sk_tickets = nullptr;
+  int sk_max_n = 0;           // widest N (output columns) the accumulators cover
   // measurement hook: events bracketing a kernel (index = dllm_prof_kernel)
   cudaEvent_t prof_begin[8] = {};
   cudaEvent_t prof_end[8] = {};
@@ -139,17 +148,24 @@ cudaError_t launch_active_rows(dllm_cache* c, const void* src, const int* rows, 
                                int q_len, void* dst, cudaStream_t st);
 cudaError_t attn_dense(dllm_cache* c, int layer, int q_pos0, int q_len, int kv_len, int n_seq, void* out,
                        cudaStream_t st);
+// Layer-0 attention of the active block with the kept state of the
+// unchanged key tiles (bf16, q_len <= 64).
+cudaError_t attn_facache(dllm_cache* c, int q_pos0, int q_len, void* out, cudaStream_t st);
 
 // misc.cu ------------------------------------------------------------------
 cudaError_t launch_gather(dllm_cache* c, int layer, const int* rows, const int* n_rows, int n_host,
                           const void* x, const int* tok, const void* embed, int t, cudaStream_t st);
 cudaError_t launch_rownorm(dllm_cache* c, const void* h, int M, const int* M_dev, int d, float* rs,
                            cudaStream_t st);
+// fail_word: see lm_merge_kernel (null: always merge)
 cudaError_t launch_lm_merge(const void* part, int M, int n_tiles, int* argmax, float* p1, float* ent,
-                            cudaStream_t st);
+                            const unsigned* fail_word, cudaStream_t st);
+// R: dilation radius of the next step's refresh set; full: the next step
+// refreshes every row (the schedules of stab_update)
 cudaError_t launch_stab(dllm_cache* c, const int* argmax, const float* p1, int* tok, int q_start, int t,
-                        int last, int* rows, int* n_rows, cudaStream_t st);
+                        int last, int R, int full, int* rows, int* n_rows, cudaStream_t st);
 cudaError_t launch_refresh_all(dllm_cache* c, int q_start, int* rows, int* n_rows, cudaStream_t st);
 cudaError_t launch_reset(dllm_cache* c, cudaStream_t st);
+cudaError_t launch_wait_selftest(dllm_cache* c, uint64_t limit_ns, cudaStream_t st);
 
 }  // namespace dllm

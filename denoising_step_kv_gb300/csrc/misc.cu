@@ -128,16 +128,28 @@ __global__ void __launch_bounds__(256) rownorm_kernel(const T* __restrict__ h, i
 
 // One 128-thread CTA per row: every thread merges its tiles in increasing
 // vocab order, then a tree merge across threads (ties: lower index wins).
+// fail_word (may be null): an error word of this call alone; when any bit is
+// set (a wait of the GEMM gave up, so some partials were never written) the
+// row gets argmax -1 and NaN probability and entropy instead.
 constexpr int MERGE_THREADS = 128;
 __global__ void __launch_bounds__(MERGE_THREADS) lm_merge_kernel(const LMPart* __restrict__ part, int M,
                                                                  int n_tiles, int* __restrict__ argmax,
-                                                                 float* __restrict__ p1, float* __restrict__ ent) {
+                                                                 float* __restrict__ p1, float* __restrict__ ent,
+                                                                 const unsigned* __restrict__ fail_word) {
   __shared__ float s_m[MERGE_THREADS / 32], s_s[MERGE_THREADS / 32], s_a[MERGE_THREADS / 32];
   __shared__ int s_i[MERGE_THREADS / 32];
   const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_launch();
   pdl_wait();
   if (i >= M) return;
+  if (fail_word && *fail_word != 0u) {
+    if (tid == 0) {
+      argmax[i] = -1;
+      p1[i] = __int_as_float(0x7fc00000);
+      ent[i] = __int_as_float(0x7fc00000);
+    }
+    return;
+  }
   float m = -INFINITY, s = 0.f, a = 0.f;
   int idx = 0x7fffffff;
   for (int tt = tid; tt < n_tiles; tt += MERGE_THREADS) {
@@ -173,7 +185,7 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
     const int* __restrict__ argmax, const float* __restrict__ p1, int* __restrict__ tok,
     uint8_t* __restrict__ stable, int* __restrict__ hist_tok, float* __restrict__ hist_p, int* __restrict__ hist_n,
     const int* __restrict__ tok_w, const int* __restrict__ version, uint32_t* __restrict__ words, int L, int Lw,
-    int seq_rows, int n_layers, int blk, int K, float tau, int R, int q0, int t, int last, int expiry,
+    int seq_rows, int n_layers, int blk, int K, float tau, int R, int q0, int t, int last, int full, int expiry,
     int active_queries, unsigned* __restrict__ ticket, int* __restrict__ rows, int* __restrict__ n_rows) {
   __shared__ uint8_t s_unst[64];
   __shared__ int s_last;
@@ -250,7 +262,7 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
     bool f = false;
     if (p < L) {
       const int r = b * L + p;
-      if (last) {
+      if (last || full) {
         f = true;
       } else {
         // independent loads (no short-circuit between them): any layer's
@@ -277,7 +289,7 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
   if (!s_last) return;
   __threadfence();
   // the row list: the refresh set, plus every active row when they all query
-  compact_words(words, gridDim.x * Lw, L, Lw, q0, active_queries && !last ? nac : 0, rows, n_rows);
+  compact_words(words, gridDim.x * Lw, L, Lw, q0, active_queries && !last && !full ? nac : 0, rows, n_rows);
   if (threadIdx.x == 0) *ticket = 0u;
 }
 
@@ -387,7 +399,33 @@ __global__ void __launch_bounds__(256) active_rows_kernel(const uint4* __restric
   for (int c = lane; c < row_vec; c += 32) o[c] = found ? s[c] : make_uint4(0u, 0u, 0u, 0u);
 }
 
+// The bounded wait on a barrier that nothing arrives on: thread 0 gives up
+// after limit_ns, sets DLLM_ERR_TIMEOUT and raises the CTA's abort flag; lane
+// 0 of every other warp waits on a second such barrier (limit 4 x limit_ns)
+// and leaves through that flag.  Every thread then returns normally.
+__global__ void __launch_bounds__(128) wait_selftest_kernel(uint64_t limit_ns, unsigned* err) {
+  __shared__ uint64_t bar_a, bar_b;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_a, 1);
+    mbar_init(&bar_b, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    mbar_wait_for(&bar_a, 0, &abort_flag, err, limit_ns);
+  else if ((threadIdx.x & 31) == 0)
+    mbar_wait_for(&bar_b, 0, &abort_flag, nullptr, 4 * limit_ns);
+  __syncthreads();
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(dllm_cache* c, uint64_t limit_ns, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 128, 0, st>>>(limit_ns, c->err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_active_rows(dllm_cache* c, const void* src, const int* rows, const int* n_rows, int q_start,
                                int q_len, void* dst, cudaStream_t st) {
@@ -432,18 +470,18 @@ cudaError_t launch_rownorm(dllm_cache* c, const void* h, int M, const int* M_dev
 }
 
 cudaError_t launch_lm_merge(const void* part, int M, int n_tiles, int* argmax, float* p1, float* ent,
-                            cudaStream_t st) {
+                            const unsigned* fail_word, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
   return launch_ex(lm_merge_kernel, dim3(M), dim3(MERGE_THREADS), 0, st, 0, static_cast<const LMPart*>(part), M,
-                   n_tiles, argmax, p1, ent);
+                   n_tiles, argmax, p1, ent, fail_word);
 }
 
 cudaError_t launch_stab(dllm_cache* c, const int* argmax, const float* p1, int* tok, int q_start, int t, int last,
-                        int* rows, int* n_rows, cudaStream_t st) {
+                        int R, int full, int* rows, int* n_rows, cudaStream_t st) {
   const dllm_cache_cfg& g = c->cfg;
   return launch_ex(swd_kernel, dim3(g.batch), dim3(1024), 0, st, 0, argmax, p1, tok, c->stable, c->hist_tok, c->hist_p,
                    c->hist_n, c->tok_w, c->version, c->words, g.seq_len, c->Lw, c->seq_rows, g.n_layers, g.block_len,
-                   g.swd_K, g.swd_tau, g.swd_R, q_start, t, last, g.expiry, g.active_queries, c->ticket, rows,
+                   g.swd_K, g.swd_tau, R, q_start, t, last, full, g.expiry, g.active_queries, c->ticket, rows,
                    n_rows);
 }
 
@@ -456,6 +494,17 @@ cudaError_t launch_refresh_all(dllm_cache* c, int q_start, int* rows, int* n_row
 
 cudaError_t launch_reset(dllm_cache* c, cudaStream_t st) {
   const dllm_cache_cfg& g = c->cfg;
+  if (c->sk_acc) {   // stream-K accumulators and tickets (left dirty only by a wait that gave up)
+    const size_t tiles = static_cast<size_t>(cdiv(c->sk_max_n, 128));
+    cudaError_t e = cudaMemsetAsync(c->sk_acc, 0, tiles * 512 * 128 * sizeof(float), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->sk_tickets, 0, tiles * sizeof(unsigned), st);
+    if (e != cudaSuccess) return e;
+  }
+  if (c->fa_key) {   // no kept attention state is valid (block start -1 never matches)
+    cudaError_t e = cudaMemsetAsync(c->fa_key, 0xff, static_cast<size_t>(g.batch) * g.n_heads * 66 * sizeof(int), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->fa_rebuilt, 0, sizeof(int), st);
+    if (e != cudaSuccess) return e;
+  }
   const int nv = g.n_layers * c->seq_rows;
   const int nh = g.batch * g.block_len;
   reset_kernel<<<std::max(1, std::min(cdiv(std::max(nv, c->seq_rows), 256), 1024)), 256, 0, st>>>(

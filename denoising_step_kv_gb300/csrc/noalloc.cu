@@ -66,7 +66,7 @@ extern "C" dllm_status lmhead_conf_noalloc(const void* h_dev, const void* w_lm_d
     return na_fail(DLLM_EINVAL, "lmhead_conf_noalloc: M outside [0, 256] (the static scratch's row limit)");
   if (V < 2 || V > NA_MAX_VOCAB)
     return na_fail(DLLM_EINVAL, "lmhead_conf_noalloc: V outside [2, 131072] (the static scratch's vocab limit)");
-  if (d < 8 || d % 8 != 0) return na_fail(DLLM_EINVAL, "lmhead_conf_noalloc: d must be a positive multiple of 8");
+  if (d < 64 || d % 64 != 0) return na_fail(DLLM_EINVAL, "lmhead_conf_noalloc: d must be a positive multiple of 64");
   if (mask_id >= V) return na_fail(DLLM_EINVAL, "lmhead_conf_noalloc: mask_id >= V");
   if (!(rms_eps >= 0.f)) return na_fail(DLLM_EINVAL, "lmhead_conf_noalloc: rms_eps < 0");
   if ((reinterpret_cast<uintptr_t>(h_dev) | reinterpret_cast<uintptr_t>(w_lm_dev)) & 15u)
@@ -95,11 +95,13 @@ extern "C" dllm_status lmhead_conf_noalloc(const void* h_dev, const void* w_lm_d
   float* rs = reinterpret_cast<float*>(scratch + NA_RS_OFF);
   const int n_tiles = cdiv(V, lm_tile_cols(&ctx, M, V));
   // the error word is the only scratch that must start at zero; the
-  // statistics and row scales are fully rewritten by every call
+  // statistics and row scales are fully rewritten by every call.  A wait
+  // that gives up leaves some statistics unwritten and sets the word, and
+  // the merge then writes argmax -1 and NaN instead of stale results.
   if ((e = cudaMemsetAsync(ctx.err, 0, sizeof(unsigned), st)) != cudaSuccess ||
       (e = launch_rownorm(&ctx, h_dev, M, nullptr, d, rs, st)) != cudaSuccess ||
       (e = gemm_lm(&ctx, h_dev, w_lm_dev, M, V, d, rs, mask_id, scratch, n_tiles, st)) != cudaSuccess ||
-      (e = launch_lm_merge(scratch, M, n_tiles, argmax_dev, p_top1_dev, entropy_dev, st)) != cudaSuccess)
+      (e = launch_lm_merge(scratch, M, n_tiles, argmax_dev, p_top1_dev, entropy_dev, ctx.err, st)) != cudaSuccess)
     return na_fail(DLLM_ECUDA, std::string("lmhead_conf_noalloc: ") + cudaGetErrorString(e));
   return DLLM_OK;
 }

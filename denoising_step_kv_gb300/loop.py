@@ -34,15 +34,17 @@ def to_device(a, device="cuda"):
 
 
 class DenseGenerator:
-    """Single-layer cached denoiser (dense positional cache)."""
+    """Single-layer cached denoiser (dense positional cache).  facache: the
+    attention keeps the softmax state of the key tiles outside the block's
+    window (bf16 only; see block_attn)."""
 
-    def __init__(self, w, weights, device="cuda"):
+    def __init__(self, w, weights, device="cuda", facache=False):
         assert not w.streaming and w.n_layers == 1 and not w.ffn
         self.w = w
         self.W = weights
         B, L, d, blk = w.batch, w.seq_len, w.d_model, w.block_len
         dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
-        self.cache = K.dllm_cache_init(K.make_cfg(w))
+        self.cache = K.dllm_cache_init(K.make_cfg(w, facache=facache))
         i32 = dict(dtype=torch.int32, device=device)
         self.tok = torch.zeros(B, L, **i32)
         self.rows = torch.zeros(B * L, **i32)
@@ -78,7 +80,7 @@ class DenseGenerator:
         K.attn_out(c, self.o, W["w_o"][0], None, self.tok, W["embed"], q0, blk, None, self.h, stream)
         K.lmhead_conf(c, self.h, W["w_lm"], w.batch * blk, w.vocab, w.d_model, w.mask_id, self.argmax,
                       self.p1, self.ent, stream)
-        K.stab_update(c, self.argmax, self.p1, self.tok, q0, t, s == w.steps_per_block - 1, self.rows,
+        K.stab_update(c, self.argmax, self.p1, self.tok, q0, t, s, s == w.steps_per_block - 1, self.rows,
                       self.n_rows, stream)
 
     def schedule(self):
@@ -208,7 +210,7 @@ class LayerStackGenerator:
         K.active_rows(c, self.O, self.rows, self.n_rows, q0, blk, self.o, stream)
         K.lmhead_conf(c, self.h, W["w_lm"], w.batch * blk, w.vocab, w.d_model, w.mask_id, self.argmax,
                       self.p1, self.ent, stream)
-        K.stab_update(c, self.argmax, self.p1, self.tok, q0, t, s == w.steps_per_block - 1, self.rows,
+        K.stab_update(c, self.argmax, self.p1, self.tok, q0, t, s, s == w.steps_per_block - 1, self.rows,
                       self.n_rows, stream)
 
     def make_prof_events(self, kernels, n_steps):

@@ -103,6 +103,19 @@ typedef struct {
   int max_pos;       /* RoPE positions (streaming: stream length); 0 = L */
   int ffn;           /* FFN width F of the multi-layer denoiser (0 = none);
                         sizes the FFN workspace */
+  int swd_R_min;     /* < 0: the dilation radius is swd_R at every step;
+                        else it grows with the block-local step s:
+                        R(s) = swd_R_min + floor((swd_R - swd_R_min + 1) s
+                        / steps_per_block) ("Stable Window Decoding" 4.4) */
+  int steps_per_block; /* Tb, the steps of a block (for the radius schedule) */
+  int full_every;    /* > 0: the refresh set of block-local steps s with
+                        s % full_every == 0 is every row ("I/O-aware KV cache
+                        and self-verifying parallel decoding" 5.1) */
+  int facache;       /* 1: block_attn keeps the online-softmax state of the
+                        key tiles outside the block's window and reuses it
+                        while the block and its query tokens are unchanged
+                        ("LaCache", Methodology 1, FACache); dense bf16
+                        single-layer caches only */
 } dllm_cache_cfg;
 
 /* Opaque handle: per-layer Q/K/V cache, versions, the token each row was
@@ -143,7 +156,9 @@ typedef enum {
   DLLM_FIELD_STABLE = 5,    /* uint8 [B*L] */
   DLLM_FIELD_HIST_TOK = 6,  /* int32 [B][block_len][swd_K] ring of top-1 ids */
   DLLM_FIELD_HIST_P = 7,    /* float [B][block_len][swd_K] ring of top-1 probs */
-  DLLM_FIELD_HIST_N = 8     /* int32 [B][block_len] records pushed this block */
+  DLLM_FIELD_HIST_N = 8,    /* int32 [B][block_len] records pushed this block */
+  DLLM_FIELD_FA_REBUILT = 9 /* int32 [1]: (sequence, head) attention states
+                               rebuilt since the last reset (facache) */
 } dllm_field;
 
 /* Blocking copy of one state field between the handle and HOST memory
@@ -189,7 +204,14 @@ dllm_status kv_refresh(dllm_cache* c, int layer, const void* x_dev, const int32_
      keys/values all L positions; out_dev [B][q_len][d].
    streaming: the query is stream token n = q_start (q_len = 1), keys/values
      the min(n + 1, S + W) entries the ring holds; out_dev [1][d].
-   Split-KV with an online-softmax merge; scratch owned by the handle. */
+   Split-KV with an online-softmax merge; scratch owned by the handle.
+   With cfg.facache (layer 0): the key tiles that [q_start - swd_R,
+   q_start + q_len + swd_R) touches form the window; the online-softmax state
+   (m, l, O~) of each (sequence, head, query) over all other tiles is kept
+   with the block start, q_len and the queries' token-at-write, and while
+   they are unchanged only the window's tiles are read and merged with it;
+   otherwise every tile is read and the state rebuilt.  The result equals the
+   plain attention up to fp32 rounding order. */
 dllm_status block_attn(dllm_cache* c, int layer, int q_start, int q_len, void* out_dev,
                        void* stream);
 
@@ -257,15 +279,18 @@ dllm_status lmhead_conf(dllm_cache* c, const void* h_dev, const void* w_lm_dev, 
      last_step != 0: every still-unstable active position commits its argmax,
      the history is cleared, and the next refresh set is the full set of the
      next block (as refresh_all(q_start + block_len)).
-     Otherwise rows = dilate_R(unstable active) U {tok != token-at-write}
-       U {(t + 1) - version > expiry}, ascending b * L + pos; with
+     Otherwise, with s = step_in_block (the block-local index of the step
+     just run): if cfg.full_every > 0 and (s + 1) % full_every == 0 every
+     row; else rows = dilate_R(unstable active) U {tok != token-at-write}
+       U {(t + 1) - version > expiry}, R = the radius of step s + 1 (see
+       cfg.swd_R_min), ascending b * L + pos; with
      active_queries the list also holds every active row (the refresh set
      itself stays in the handle and gates kv_refresh's K/V writes).
    argmax_dev / p_top1_dev: [B * block_len] device; tok_dev [B][L] device,
    updated in place; rows_dev [B * L], n_rows_dev [1] device outputs. */
 dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p_top1_dev,
-                        int32_t* tok_dev, int q_start, int t, int last_step, int32_t* rows_dev,
-                        int32_t* n_rows_dev, void* stream);
+                        int32_t* tok_dev, int q_start, int t, int step_in_block, int last_step,
+                        int32_t* rows_dev, int32_t* n_rows_dev, void* stream);
 
 /* --- without device allocation ---------------------------------------- */
 
@@ -278,7 +303,10 @@ dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p
    lmhead_conf, plus the storage dtype and the RMSNorm epsilon.
    Scratch lives in one static device array of 4 MiB + 1.25 KiB that every GPU
    which loads the library keeps until the process exits; it bounds a call to
-   M <= 256 rows and V <= 131072 (larger sizes return DLLM_EINVAL).  The first
+   M <= 256 rows and V <= 131072 (larger sizes return DLLM_EINVAL); d must
+   be a multiple of 64.  There is no handle to hold a device error word: if a
+   bounded wait inside the kernels gives up, the affected rows come back with
+   argmax -1 and NaN top-1 probability and entropy.  The first
    call on a device resolves the array's address on that device (the device
    must be current); make that first call before any stream capture.  Every
    call shares the array and leaves its contents behind: calls whose kernels
@@ -288,6 +316,18 @@ dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p
 dllm_status lmhead_conf_noalloc(const void* h_dev, const void* w_lm_dev, int M, int V, int d, int dtype,
                                 int mask_id, float rms_eps, int32_t* argmax_dev, float* p_top1_dev,
                                 float* entropy_dev, void* stream);
+
+/* --- diagnostics ------------------------------------------------------ */
+
+/* Exercise the bounded wait that every kernel's barrier waits use (no
+   counterpart on the pages; it tests the failure path without faulting the
+   GPU): one CTA waits on a shared-memory barrier that nothing arrives on,
+   gives up after limit_ns nanoseconds (1e3 .. 2e9; the kernels' own limit is
+   2 s), sets DLLM_ERR_TIMEOUT in the handle's error word and raises the
+   CTA's abort flag, through which its other waiting warps leave; every
+   thread then returns normally and the context stays usable.  Asynchronous
+   on `stream`; read the result with dllm_cache_check. */
+dllm_status dllm_wait_selftest(dllm_cache* c, uint64_t limit_ns, void* stream);
 
 /* --- measurement ------------------------------------------------------ */
 

@@ -1,5 +1,7 @@
 """Helpers of the GPU tests: device tensors from generated arrays and reads
 of the library's state through dllm_state_copy."""
+import functools
+
 import numpy as np
 import torch
 
@@ -111,3 +113,20 @@ def write_kv(c, field, layer, w, arr):
     flat = np.zeros(n, dtype=np.float64)
     flat[kv_index(B, L, w.n_heads, w.head_dim, esize)] = np.asarray(arr, dtype=np.float64).reshape(B, L, w.n_heads, w.head_dim)
     write_field(c, field, layer, flat, "bf16" if w.dtype == "bf16" else "f32")
+
+
+@functools.lru_cache(maxsize=8)
+def _kv_idx(B, L, H, dh, esize, seqs):
+    return torch.from_numpy(kv_index(B, L, H, dh, esize)[list(seqs)].reshape(-1))
+
+
+def read_kv_seqs(c, field, layer, w, seqs):
+    """Q/K/V of `layer` for the sequences `seqs` only, as [len(seqs), L, H,
+    dh] float64 (one read of the whole field, then only those rows decoded)."""
+    esize = 2 if w.dtype == "bf16" else 4
+    n = K.state_size(c, field, layer) // esize
+    host = torch.empty(n, dtype=torch.int16 if esize == 2 else torch.float32)
+    K.dllm_state_copy(c, field, layer, host, False)
+    vals = host[_kv_idx(w.batch, w.seq_len, w.n_heads, w.head_dim, esize, tuple(seqs))]
+    vals = vals.view(torch.bfloat16) if esize == 2 else vals
+    return vals.double().numpy().reshape(len(seqs), w.seq_len, w.n_heads, w.head_dim)

@@ -77,10 +77,11 @@ def test_kv_refresh_ragged_rows(name):
 
 
 @pytest.mark.parametrize("name", ["big_rows", "big_rows_dh64"])
-@pytest.mark.parametrize("n", [None, 700, 530, 513, 200])
+@pytest.mark.parametrize("n", [None, 700, 530, 513, 512, 300, 257, 200])
 def test_kv_refresh_large_m(name, n):
-    """Row counts above the weight-streaming range: the host count (every
-    row) and device counts on both sides of the 512-row switch."""
+    """Row counts around the weight-streaming range: the host count (every
+    row) and device counts on both sides of the 512-row switch (257..512: the
+    stream-K kernel's two-MMA, single-accumulator path)."""
     w, m, W, D = _setup(name)
     B, L, H, dh = w.batch, w.seq_len, w.n_heads, w.head_dim
     tok = G.integers(5, 1, w.vocab, (B, L))
@@ -333,7 +334,7 @@ def test_stab_update_random_state(name, last, seed):
         tok_d = i32(tok)
         rows = torch.full((B * L,), -1, dtype=torch.int32, device="cuda")
         n_rows = torch.zeros(1, dtype=torch.int32, device="cuda")
-        K.stab_update(c, i32(argmax), torch.from_numpy(p1.reshape(-1)).cuda(), tok_d, q0, t, last, rows, n_rows)
+        K.stab_update(c, i32(argmax), torch.from_numpy(p1.reshape(-1)).cuda(), tok_d, q0, t, 1, last, rows, n_rows)
         assert K.dllm_cache_check(c) == 0
         n = int(n_rows.item())
         assert n == len(rows_o)

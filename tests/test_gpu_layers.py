@@ -19,8 +19,6 @@ GPU's argmax and top-1 probabilities, bit for bit, at every step.  The
 12-layer shape runs one whole block (64 steps: full refreshes at block-local
 steps 0, 3, 6, ... from version expiry), and its sharp variant commits
 positions inside the block."""
-import functools
-
 import numpy as np
 import pytest
 import torch
@@ -28,7 +26,7 @@ import torch
 import oracle as O
 from denoising_step_kv_gb300 import _lib as K
 from denoising_step_kv_gb300 import loop
-from gpu_util import close, kv_index, read_field, tol, worst
+from gpu_util import close, read_field, read_kv_seqs, tol, worst
 from test_gpu_fullsize import _qkv_close, _qkv_worst
 from workloads import configs as C
 from workloads import generate as G
@@ -36,20 +34,7 @@ from workloads import generate as G
 pytestmark = pytest.mark.gpu
 
 
-@functools.lru_cache(maxsize=4)
-def _kv_idx(B, L, H, dh, seqs):
-    return torch.from_numpy(kv_index(B, L, H, dh, 2)[list(seqs)].reshape(-1))
-
-
-def _kv_seqs(c, field, layer, w, seqs):
-    """Q/K/V of `layer` for the sequences `seqs` as [len(seqs), L, H, dh] f64
-    (one device read of the whole field, then only those rows decoded)."""
-    n = K.state_size(c, field, layer) // 2
-    host = torch.empty(n, dtype=torch.int16)
-    K.dllm_state_copy(c, field, layer, host, False)
-    idx = _kv_idx(w.batch, w.seq_len, w.n_heads, w.head_dim, tuple(seqs))
-    shape = (len(seqs), w.seq_len, w.n_heads, w.head_dim)
-    return host[idx].view(torch.bfloat16).double().numpy().reshape(shape)
+_kv_seqs = read_kv_seqs
 
 
 def _rows_f64(t, idx):
@@ -187,7 +172,7 @@ def _teacher_forced(name, n_steps, seqs=None, n_per_seq=None):
             last = s == w.steps_per_block - 1
             newly = O.swd_update(swd, q0, g_am, g_p1, tok_o, stable_o, w.swd_K, w.swd_tau, last)
             stats["commits"] += int(newly.sum())
-            K.stab_update(gen.cache, gen.argmax, gen.p1, gen.tok, q0, t, last, gen.rows, gen.n_rows)
+            K.stab_update(gen.cache, gen.argmax, gen.p1, gen.tok, q0, t, s, last, gen.rows, gen.n_rows)
             if last:
                 swd.reset()
                 rf = np.arange(B * L)
@@ -221,6 +206,7 @@ def test_layers_teacher_forced_twelve_layer_block(name):
     sequences 0, 7 and 15."""
     w = C.get(name)
     stats = _teacher_forced(name, w.steps_per_block, seqs=[0, 7, 15], n_per_seq=24)
-    assert stats["full"] >= w.steps_per_block // 3          # version expiry waves
     if name.endswith("sharp"):
         assert stats["commits"] > 0
+    else:           # version expiry: every row at block-local steps 0, 3, 6, ...
+        assert stats["full"] >= w.steps_per_block // 3

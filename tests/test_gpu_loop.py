@@ -27,7 +27,7 @@ def _ambiguous(rec, w):
 
 
 @pytest.mark.parametrize("name", ["tiny_fp32", "tiny_fp32_sharp", "mid_bf16", "mid_bf16_dh64", "mid_bf16_sharp",
-                                  "big_rows"])
+                                  "big_rows", "mid_bf16_sched"])
 def test_free_running_generation(name):
     w = C.get(name)
     m = G.model(w)
@@ -102,7 +102,7 @@ def _load_pre(gen, w, rec):
     gen.n_rows.fill_(len(rows))
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32_sharp", "mid_bf16", "mid_bf16_dh64", "mid_bf16_sharp"])
+@pytest.mark.parametrize("name", ["tiny_fp32_sharp", "mid_bf16", "mid_bf16_dh64", "mid_bf16_sharp", "mid_bf16_sched"])
 def test_teacher_forced_steps(name):
     """Every step starts from the oracle's pre-step state (caches included);
     exactness is required away from ambiguous positions."""
