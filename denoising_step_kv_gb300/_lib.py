@@ -26,7 +26,9 @@ class CacheCfg(ctypes.Structure):
         ("swd_tau", ctypes.c_float), ("swd_R", ctypes.c_int), ("block_len", ctypes.c_int),
         ("mask_id", ctypes.c_int), ("active_queries", ctypes.c_int), ("vocab", ctypes.c_int),
         ("max_pos", ctypes.c_int), ("ffn", ctypes.c_int), ("swd_R_min", ctypes.c_int),
-        ("steps_per_block", ctypes.c_int), ("full_every", ctypes.c_int), ("facache", ctypes.c_int),
+        ("steps_per_block", ctypes.c_int), ("full_every", ctypes.c_int), ("gate", ctypes.c_int),
+        ("conf_alpha", ctypes.c_float), ("conf_beta", ctypes.c_float), ("conf_lambda", ctypes.c_float),
+        ("conf_theta", ctypes.c_float), ("facache", ctypes.c_int),
     ]
 
 
@@ -51,7 +53,7 @@ _SIGS = {
     "attn_out": [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _VP],
     "ffn_gelu": [_VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _VP],
     "lmhead_conf": [_VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP],
-    "stab_update": [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP],
+    "stab_update": [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP],
     "dllm_profile_events": [_VP, _I, _VP, _VP],
     "lmhead_conf_noalloc": [_VP, _VP, _I, _I, _I, _I, _I, ctypes.c_float, _VP, _VP, _VP, _VP],
     "dllm_wait_selftest": [_VP, ctypes.c_uint64, _VP],
@@ -108,6 +110,9 @@ def make_cfg(w, vocab=None, facache=False):
     c.max_pos = w.stream_len if w.streaming else 0
     c.ffn = w.ffn
     c.swd_R_min, c.steps_per_block, c.full_every = w.swd_R_min, w.steps_per_block, w.full_every
+    c.gate = 1 if w.gate == "confidence" else 0
+    c.conf_alpha, c.conf_beta, c.conf_theta = w.conf_alpha, w.conf_beta, w.conf_theta
+    c.conf_lambda = 3.0 / w.steps_per_block if w.steps_per_block else 0.0
     return c
 
 
@@ -197,9 +202,9 @@ def lmhead_conf(c, h, w_lm, M, V, d, mask_id, argmax, p_top1, entropy, stream=No
                                             _p(entropy), _s(stream)))
 
 
-def stab_update(c, argmax, p_top1, tok, q_start, t, step_in_block, last_step, rows, n_rows, stream=None):
-    _check("stab_update", lib().stab_update(c, _p(argmax), _p(p_top1), _p(tok), q_start, t, step_in_block,
-                                            1 if last_step else 0, _p(rows), _p(n_rows), _s(stream)))
+def stab_update(c, argmax, p_top1, entropy, tok, q_start, t, step_in_block, last_step, rows, n_rows, stream=None):
+    _check("stab_update", lib().stab_update(c, _p(argmax), _p(p_top1), _p(entropy), _p(tok), q_start, t,
+                                            step_in_block, 1 if last_step else 0, _p(rows), _p(n_rows), _s(stream)))
 
 
 def dllm_profile_events(c, kernel, ev_begin, ev_end):

@@ -60,7 +60,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 void free_all(dllm_cache* c) {
   void* bufs[] = {c->q, c->k, c->v, c->version, c->tok_w, c->stable, c->hist_tok, c->hist_p, c->hist_n, c->words,
                   c->rope, c->err, c->ticket, c->X, c->rs, c->lm_part, c->lm_rs, c->ffn_buf,
-                  c->fa_state, c->fa_key, c->fa_rebuilt, c->sk_acc, c->sk_tickets};
+                  c->fa_state, c->fa_key, c->fa_rebuilt};
   for (void* b : bufs)
     if (b) cudaFree(b);
 }
@@ -111,6 +111,7 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
       return fail(DLLM_EINVAL, "dllm_cache_init: need 1 <= block_len <= min(64, seq_len)");
     if (g.swd_K < 1 || g.swd_K > 8 || g.swd_R < 0)
       return fail(DLLM_EINVAL, "dllm_cache_init: need 1 <= swd_K <= 8 and swd_R >= 0");
+    if (g.gate != 0 && g.gate != 1) return fail(DLLM_EINVAL, "dllm_cache_init: gate must be 0 or 1");
     if (g.swd_R_min > g.swd_R || g.full_every < 0 || (g.swd_R_min >= 0 && g.steps_per_block < 1))
       return fail(DLLM_EINVAL, "dllm_cache_init: need swd_R_min <= swd_R, full_every >= 0 and, with a radius "
                                "schedule, steps_per_block >= 1");
@@ -168,14 +169,6 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
             dalloc(&c->lm_part, static_cast<size_t>(c->lm_rows_cap) * c->lm_tiles_cap * 16) &&
             dalloc(&c->lm_rs, static_cast<size_t>(c->lm_rows_cap) * sizeof(float)) &&
             dalloc(&c->ffn_buf, sr * static_cast<size_t>(g.ffn) * c->elem);
-  if (ok && g.dtype == DLLM_BF16) {   // stream-K accumulators: the widest projection (q k v, W_o, FFN)
-    c->sk_max_n = std::max(3 * d, std::max(d, g.ffn));
-    const size_t tiles = static_cast<size_t>(cdiv(c->sk_max_n, 128));
-    ok = dalloc(&c->sk_acc, tiles * 512 * 128 * sizeof(float)) && dalloc(&c->sk_tickets, tiles * sizeof(unsigned));
-    if (ok)
-      ok = cudaMemset(c->sk_acc, 0, tiles * 512 * 128 * sizeof(float)) == cudaSuccess &&
-           cudaMemset(c->sk_tickets, 0, tiles * sizeof(unsigned)) == cudaSuccess;
-  }
   if (ok && g.facache) {
     const size_t bh = static_cast<size_t>(g.batch) * g.n_heads;
     ok = dalloc(&c->fa_state, bh * 64 * (g.head_dim + 4) * sizeof(float)) &&
@@ -458,9 +451,9 @@ dllm_status lmhead_conf(dllm_cache* c, const void* h_dev, const void* w_lm_dev, 
   return DLLM_OK;
 }
 
-dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p_top1_dev, int32_t* tok_dev,
-                        int q_start, int t, int step_in_block, int last_step, int32_t* rows_dev, int32_t* n_rows_dev,
-                        void* stream) {
+dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p_top1_dev, const float* entropy_dev,
+                        int32_t* tok_dev, int q_start, int t, int step_in_block, int last_step, int32_t* rows_dev,
+                        int32_t* n_rows_dev, void* stream) {
   DLLM_CHECK_HANDLE(c);
   const dllm_cache_cfg& g = c->cfg;
   if (g.sink > 0) return fail(DLLM_EINVAL, "stab_update: dense mode only");
@@ -469,14 +462,16 @@ dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p
   if (q_start < 0 || q_start + g.block_len > g.seq_len)
     return fail(DLLM_EINVAL, "stab_update: active block outside the sequence");
   if (step_in_block < 0) return fail(DLLM_EINVAL, "stab_update: step_in_block < 0");
+  if (g.gate == 1 && !entropy_dev) return fail(DLLM_EINVAL, "stab_update: the confidence criterion needs entropy");
   // the schedules of the next step's refresh set
   const int s1 = step_in_block + 1;
   int R_next = g.swd_R;
   if (g.swd_R_min >= 0 && g.steps_per_block > 0)
     R_next = std::min(g.swd_R, g.swd_R_min + ((g.swd_R - g.swd_R_min + 1) * s1) / g.steps_per_block);
   const int full_next = (g.full_every > 0 && s1 % g.full_every == 0) ? 1 : 0;
-  DLLM_LAUNCH(launch_stab(c, argmax_dev, p_top1_dev, tok_dev, q_start, t, last_step ? 1 : 0, R_next, full_next,
-                          rows_dev, n_rows_dev, static_cast<cudaStream_t>(stream)),
+  DLLM_LAUNCH(launch_stab(c, argmax_dev, p_top1_dev, g.gate == 1 ? entropy_dev : nullptr, tok_dev, q_start, t,
+                          last_step ? 1 : 0, g.gate == 1 ? 0 : R_next, full_next, rows_dev, n_rows_dev,
+                          static_cast<cudaStream_t>(stream)),
               "stab_update");
   return DLLM_OK;
 }

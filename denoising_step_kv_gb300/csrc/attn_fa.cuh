@@ -33,8 +33,11 @@ namespace attn_fa {
 
 using attn_tc::KT;
 using attn_tc::LAZY;
-using attn_tc::NSLOT;
 using attn_tc::QROWS;
+// Two ring slots (K and V of two tiles) keep the CTA under 100 KB of shared
+// memory, so two CTAs share an SM: the window-only pass of every (sequence,
+// head) fits one wave, and a rebuild streams two CTAs' tiles per SM.
+constexpr int NSLOT = 2;
 
 constexpr int MAXQ = 64;                  // queries per (sequence, head) the state holds
 constexpr int KEY_INTS = 2 + MAXQ;        // q0, q_len, token-at-write of each query row
@@ -49,12 +52,15 @@ struct Shape {
   static constexpr int OFF_RING = OFF_Q + Q_BYTES;
   static constexpr int OFF_BAR = OFF_RING + NSLOT * 2 * KV_TILE;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
-  // TMEM: S/P double buffer, then O~ of the unchanged tiles, then O~ of the window
-  static constexpr uint32_t S_COL = 0, OU_COL = 2 * KT, OW_COL = 2 * KT + DH;
-  static constexpr uint32_t TMEM_COLS = (OW_COL + DH <= 256) ? 256 : 512;
+  // TMEM: S/P double buffer, O~ of the window, then O~ of the unchanged
+  // tiles (allocated only when the state is rebuilt)
+  static constexpr uint32_t S_COL = 0, OW_COL = 2 * KT, OU_COL = 2 * KT + DH;
+  static constexpr uint32_t COLS_W = (OW_COL + DH <= 256) ? 256 : 512;
+  static constexpr uint32_t COLS_UW = (OU_COL + DH <= 256) ? 256 : 512;
   static constexpr int PLD = DH + 4;      // padded fp32 row of a partial
-  // epilogue: two partial rows per MMA row, (m, l) pairs, merge weights
-  static_assert(2 * QROWS * PLD * 4 + 2 * QROWS * 8 + QROWS * 8 * 4 <= NSLOT * 2 * KV_TILE, "tail fits in the ring");
+  // epilogue, one class at a time over the drained Q and ring: partial rows,
+  // (m, l) pairs, merge weights
+  static_assert(QROWS * PLD * 4 + QROWS * 8 + QROWS * 8 * 4 <= OFF_BAR, "tail fits in Q and the ring");
 };
 
 // Stored state row of (sequence, head, query): O~[DH], m (log2 domain), l.
@@ -66,7 +72,7 @@ __host__ __device__ constexpr int state_ld(int dh) { return dh + 4; }
 // cache's token-at-write [B * L].  state: [B][H][MAXQ][DH + 4] fp32; key:
 // [B][H][KEY_INTS] int32.  out [B][q_len][ld] bf16.
 template <int DH, int R>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)
     attn_fa_kernel(const uint8_t* __restrict__ Ql, const uint8_t* __restrict__ Kl, const uint8_t* __restrict__ Vl,
                    KvLayout kv, int ld, int q_pos0, int q_len, int kv_len, int w_lo, int w_hi, float scale_log2,
                    const int* __restrict__ tok_w, int L, float* __restrict__ state, int* __restrict__ key,
@@ -101,11 +107,7 @@ __global__ void __launch_bounds__(192, 1)
     bars->abort = 0;
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(&bars->tmem, S::TMEM_COLS);
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem;
   // the window tiles are read in every case: warm L2 with the first two
   if (warp >= 2 && lane == 0) {
     const int j = (warp - 2) >> 1;
@@ -121,6 +123,12 @@ __global__ void __launch_bounds__(192, 1)
   if (tid >= 64 && tid - 64 < q_len) same = mykey[2 + tid - 64] == tok_w[static_cast<size_t>(b) * L + q_pos0 + tid - 64];
   const bool valid = __syncthreads_and(same) != 0;
   const int n_u = valid ? 0 : n_all - n_win;       // unchanged tiles streamed this time
+  const uint32_t tmem_cols = n_u > 0 ? S::COLS_UW : S::COLS_W;
+  if (warp == 1) tmem_alloc(&bars->tmem, tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
   const int n_tiles = n_u + n_win;
   // virtual tile j -> physical 64-key tile
   auto phys = [&](int j) { return j < n_u ? (j < w_lo ? j : j + n_win) : w_lo + (j - n_u); };
@@ -329,68 +337,60 @@ __global__ void __launch_bounds__(192, 1)
       okv = __shfl_sync(0xffffffffu, okv, 0);
       if (!okv) break;
     }
-    if (n_u > 0 && n_win == 0) {      // no window tiles (cannot happen with q_len >= 1): U only
-      m_u = m_ref;
-      l_u = l_sum;
-      m_ref = -INFINITY;
-      l_sum = 0.f;
-    }
   }
 
-  // ---- partials of both classes into the drained ring
+  // ---- the partials, one class at a time, over the drained Q and ring:
+  //   po[m][PLD] fp32 O~ row of MMA row m = g * QP + r, pml[m] = (m, l);
+  // the unchanged tiles' class (rebuilt) goes to the kept state in global
+  // memory, then the window's class stays in po for the merge
   tc_fence_before();
   __syncthreads();
-  float* po_u = reinterpret_cast<float*>(sm + S::OFF_RING);
-  float* po_w = po_u + QROWS * S::PLD;
-  float* pml_u = po_w + QROWS * S::PLD;                    // [QROWS][2]
-  float* pml_w = pml_u + QROWS * 2;
-  float* wts = pml_w + QROWS * 2;                          // [QROWS][8]
-  if (warp >= 2) {
-    const int wq = warp & 3;
-    const int m = wq * 32 + lane, r = m % QP;
-    if (n_tiles > 0) {
-      int ok = 1;
-      if (lane == 0)
-        ok = mbar_wait(&bars->empty[(n_tiles - 1) % NSLOT], ((n_tiles - 1) / NSLOT) & 1u, abort, err) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      tc_fence_after();
-      const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-#pragma unroll 1
-      for (int cls = 0; cls < 2; ++cls) {
-        if (cls == 0 && n_u == 0) continue;
-        float* po = cls == 0 ? po_u : po_w;
-        const uint32_t o_col = cls == 0 ? S::OU_COL : S::OW_COL;
-#pragma unroll 1
-        for (int c = 0; c < DH / 32; ++c) {
-          float o[32];
-          tmem_ld32(tmem + lane_off + o_col + c * 32, o);
-          if (r < q_len) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<float4*>(po + m * S::PLD + c * 32 + i) =
-                  ok ? make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-      }
-    }
-    if (r < q_len) {
-      pml_u[m * 2] = n_u > 0 ? m_u : -INFINITY;
-      pml_u[m * 2 + 1] = l_u;
-      pml_w[m * 2] = n_win > 0 ? m_ref : -INFINITY;
-      pml_w[m * 2 + 1] = l_sum;
-      if (n_u == 0) {
-#pragma unroll 4
-        for (int c = 0; c < DH; c += 4) *reinterpret_cast<float4*>(po_u + m * S::PLD + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
+  float* po = reinterpret_cast<float*>(sm + S::OFF_Q);
+  float* pml = po + QROWS * S::PLD;                        // [QROWS][2]
+  float* wts = pml + QROWS * 2;                            // [QROWS][8]
+  float* my_state = state + static_cast<size_t>(b * H + h) * MAXQ * state_ld(DH);
+  int last_ok = 1;
+  if (warp >= 2 && n_tiles > 0) {
+    if (lane == 0)
+      last_ok = mbar_wait(&bars->empty[(n_tiles - 1) % NSLOT], ((n_tiles - 1) / NSLOT) & 1u, abort, err) ? 1 : 0;
+    last_ok = __shfl_sync(0xffffffffu, last_ok, 0);
+    tc_fence_after();
   }
-  __syncthreads();
-  // replicas of a query, per class: weight each by 2^(m_g - M) and sum into
-  // replica 0's row (which then holds M, sum w l, sum w O~)
 #pragma unroll 1
   for (int cls = 0; cls < 2; ++cls) {
-    float* po = cls == 0 ? po_u : po_w;
-    float* pml = cls == 0 ? pml_u : pml_w;
+    if (cls == 0 && valid) continue;                       // the kept state stays
+    // a rebuild with no unchanged tile (every tile in the window) stores the
+    // empty state: m = -inf, l = 0, O~ = 0 (no TMEM columns were allocated)
+    const bool from_tmem = cls == 1 || n_u > 0;
+    if (warp >= 2) {
+      const int wq = warp & 3;
+      const int m = wq * 32 + lane, r = m % QP;
+      const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+      const uint32_t o_col = cls == 0 ? S::OU_COL : S::OW_COL;
+#pragma unroll 1
+      for (int c = 0; c < DH / 32; ++c) {
+        float o[32];
+        if (from_tmem) {
+          tmem_ld32(tmem + lane_off + o_col + c * 32, o);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0.f;
+        }
+        if (r < q_len) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(po + m * S::PLD + c * 32 + i) =
+                last_ok ? make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      if (r < q_len) {
+        pml[m * 2] = cls == 0 ? (n_u > 0 ? m_u : -INFINITY) : (n_win > 0 ? m_ref : -INFINITY);
+        pml[m * 2 + 1] = cls == 0 ? (n_u > 0 ? l_u : 0.f) : l_sum;
+      }
+    }
+    __syncthreads();
+    // replicas of a query: weight each by 2^(m_g - M), sum into replica 0's
+    // row, which then holds M, sum w l, sum w O~
     if constexpr (R > 1) {
       for (int r = tid; r < q_len; r += 192) {
         float M = -INFINITY;
@@ -427,36 +427,26 @@ __global__ void __launch_bounds__(192, 1)
       }
       __syncthreads();
     }
-  }
-  // the unchanged tiles' state: store it (rebuilt) or load the kept one
-  float* my_state = state + static_cast<size_t>(b * H + h) * MAXQ * state_ld(DH);
-  if (!valid) {
-    for (int e = tid; e < q_len * (DH / 4); e += 192) {
-      const int r = e / (DH / 4), c = (e % (DH / 4)) * 4;
-      *reinterpret_cast<float4*>(my_state + r * state_ld(DH) + c) = *reinterpret_cast<const float4*>(po_u + r * S::PLD + c);
-    }
-    for (int r = tid; r < q_len; r += 192) {
-      my_state[r * state_ld(DH) + DH] = pml_u[r * 2];
-      my_state[r * state_ld(DH) + DH + 1] = pml_u[r * 2 + 1];
-    }
-  } else {
-    for (int e = tid; e < q_len * (DH / 4); e += 192) {
-      const int r = e / (DH / 4), c = (e % (DH / 4)) * 4;
-      *reinterpret_cast<float4*>(po_u + r * S::PLD + c) = *reinterpret_cast<const float4*>(my_state + r * state_ld(DH) + c);
-    }
-    for (int r = tid; r < q_len; r += 192) {
-      pml_u[r * 2] = my_state[r * state_ld(DH) + DH];
-      pml_u[r * 2 + 1] = my_state[r * state_ld(DH) + DH + 1];
+    if (cls == 0) {   // store the rebuilt state of the unchanged tiles
+      for (int e = tid; e < q_len * (DH / 4); e += 192) {
+        const int r = e / (DH / 4), c = (e % (DH / 4)) * 4;
+        *reinterpret_cast<float4*>(my_state + r * state_ld(DH) + c) =
+            *reinterpret_cast<const float4*>(po + r * S::PLD + c);
+      }
+      for (int r = tid; r < q_len; r += 192) {
+        my_state[r * state_ld(DH) + DH] = pml[r * 2];
+        my_state[r * state_ld(DH) + DH + 1] = pml[r * 2 + 1];
+      }
+      __syncthreads();      // the state is written before the merge reads it back
     }
   }
-  __syncthreads();
-  // O = (w_U O~_U + w_W O~_W) / (w_U l_U + w_W l_W)
+  // O = (w_U O~_U + w_W O~_W) / (w_U l_U + w_W l_W), O~_U from the kept state
   for (int r = tid; r < q_len; r += 192) {
-    const float mu = pml_u[r * 2], mw = pml_w[r * 2];
+    const float mu = my_state[r * state_ld(DH) + DH], mw = pml[r * 2];
     const float M = fmaxf(mu, mw);
     const float wu = mu == -INFINITY ? 0.f : exp2f(mu - M);
     const float ww = mw == -INFINITY ? 0.f : exp2f(mw - M);
-    const float inv = 1.f / (wu * pml_u[r * 2 + 1] + ww * pml_w[r * 2 + 1]);
+    const float inv = 1.f / (wu * my_state[r * state_ld(DH) + DH + 1] + ww * pml[r * 2 + 1]);
     wts[r * 8] = wu * inv;
     wts[r * 8 + 1] = ww * inv;
   }
@@ -464,8 +454,8 @@ __global__ void __launch_bounds__(192, 1)
   for (int e = tid; e < q_len * (DH / 4); e += 192) {
     const int r = e / (DH / 4), c = (e % (DH / 4)) * 4;
     const float wu = wts[r * 8], ww = wts[r * 8 + 1];
-    const float4 u = *reinterpret_cast<const float4*>(po_u + r * S::PLD + c);
-    const float4 v = *reinterpret_cast<const float4*>(po_w + r * S::PLD + c);
+    const float4 u = *reinterpret_cast<const float4*>(my_state + r * state_ld(DH) + c);
+    const float4 v = *reinterpret_cast<const float4*>(po + r * S::PLD + c);
     bf16* op = out + static_cast<size_t>(b * q_len + r) * ld + h * DH + c;
     *reinterpret_cast<__nv_bfloat162*>(op) = __floats2bfloat162_rn(fmaf(wu, u.x, ww * v.x), fmaf(wu, u.y, ww * v.y));
     *reinterpret_cast<__nv_bfloat162*>(op + 2) = __floats2bfloat162_rn(fmaf(wu, u.z, ww * v.z), fmaf(wu, u.w, ww * v.w));
@@ -482,7 +472,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, S::TMEM_COLS);
+    tmem_dealloc(tmem, tmem_cols);
   }
 }
 

@@ -239,16 +239,6 @@ __device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap
       : "memory");
 }
 
-// Order this thread's generic shared-memory writes before later async-proxy
-// (bulk copy) reads of them, and completed async-proxy global writes before
-// later generic accesses.
-__device__ __forceinline__ void fence_async_smem_cta() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void fence_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 // Bring [p, p + bytes) into L2 (one prefetch per 128-byte line).
 __device__ __forceinline__ void prefetch_l2(const void* p, int bytes) {
   const char* c = static_cast<const char*>(p);

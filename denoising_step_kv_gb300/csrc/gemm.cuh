@@ -706,246 +706,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// Weight-streaming GEMM for M <= 512 rows, stream-K over (tile, k-block)
-// units: D^T = B . A^T with the weights B [N][K] as the MMA's A operand (a
-// 128-column tile on the TMEM lanes) and the rows A [M][K] as its B operand
-// (M rounded up to 16 on the TMEM columns, two MMAs when M > 256).  The
-// n_tiles * nK units are cut into gridDim.x contiguous ranges, one per CTA
-// (one CTA per SM), so every SM streams the same number of weight bytes
-// whatever N and K are.  A range covers pieces ("segments") of one or two
-// tiles.  A segment's fp32 partial goes from TMEM through shared memory into
-// the tile's global accumulator acc[tile][M][128] by bulk reduce-adds
-// (performed at L2); the CTA that finishes a tile's last segment (an
-// arrival ticket per tile) reads the sum, zeroes it for the next launch, and
-// runs the epilogue on it.  Two TMEM accumulators (M <= 256) let a segment's
-// reduce overlap the next segment's MMAs.  The sum over segments is in
-// arrival order, so the last bits of a result may differ between launches.
-constexpr int SK_MAX_ROWS = 512;
-constexpr int SK_CHUNK = 32;                               // rows per epilogue chunk
-constexpr int SK_CHUNK_BYTES = SK_CHUNK * 128 * 4;         // 16 KB of fp32
-constexpr int SK_RING = 168 * 1024;
-constexpr int SK_MAX_ST = 8;
-constexpr int SK_TLD = 129;                                // padded row of the fixup's sum
-struct SkBars {
-  uint64_t full[SK_MAX_ST];
-  uint64_t empty[SK_MAX_ST];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
-  uint32_t tmem;
-  int abort;
-  int last;
-  int seg_ok;
-};
-constexpr size_t SK_SMEM = 1024 + SK_RING + 2 * SK_CHUNK_BYTES + sizeof(SkBars);
-static_assert(SK_CHUNK * SK_TLD * 4 <= 2 * SK_CHUNK_BYTES, "fixup chunk fits in the chunk buffers");
-
-// CTA g of G owns units [U g / G, U (g + 1) / G); the owner of unit u:
-__host__ __device__ __forceinline__ int sk_owner(long long u, int G, long long U) {
-  return static_cast<int>(((u + 1) * G + U - 1) / U) - 1;
-}
-
-__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
-                   reinterpret_cast<uint64_t>(dst)),
-               "r"(smem_u32(src)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-template <class Epi>
-__global__ void __launch_bounds__(THREADS, 1)
-    gemm_streamk_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                        int M_host, const int* __restrict__ M_dev, int M_cap, int N, int K, Epi epi,
-                        float* __restrict__ acc, unsigned* __restrict__ tickets, unsigned* err) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  float* chunk = reinterpret_cast<float*>(smem + SK_RING);          // 2 x [32][128] fp32
-  SkBars* bars = reinterpret_cast<SkBars*>(smem + SK_RING + 2 * SK_CHUNK_BYTES);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < SK_MAX_ST; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&bars->tfull[a], 1);
-      mbar_init(&bars->tempty[a], 4);
-    }
-    bars->abort = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) tmem_alloc(&bars->tmem, 512);
-  if (threadIdx.x == 32) {
-    prefetch_tmap(&tmW);
-    prefetch_tmap(&tmX);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem;
-  volatile int* abort = &bars->abort;
-  pdl_launch();
-  pdl_wait();
-  const int M = M_dev ? min(*M_dev, M_cap) : M_host;
-  const int G = gridDim.x, g = blockIdx.x;
-  const int n_tiles = (N + 127) / 128, nK = (K + BK - 1) / BK;
-  const long long U = static_cast<long long>(n_tiles) * nK;
-  const long long u0 = U * g / G, u1 = U * (g + 1) / G;
-  const bool run = M > 0 && M <= SK_MAX_ROWS && u1 > u0;
-  const int xrows = (M + SKN_XBOX - 1) / SKN_XBOX * SKN_XBOX;
-  const int nx = xrows / SKN_XBOX;
-  const int n_mma = (M + 15) / 16 * 16;
-  const int stage_bytes = SKN_W_BYTES + xrows * 128;
-  const int n_st = run ? min(SK_MAX_ST, SK_RING / stage_bytes) : 1;
-  const int n_acc = n_mma <= 256 ? 2 : 1;                         // TMEM accumulators of 256 / 512 columns
-
-  if (run && warp == 0) {
-    if (lane == 0) {
-      uint32_t issued = 0, par = 0;
-      int i = 0;
-      for (long long u = u0; u < u1; ++u, ++i) {
-        const int tile = static_cast<int>(u / nK), kb = static_cast<int>(u % nK);
-        const int stage = i % n_st;
-        const uint32_t phase = (i / n_st) & 1u;
-        if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort, err)) break;
-        uint8_t* st = smem + stage * stage_bytes;
-        mbar_expect_tx(&bars->full[stage], stage_bytes);
-        tma_load_2d(st, &tmW, kb * BK, tile * 128, &bars->full[stage]);
-        for (int j = 0; j < nx; ++j)
-          tma_load_2d(st + SKN_W_BYTES + j * SKN_XBOX * 128, &tmX, kb * BK, j * SKN_XBOX, &bars->full[stage]);
-        issued |= 1u << stage;
-        par = (par & ~(1u << stage)) | (phase << stage);
-      }
-      if (*abort)
-        for (int s = 0; s < n_st; ++s)
-          if (issued & (1u << s)) mbar_wait(&bars->full[s], (par >> s) & 1u, nullptr, err);
-    }
-  } else if (run && warp == 1) {
-    if (lane == 0) {
-      int i = 0, seg = 0;
-      bool ok = true;
-      for (long long u = u0; ok && u < u1; ++seg) {
-        const int tile = static_cast<int>(u / nK);
-        const long long seg_end = min(u1, static_cast<long long>(tile + 1) * nK);
-        const int a = seg % n_acc;
-        // the epilogue has drained this accumulator's previous segment
-        if (seg >= n_acc && !mbar_wait(&bars->tempty[a], ((seg / n_acc) - 1) & 1u, abort, err)) break;
-        tc_fence_after();
-        const uint32_t d0 = tmem + static_cast<uint32_t>(a * 256);
-        for (bool first = true; u < seg_end; ++u, ++i, first = false) {
-          const int stage = i % n_st;
-          const uint32_t phase = (i / n_st) & 1u;
-          if (!mbar_wait(&bars->full[stage], phase, abort, err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t w0 = smem_u32(smem + stage * stage_bytes), x0 = w0 + SKN_W_BYTES;
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint32_t accum = (first && k == 0) ? 0u : 1u;
-            const int n1 = min(n_mma, 256);
-            tc_mma_bf16(d0, sdesc_sw128(w0 + k * 32), sdesc_sw128(x0 + k * 32), idesc_bf16(128, n1), accum);
-            if (n_mma > 256)
-              tc_mma_bf16(d0 + 256, sdesc_sw128(w0 + k * 32), sdesc_sw128(x0 + 256 * 128 + k * 32),
-                          idesc_bf16(128, n_mma - 256), accum);
-          }
-          tc_commit(&bars->empty[stage]);
-        }
-        tc_commit(&bars->tfull[a]);       // this segment's MMAs are done
-      }
-    }
-  } else if (run) {
-    // epilogue warps: thread = TMEM lane = output column f of the tile
-    const int q = warp & 3, f = q * 32 + lane;
-    const bool issuer = threadIdx.x == 64;
-    int seg = 0;
-    for (long long u = u0; u < u1; ++seg) {
-      const int tile = static_cast<int>(u / nK);
-      const long long t_begin = static_cast<long long>(tile) * nK, t_end = t_begin + nK;
-      const long long seg_end = min(u1, t_end);
-      u = seg_end;
-      const int a = seg % n_acc;
-      // one thread waits for the segment's MMAs; the four warps then go on
-      // (or leave) together, so that no named barrier below misses a warp
-      if (issuer) bars->seg_ok = mbar_wait(&bars->tfull[a], (seg / n_acc) & 1u, abort, err) ? 1 : 0;
-      epi_bar();
-      if (!bars->seg_ok) break;
-      tc_fence_after();
-      float* acc_t = acc + static_cast<size_t>(tile) * SK_MAX_ROWS * 128;
-      const int n_chunks = (M + SK_CHUNK - 1) / SK_CHUNK;
-      for (int c = 0; c < n_chunks; ++c) {
-        float* buf = chunk + (c & 1) * (SK_CHUNK * 128);
-        float v[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * 256 + c * 32), v);
-        // the bulk reduce that read this buffer two chunks ago has finished reading
-        if (issuer && c >= 2) bulk_wait_read_le1();
-        epi_bar();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) buf[j * 128 + f] = v[j];
-        fence_async_smem_cta();
-        epi_bar();
-        if (issuer) {
-          const int rows = min(SK_CHUNK, M - c * SK_CHUNK);
-          bulk_reduce_add_f32(acc_t + static_cast<size_t>(c) * SK_CHUNK * 128, buf, rows * 512u);
-          bulk_commit();
-        }
-      }
-      // TMEM is read out: the MMAs may reuse this accumulator
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tempty[a]);
-      // every reduce of this segment is complete and visible, then the ticket
-      if (issuer) {
-        bulk_wait_all();
-        fence_async_global();
-        __threadfence();
-        const int g_first = sk_owner(t_begin, G, U), g_last = sk_owner(t_end - 1, G, U);
-        const unsigned prev = atomicAdd(&tickets[tile], 1u);
-        bars->last = prev == static_cast<unsigned>(g_last - g_first);
-      }
-      epi_bar();
-      if (!bars->last) continue;
-      // the last segment of the tile: read the sum, zero it, run the epilogue
-      __threadfence();
-      float* tsum = chunk;                                    // [32][SK_TLD] padded
-      const int n0 = tile * 128;
-      for (int c = 0; c < n_chunks; ++c) {
-        const int rows = min(SK_CHUNK, M - c * SK_CHUNK);
-        float* src = acc_t + static_cast<size_t>(c) * SK_CHUNK * 128;
-        for (int e = threadIdx.x - 64; e < rows * 128; e += 128) {
-          tsum[(e >> 7) * SK_TLD + (e & 127)] = __ldcg(src + e);
-          src[e] = 0.f;
-        }
-        epi_bar();
-        for (int it = threadIdx.x - 64; it < rows * Epi::PARTS; it += 128) {
-          const int rr = it % rows, piece = it / rows;
-          const float* row = tsum + rr * SK_TLD;
-          auto ldr = [row](int col, float (&vv)[32]) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) vv[j] = row[col + j];
-          };
-          epi.run_part(c * SK_CHUNK + rr, n0, piece, M, N, ldr);
-        }
-        epi_bar();
-      }
-      if (threadIdx.x == 64) tickets[tile] = 0u;
-    }
-    if (issuer) bulk_wait_all();     // no bulk copy may still read this CTA's shared memory
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
 }  // namespace tc
 
 namespace simt {

@@ -78,28 +78,6 @@ cudaError_t launch_skinny(dllm_cache* c, const void* A, int a_rows, int M_host, 
                    tx, M_host, M_dev, a_rows, N, K, epi, c->err);
 }
 
-template <class Epi>
-cudaError_t launch_streamk(dllm_cache* c, const void* A, int a_rows, int M_host, const int* M_dev, const void* W,
-                           int N, int K, const Epi& epi, cudaStream_t st) {
-  static PerDeviceOnce attr;
-  {
-    const cudaError_t e = set_smem_once(attr, tc::gemm_streamk_kernel<Epi>, tc::SK_SMEM);
-    if (e != cudaSuccess) return e;
-  }
-  CUtensorMap tw, tx;
-  if (!make_tmap_2d(&tw, W, K, N, static_cast<uint64_t>(K) * 2, tc::BK, 128, true) ||
-      !make_tmap_2d(&tx, A, K, a_rows, static_cast<uint64_t>(K) * 2, tc::BK, tc::SKN_XBOX, true))
-    return cudaErrorInvalidValue;
-  const long long units = static_cast<long long>(cdiv(N, 128)) * cdiv(K, tc::BK);
-  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(c->num_sms, units)));
-  return launch_ex(tc::gemm_streamk_kernel<Epi>, dim3(grid), dim3(tc::THREADS), tc::SK_SMEM, st, 0, tw, tx, M_host,
-                   M_dev, a_rows, N, K, epi, c->sk_acc, c->sk_tickets, c->err);
-}
-
-// Epilogues that run on the stream-K kernel (the LM head keeps its own kernels).
-template <class Epi> struct StreamKOk { static constexpr bool value = true; };
-template <> struct StreamKOk<EpiLM> { static constexpr bool value = false; };
-
 // Clusters of the weight-streaming kernel (split s) that fit on the GPU at
 // once: clusters must sit inside one GPC, so this can be below num_sms / s.
 template <class Epi, int S>
@@ -169,23 +147,6 @@ template <class Epi>
 cudaError_t run_tc(dllm_cache* c, const void* A, int a_rows, int M_host, const int* M_dev, const void* B, int N,
                    int K, const Epi& epi, cudaStream_t st, bool wide_ok = true) {
   if (!M_dev && M_host <= 0) return cudaSuccess;
-  if (StreamKOk<Epi>::value && c->sk_acc && N <= c->sk_max_n) {
-    // up to SK_MAX_ROWS rows: stream-K weight streaming; beyond: the large-M kernels
-    const int m_rows = M_dev ? a_rows : M_host;
-    cudaError_t e = cudaSuccess;
-    if (M_dev || M_host <= tc::SK_MAX_ROWS) {
-      e = launch_streamk(c, A, a_rows, M_host, M_dev, B, N, K, epi, st);
-      if (e != cudaSuccess || m_rows <= tc::SK_MAX_ROWS) return e;
-    }
-    CUtensorMap ta, tb;
-    if (!make_tmap_2d(&ta, A, K, a_rows, static_cast<uint64_t>(K) * 2, tc::BK, tc::BM, true) ||
-        !make_tmap_2d(&tb, B, K, N, static_cast<uint64_t>(K) * 2, tc::BK, tc::BN, true))
-      return cudaErrorInvalidValue;
-    const int M_min = tc::SK_MAX_ROWS + 1;
-    if (wide_ok && N % tc::PBN == 0)
-      return launch_pair<Epi, 4>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
-    return launch_persistent<Epi, 4>(c, ta, tb, a_rows, M_host, M_dev, M_min, N, K, epi, st);
-  }
   const int split = skinny_split<Epi>(c, N);
   const int m_rows = M_dev ? a_rows : M_host;     // most rows this call can see
   cudaError_t e = cudaSuccess;

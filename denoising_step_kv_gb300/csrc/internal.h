@@ -48,11 +48,6 @@ struct dllm_cache {
   float* fa_state = nullptr;  // [B][H][64][head_dim + 4]: O~, m (log2 domain), l
   int* fa_key = nullptr;      // [B][H][66]: block start, block length, token-at-write of the queries
   int* fa_rebuilt = nullptr;  // (sequence, head) states rebuilt since the last reset
-  // stream-K weight-streaming GEMM: per 128-column tile an fp32 accumulator
-  // [512][128] (kept zero between launches) and an arrival ticket
-  float* sk_acc = nullptr;
-  unsigned* sk_tickets = nullptr;
-  int sk_max_n = 0;           // widest N (output columns) the accumulators cover
   // measurement hook: events bracketing a kernel (index = dllm_prof_kernel)
   cudaEvent_t prof_begin[8] = {};
   cudaEvent_t prof_end[8] = {};
@@ -162,8 +157,9 @@ cudaError_t launch_lm_merge(const void* part, int M, int n_tiles, int* argmax, f
                             const unsigned* fail_word, cudaStream_t st);
 // R: dilation radius of the next step's refresh set; full: the next step
 // refreshes every row (the schedules of stab_update)
-cudaError_t launch_stab(dllm_cache* c, const int* argmax, const float* p1, int* tok, int q_start, int t,
-                        int last, int R, int full, int* rows, int* n_rows, cudaStream_t st);
+// ent: the active rows' entropies with the confidence criterion, else null
+cudaError_t launch_stab(dllm_cache* c, const int* argmax, const float* p1, const float* ent, int* tok, int q_start,
+                        int t, int last, int R, int full, int* rows, int* n_rows, cudaStream_t st);
 cudaError_t launch_refresh_all(dllm_cache* c, int q_start, int* rows, int* n_rows, cudaStream_t st);
 cudaError_t launch_reset(dllm_cache* c, cudaStream_t st);
 cudaError_t launch_wait_selftest(dllm_cache* c, uint64_t limit_ns, cudaStream_t st);

@@ -1,6 +1,7 @@
 // Row gather + RMS scale, LM-head tile merge, the Stable-Window-Decoding
 // update with refresh-set construction, and state reset.
 #include <algorithm>
+#include <cmath>
 
 #include "common.cuh"
 #include "epilogue.cuh"
@@ -181,8 +182,16 @@ __device__ void compact_words(const uint32_t* __restrict__ words, int nw, int L,
 
 // Stable-Window-Decoding update of the active block of sequence blockIdx.x,
 // then one flag bit per position for the next step's refresh set.
+//
+// ent (may be null): the confidence criterion - an unstable active row joins
+// the next refresh set when alpha (1 - ent / H_max) + beta exp(-lambda age)
+// < theta (R is then 0); else every unstable active row is dilated by R.
+struct ConfGate {
+  float alpha, beta, lambda, theta, h_max;
+};
 __global__ void __launch_bounds__(1024, 1) swd_kernel(
-    const int* __restrict__ argmax, const float* __restrict__ p1, int* __restrict__ tok,
+    const int* __restrict__ argmax, const float* __restrict__ p1, const float* __restrict__ ent, ConfGate cg,
+    int* __restrict__ tok,
     uint8_t* __restrict__ stable, int* __restrict__ hist_tok, float* __restrict__ hist_p, int* __restrict__ hist_n,
     const int* __restrict__ tok_w, const int* __restrict__ version, uint32_t* __restrict__ words, int L, int Lw,
     int seq_rows, int n_layers, int blk, int K, float tau, int R, int q0, int t, int last, int full, int expiry,
@@ -254,7 +263,13 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
       if (!st) tok[r] = a;
       hist_n[h] = 0;
     }
-    s_unst[j] = st ? 0 : 1;
+    bool flag = !st;
+    if (ent && flag) {   // cache confidence at step t + 1 of this row's layer-0 entry
+      const float age = static_cast<float>(t + 1 - version[r]);
+      const float conf = cg.alpha * (1.f - ent[h] / cg.h_max) + cg.beta * expf(-(cg.lambda * age));
+      flag = conf < cg.theta;
+    }
+    s_unst[j] = flag ? 1 : 0;
   }
   __syncthreads();
   for (int base = 0; base < L; base += blockDim.x) {
@@ -476,10 +491,12 @@ cudaError_t launch_lm_merge(const void* part, int M, int n_tiles, int* argmax, f
                    n_tiles, argmax, p1, ent, fail_word);
 }
 
-cudaError_t launch_stab(dllm_cache* c, const int* argmax, const float* p1, int* tok, int q_start, int t, int last,
-                        int R, int full, int* rows, int* n_rows, cudaStream_t st) {
+cudaError_t launch_stab(dllm_cache* c, const int* argmax, const float* p1, const float* ent, int* tok, int q_start,
+                        int t, int last, int R, int full, int* rows, int* n_rows, cudaStream_t st) {
   const dllm_cache_cfg& g = c->cfg;
-  return launch_ex(swd_kernel, dim3(g.batch), dim3(1024), 0, st, 0, argmax, p1, tok, c->stable, c->hist_tok, c->hist_p,
+  const ConfGate cg{g.conf_alpha, g.conf_beta, g.conf_lambda, g.conf_theta,
+                    static_cast<float>(std::log(static_cast<double>(g.vocab - 1)))};
+  return launch_ex(swd_kernel, dim3(g.batch), dim3(1024), 0, st, 0, argmax, p1, ent, cg, tok, c->stable, c->hist_tok, c->hist_p,
                    c->hist_n, c->tok_w, c->version, c->words, g.seq_len, c->Lw, c->seq_rows, g.n_layers, g.block_len,
                    g.swd_K, g.swd_tau, R, q_start, t, last, full, g.expiry, g.active_queries, c->ticket, rows,
                    n_rows);
@@ -494,10 +511,8 @@ cudaError_t launch_refresh_all(dllm_cache* c, int q_start, int* rows, int* n_row
 
 cudaError_t launch_reset(dllm_cache* c, cudaStream_t st) {
   const dllm_cache_cfg& g = c->cfg;
-  if (c->sk_acc) {   // stream-K accumulators and tickets (left dirty only by a wait that gave up)
-    const size_t tiles = static_cast<size_t>(cdiv(c->sk_max_n, 128));
-    cudaError_t e = cudaMemsetAsync(c->sk_acc, 0, tiles * 512 * 128 * sizeof(float), st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(c->sk_tickets, 0, tiles * sizeof(unsigned), st);
+  {  // until a refresh set is built, every row may write its K/V (the gate of active queries)
+    cudaError_t e = cudaMemsetAsync(c->words, 0xff, static_cast<size_t>(g.batch) * c->Lw * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
   }
   if (c->fa_key) {   // no kept attention state is valid (block start -1 never matches)

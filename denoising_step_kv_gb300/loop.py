@@ -80,7 +80,7 @@ class DenseGenerator:
         K.attn_out(c, self.o, W["w_o"][0], None, self.tok, W["embed"], q0, blk, None, self.h, stream)
         K.lmhead_conf(c, self.h, W["w_lm"], w.batch * blk, w.vocab, w.d_model, w.mask_id, self.argmax,
                       self.p1, self.ent, stream)
-        K.stab_update(c, self.argmax, self.p1, self.tok, q0, t, s, s == w.steps_per_block - 1, self.rows,
+        K.stab_update(c, self.argmax, self.p1, self.ent, self.tok, q0, t, s, s == w.steps_per_block - 1, self.rows,
                       self.n_rows, stream)
 
     def schedule(self):
@@ -210,7 +210,7 @@ class LayerStackGenerator:
         K.active_rows(c, self.O, self.rows, self.n_rows, q0, blk, self.o, stream)
         K.lmhead_conf(c, self.h, W["w_lm"], w.batch * blk, w.vocab, w.d_model, w.mask_id, self.argmax,
                       self.p1, self.ent, stream)
-        K.stab_update(c, self.argmax, self.p1, self.tok, q0, t, s, s == w.steps_per_block - 1, self.rows,
+        K.stab_update(c, self.argmax, self.p1, self.ent, self.tok, q0, t, s, s == w.steps_per_block - 1, self.rows,
                       self.n_rows, stream)
 
     def make_prof_events(self, kernels, n_steps):

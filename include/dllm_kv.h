@@ -111,6 +111,14 @@ typedef struct {
   int full_every;    /* > 0: the refresh set of block-local steps s with
                         s % full_every == 0 is every row ("I/O-aware KV cache
                         and self-verifying parallel decoding" 5.1) */
+  int gate;          /* refresh criterion of the active block: 0 = the
+                        unstable rows dilated by R ("Stable Window Decoding"
+                        3.2); 1 = the unstable rows whose cache confidence
+                        conf_alpha (1 - H / ln(vocab - 1)) + conf_beta
+                        exp(-conf_lambda (t + 1 - version)) is below
+                        conf_theta ("I/O-aware KV cache and self-verifying
+                        parallel decoding" 3.1); fp32, in that order */
+  float conf_alpha, conf_beta, conf_lambda, conf_theta;
   int facache;       /* 1: block_attn keeps the online-softmax state of the
                         key tiles outside the block's window and reuses it
                         while the block and its query tokens are unchanged
@@ -286,11 +294,14 @@ dllm_status lmhead_conf(dllm_cache* c, const void* h_dev, const void* w_lm_dev, 
        cfg.swd_R_min), ascending b * L + pos; with
      active_queries the list also holds every active row (the refresh set
      itself stays in the handle and gates kv_refresh's K/V writes).
-   argmax_dev / p_top1_dev: [B * block_len] device; tok_dev [B][L] device,
-   updated in place; rows_dev [B * L], n_rows_dev [1] device outputs. */
+   With cfg.gate = 1 the dilated window is replaced by the unstable rows
+   whose cache confidence is below conf_theta (entropy_dev then required).
+   argmax_dev / p_top1_dev / entropy_dev: [B * block_len] device; tok_dev
+   [B][L] device, updated in place; rows_dev [B * L], n_rows_dev [1] device
+   outputs. */
 dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p_top1_dev,
-                        int32_t* tok_dev, int q_start, int t, int step_in_block, int last_step,
-                        int32_t* rows_dev, int32_t* n_rows_dev, void* stream);
+                        const float* entropy_dev, int32_t* tok_dev, int q_start, int t, int step_in_block,
+                        int last_step, int32_t* rows_dev, int32_t* n_rows_dev, void* stream);
 
 /* --- without device allocation ---------------------------------------- */
 

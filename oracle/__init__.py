@@ -12,12 +12,14 @@ output O, residual stream h, FFN intermediate).
 """
 from .model import (bf16_bits_to_f64, round_store, rms_scale, rope, project_qkv,
                     attention, attention_partial, merge_partials, out_proj, ffn, lm_head_conf, gelu)
-from .swd import SWDState, swd_update, dilate, refresh_rows, expired_rows, radius_at, full_refresh_at
+from .swd import (SWDState, swd_update, dilate, refresh_rows, expired_rows, radius_at, full_refresh_at,
+                  confidence, confidence_rows)
 from .run import run_dense, run_stream, weights_f64, ring_positions, RingSim, NEVER
 
 __all__ = [
     "bf16_bits_to_f64", "round_store", "rms_scale", "rope", "project_qkv",
     "attention", "attention_partial", "merge_partials", "out_proj", "ffn", "lm_head_conf", "gelu", "SWDState",
-    "swd_update", "dilate", "refresh_rows", "expired_rows", "radius_at", "full_refresh_at", "run_dense",
+    "swd_update", "dilate", "refresh_rows", "expired_rows", "radius_at", "full_refresh_at", "confidence",
+    "confidence_rows", "run_dense",
     "run_stream", "weights_f64", "ring_positions", "RingSim", "NEVER",
 ]

@@ -29,7 +29,7 @@ from collections import deque
 import numpy as np
 
 from . import model as M
-from .swd import SWDState, swd_update, refresh_rows, radius_at, full_refresh_at
+from .swd import SWDState, swd_update, refresh_rows, radius_at, full_refresh_at, confidence_rows
 
 NEVER = -(1 << 30)     # version of a cache entry that was never written
 
@@ -85,6 +85,12 @@ def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre
     block start and the queries' token-at-write, and reused (merged with the
     window's fresh state) while they are unchanged; the record's
     "fa_rebuilt" lists the sequences whose state was recomputed.
+    With the workload's early_exit ([SWD] 3.2 and 4.2: when no position is
+    unstable the step may "compute all or end"): a sequence whose active
+    rows are all stable after a step that is not its block's last ends the
+    block - the later steps of the block refresh none of its rows and
+    compute no attention, LM head or update for it (the record's "done"
+    lists those sequences; their argmax is -1 and p1 / entropy NaN).
     """
     B, L, H, dh, d = w.batch, w.seq_len, w.n_heads, w.head_dim, w.d_model
     nl, blk = w.n_layers, w.block_len
@@ -104,6 +110,7 @@ def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre
     for bi in range(w.n_blocks):
         q0 = w.n_prompt + bi * blk
         ac_flat = (np.arange(B)[:, None] * L + q0 + np.arange(blk)[None, :]).reshape(-1)
+        done = np.zeros(B, dtype=bool)            # sequences whose block has ended
         for s in range(w.steps_per_block):
             if t >= total:
                 return trace
@@ -115,6 +122,8 @@ def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre
             full = s == 0 or force_all or mode == "recompute"
             rows = flat_all if full else rows_next          # the refresh set Rf
             rec["rows"] = rows.copy()
+            rec["done"] = done.copy()
+            live_ac = ac_flat[~done[ac_flat // L]]           # active rows of the sequences still running
             # layer-0 bookkeeping of the refreshed rows
             version[:, rows // L, rows % L] = t
             tok_w.reshape(-1)[rows] = tok.reshape(-1)[rows]
@@ -129,6 +138,8 @@ def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre
                 o = np.zeros((B * blk, H, dh))
                 rec["fa_rebuilt"] = []
                 for b in range(B):
+                    if done[b]:
+                        continue
                     qa = caches[0][0][b, q0:q0 + blk]
                     kb, vb = caches[1][0][b], caches[2][0][b]
                     if not facache:
@@ -146,32 +157,48 @@ def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre
                 o_ac = M.round_store(o.reshape(B * blk, d), w.dtype)
                 h_ac = M.out_proj(o_ac, W["w_o"][0], x_emb[ac_flat], w.dtype)
             else:
-                P = _query_rows(w, rows, ac_flat)
+                P = _query_rows(w, rows, live_ac)
                 rec["queries"] = P.copy()
                 o_p, h_p = _layer_stack(w, W, x_emb[P], P % L, P, caches, np.isin(P, rows))
-                where = np.searchsorted(P, ac_flat)
-                assert np.array_equal(P[where], ac_flat), "active rows must pass through the layers"
-                o_ac, h_ac = o_p[where], h_p[where]
+                o_ac, h_ac = np.zeros((B * blk, d)), np.zeros((B * blk, d))
+                live = ~done[ac_flat // L]
+                where = np.searchsorted(P, live_ac)
+                assert np.array_equal(P[where], live_ac), "active rows must pass through the layers"
+                o_ac[live], h_ac[live] = o_p[where], h_p[where]
             am, p1, ent, margin = M.lm_head_conf(h_ac, W["w_lm"], w.mask_id, w.rms_eps)
+            gone = done[ac_flat // L]                        # no LM head for ended sequences
+            am, p1, ent, margin = (np.where(gone, -1, am).astype(np.int32), np.where(gone, np.nan, p1),
+                                   np.where(gone, np.nan, ent), np.where(gone, np.inf, margin))
             am, p1 = am.reshape(B, blk), p1.reshape(B, blk)
             rec.update(argmax=am, p1=p1, ent=ent.reshape(B, blk), margin=margin.reshape(B, blk),
                        o=o_ac.reshape(B, blk, d), h=h_ac.reshape(B, blk, d))
             last = s == w.steps_per_block - 1
             rec["newly"] = swd_update(swd, q0, am, p1, tok, stable, w.swd_K, w.swd_tau, last)
+            if w.early_exit and not last:
+                done |= stable[:, q0:q0 + blk].all(axis=1)
             if last:
                 swd.reset()
                 rows_next = flat_all
             elif full_refresh_at(s + 1, w.full_every):
                 rows_next = flat_all
+            elif w.gate == "confidence":
+                rows_next = confidence_rows(stable, tok, tok_w, version, q0, blk, rec["ent"], np.log(w.vocab - 1),
+                                            t + 1, w.expiry, w.conf_alpha, w.conf_beta, 3.0 / w.steps_per_block,
+                                            w.conf_theta)
             else:
                 R_next = radius_at(s + 1, w.steps_per_block, w.swd_R, w.swd_R_min)
                 rows_next = refresh_rows(stable, tok, tok_w, version, q0, blk, R_next, t + 1, w.expiry)
-            # the row list the next step runs on: Rf, plus the active block
-            # when every active row queries (the next step is in this block
-            # unless this was its last step, and then Rf is every row)
+            if not last and done.any():                 # ended sequences refresh nothing
+                rows_next = rows_next[~done[rows_next // L]]
+            # the row list the next step runs on: Rf, plus the active block of
+            # the running sequences when every active row queries (the next
+            # step is in this block unless this was its last step, and then
+            # Rf is every row)
+            nxt_ac = ac_flat if last else ac_flat[~done[ac_flat // L]]
             rec.update(tok=tok.copy(), stable=stable.copy(), version=version.copy(),
                        tok_w=tok_w.copy(), swd=swd.copy(), rf_next=rows_next.copy(),
-                       rows_next=_query_rows(w, rows_next, ac_flat))
+                       rows_next=_query_rows(w, rows_next, nxt_ac), done_next=done.copy() if not last else
+                       np.zeros(B, dtype=bool))
             trace.append(rec)
             t += 1
     return trace
@@ -179,10 +206,11 @@ def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre
 
 def _query_rows(w, rf, ac_flat):
     """Rows that pass through the layers: the refresh set, plus the active
-    block when the workload runs every active row as a query."""
+    rows (of the running sequences) when the workload runs every active row
+    as a query."""
     if not w.active_queries or len(rf) == w.batch * w.seq_len:
         return rf.copy()
-    return np.union1d(rf, ac_flat).astype(rf.dtype)
+    return np.union1d(rf, ac_flat).astype(np.int64)
 
 
 def _recompute_step(w, W, x_emb, pos_all, ac_flat):

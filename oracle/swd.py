@@ -13,6 +13,10 @@ Sources, cited by page title and section:
   [TA]   "Diffusion latent cache with time anchors" page (mhpq.cn/news/1098081),
          2.3 and 3.1: every cache entry carries the step it was written at; a
          lookup at step t rejects it when t - version > 2.
+  [FlashdLLM] "I/O-aware KV cache and self-verifying parallel decoding"
+         (bjdmk.com.cn/news/5926815), 3.1: the cache confidence of position i
+         at step t, alpha (1 - H_i / H_max) + beta exp(-lambda (t - t_write));
+         alpha ~ 0.7, beta ~ 0.3, lambda ~ 3 / T.
   [LaCache] "Problem statement" / "Inference workflow": the prompt and the
          masked suffix keep their token ids inside a block; the block's first
          step runs a full forward and refills the caches.
@@ -132,6 +136,36 @@ def radius_at(s, steps, R, R_min):
 def full_refresh_at(s, every):
     """Is block-local step s a scheduled refresh of every row?"""
     return every > 0 and s % every == 0
+
+
+def confidence(ent, H_max, age, alpha, beta, lam):
+    """[FlashdLLM] 3.1 cache confidence, in fp32 in this order:
+    alpha * (1 - ent / H_max) + beta * exp(-lam * age)."""
+    f = np.float32
+    a = f(alpha) * (f(1.0) - f(ent) / f(H_max))
+    b = f(beta) * np.exp(-(f(lam) * f(age)), dtype=np.float32)
+    return f(a + b)
+
+
+def confidence_rows(stable, tok, tok_w, version, q0, blk, ent, H_max, t_next, expiry, alpha, beta, lam, theta):
+    """Refresh set for step t_next with the confidence criterion in place of
+    the window: an active position still unstable is refreshed when its cache
+    confidence (its entropy at this step, the age t_next - version of its
+    layer-0 entry) is below theta; plus changed and expired rows as always.
+    ent: [B, blk] entropies of the active block."""
+    B, L = tok.shape
+    rf = np.zeros((B, L), dtype=bool)
+    for b in range(B):
+        for j in range(blk):
+            p = q0 + j
+            if stable[b, p]:
+                continue
+            age = t_next - int(version[0, b, p])
+            if confidence(ent[b, j], H_max, age, alpha, beta, lam) < np.float32(theta):
+                rf[b, p] = True
+    rf |= tok != tok_w
+    rf |= expired_rows(version, t_next, expiry)
+    return np.flatnonzero(rf.reshape(-1)).astype(np.int32)
 
 
 def refresh_rows(stable, tok, tok_w, version, q0, blk, R, t_next, expiry):

@@ -334,7 +334,8 @@ def test_stab_update_random_state(name, last, seed):
         tok_d = i32(tok)
         rows = torch.full((B * L,), -1, dtype=torch.int32, device="cuda")
         n_rows = torch.zeros(1, dtype=torch.int32, device="cuda")
-        K.stab_update(c, i32(argmax), torch.from_numpy(p1.reshape(-1)).cuda(), tok_d, q0, t, 1, last, rows, n_rows)
+        K.stab_update(c, i32(argmax), torch.from_numpy(p1.reshape(-1)).cuda(), None, tok_d, q0, t, 1, last, rows,
+                      n_rows)
         assert K.dllm_cache_check(c) == 0
         n = int(n_rows.item())
         assert n == len(rows_o)

@@ -131,7 +131,7 @@ def _check_step_layers(gen, w, W64, D, t, q0, s, P, rf, seqs, n_per_seq, stats):
     sure = margin > 1e-2
     assert np.array_equal(g_am[ia][sure], am[sure]), (w.name, t, "argmax")
     stats["sure"] += int(sure.sum())
-    return g_am.reshape(B, blk), g_p1.reshape(B, blk)
+    return g_am.reshape(B, blk), g_p1.reshape(B, blk), g_ent.reshape(B, blk)
 
 
 def _teacher_forced(name, n_steps, seqs=None, n_per_seq=None):
@@ -165,19 +165,25 @@ def _teacher_forced(name, n_steps, seqs=None, n_per_seq=None):
             want_P = rf if len(rf) == B * L else np.union1d(rf, ac)
             assert np.array_equal(P, want_P), (name, t, "row list")
             stats["full"] += int(len(rf) == B * L)
-            g_am, g_p1 = _check_step_layers(gen, w, W64, D, t, q0, s, P, rf, seqs, n_per_seq, stats)
+            g_am, g_p1, g_ent = _check_step_layers(gen, w, W64, D, t, q0, s, P, rf, seqs, n_per_seq, stats)
             # bookkeeping of the refresh set, then SWD on the GPU's outputs
             version_o[:, rf // L, rf % L] = t
             tok_w_o.reshape(-1)[rf] = tok_o.reshape(-1)[rf]
             last = s == w.steps_per_block - 1
             newly = O.swd_update(swd, q0, g_am, g_p1, tok_o, stable_o, w.swd_K, w.swd_tau, last)
             stats["commits"] += int(newly.sum())
-            K.stab_update(gen.cache, gen.argmax, gen.p1, gen.tok, q0, t, s, last, gen.rows, gen.n_rows)
-            if last:
-                swd.reset()
+            K.stab_update(gen.cache, gen.argmax, gen.p1, gen.ent, gen.tok, q0, t, s, last, gen.rows, gen.n_rows)
+            if last or O.full_refresh_at(s + 1, w.full_every):
+                if last:
+                    swd.reset()
                 rf = np.arange(B * L)
+            elif w.gate == "confidence":
+                rf = O.confidence_rows(stable_o, tok_o, tok_w_o, version_o, q0, blk, g_ent, np.log(w.vocab - 1),
+                                       t + 1, w.expiry, w.conf_alpha, w.conf_beta, 3.0 / w.steps_per_block,
+                                       w.conf_theta)
             else:
-                rf = O.refresh_rows(stable_o, tok_o, tok_w_o, version_o, q0, blk, w.swd_R, t + 1, w.expiry)
+                R = O.radius_at(s + 1, w.steps_per_block, w.swd_R, w.swd_R_min)
+                rf = O.refresh_rows(stable_o, tok_o, tok_w_o, version_o, q0, blk, R, t + 1, w.expiry)
             assert np.array_equal(gen.tok.cpu().numpy(), tok_o), (name, t, "tok")
             assert np.array_equal(read_field(gen.cache, K.FIELD_STABLE, 0, (B, L), "u8").astype(bool), stable_o), \
                 (name, t, "stable")
@@ -191,13 +197,15 @@ def _teacher_forced(name, n_steps, seqs=None, n_per_seq=None):
     return stats
 
 
-@pytest.mark.parametrize("name", ["mid_multi", "mid_multi_sharp"])
+@pytest.mark.parametrize("name", ["mid_multi", "mid_multi_sharp", "mid_multi_conf"])
 def test_layers_teacher_forced_small(name):
     w = C.get(name)
     stats = _teacher_forced(name, w.n_steps)
     assert stats["rows"] > 0 and stats["full"] >= w.n_blocks
     if name.endswith("sharp"):
         assert stats["commits"] > 0 and stats["quiet"] > 0      # query-only rows were checked
+    if name.endswith("conf"):                                   # confident rows only query
+        assert stats["quiet"] > 0
 
 
 @pytest.mark.parametrize("name", ["twelve_layer", "twelve_layer_sharp"])

@@ -64,7 +64,7 @@ def test_null_handle_is_einval(lib):
     assert lib.kv_refresh(None, 0, None, None, None, None, None, None, 0, None) == 1
     assert lib.block_attn(None, 0, 0, 1, None, None) == 1
     assert lib.lmhead_conf(None, None, None, 1, 2, 2, 0, None, None, None, None) == 1
-    assert lib.stab_update(None, None, None, None, 0, 0, 0, 0, None, None, None) == 1
+    assert lib.stab_update(None, None, None, None, None, 0, 0, 0, 0, None, None, None) == 1
     assert b"null" in lib.dllm_last_error()
 
 

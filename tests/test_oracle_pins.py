@@ -395,6 +395,72 @@ def test_schedules_shape_the_refresh_sets():
     assert saw_partial > 0
 
 
+def test_confidence_closed_form_and_rows():
+    """[FlashdLLM] 3.1: alpha (1 - H / H_max) + beta exp(-lambda age), against
+    scalar code; the rows are the unstable active positions below theta, plus
+    changed and expired rows."""
+    H_max = math.log(999.0)
+    for ent, age in ((0.0, 0), (H_max, 0), (2.5, 3), (6.0, 10)):
+        want = 0.7 * (1.0 - ent / H_max) + 0.3 * math.exp(-0.3 * age)
+        assert abs(float(O.confidence(ent, H_max, age, 0.7, 0.3, 0.3)) - want) < 1e-6
+    B, L, q0, blk = 1, 12, 4, 4
+    stable = np.zeros((B, L), dtype=bool)
+    stable[0, 5] = True
+    tok = np.ones((B, L), dtype=np.int64)
+    tok_w = tok.copy()
+    tok_w[0, 10] = 3                                     # a changed row
+    version = np.full((1, B, L), 9)
+    version[0, 0, 7] = 2                                 # an old entry: low confidence
+    ent = np.array([[6.5, 0.1, 0.2, 0.2]])               # position 4 is unsure, 5 stable, 6 and 7 sure
+    rows = O.confidence_rows(stable, tok, tok_w, version, q0, blk, ent, H_max, 10, -1, 0.7, 0.3, 0.3, 0.5)
+    # 4: 0.7 * 0.06 + 0.3 e^-0.3 < 0.5; 6: 0.68 + ...; 7: 0.68 + 0.3 e^-2.4 > 0.5; 10: changed
+    assert list(rows) == [4, 10]
+    ent2 = np.array([[6.5, 0.1, 0.2, 4.9]])             # 7: 0.7 * 0.29 + 0.3 e^-2.4 < 0.5
+    assert list(O.confidence_rows(stable, tok, tok_w, version, q0, blk, ent2, H_max, 10, -1, 0.7, 0.3, 0.3,
+                                  0.5)) == [4, 7, 10]
+
+
+def test_confidence_gate_loop():
+    """mid_bf16_conf: every partial step's refresh set is the confidence
+    rule applied to the step's entropies and versions; some steps refresh a
+    part of the block only, and some positions commit."""
+    w, W, tok0 = _load("mid_bf16_conf")
+    tr = O.run_dense(w, W, tok0, mode="cached")
+    partial = 0
+    for prev, r in zip(tr[:-1], tr[1:]):
+        if r["s"] == 0:
+            continue
+        want = O.confidence_rows(prev["stable"], prev["tok"], prev["tok_w"], prev["version"], r["q0"], w.block_len,
+                                 prev["ent"], np.log(w.vocab - 1), r["t"], w.expiry, w.conf_alpha, w.conf_beta,
+                                 3.0 / w.steps_per_block, w.conf_theta)
+        assert np.array_equal(r["rows"], want), r["t"]
+        partial += 0 < len(r["rows"]) < w.batch * w.block_len
+    assert partial > 0 and sum(int(r["newly"].sum()) for r in tr) > 0
+
+
+@pytest.mark.parametrize("name", ["mid_bf16_exit", "mid_multi_exit"])
+def test_early_exit_changes_no_token(name):
+    """A sequence whose active rows are all stable ends its block: its later
+    steps refresh nothing and compute nothing, and every token of every step
+    equals the run without early exit (stable positions never change)."""
+    from dataclasses import replace
+    w, W, tok0 = _load(name)
+    a = O.run_dense(w, W, tok0, mode="cached")
+    b = O.run_dense(replace(w, early_exit=0), W, tok0, mode="cached")
+    L, blk = w.seq_len, w.block_len
+    ended = 0
+    for ra, rb in zip(a, b):
+        assert np.array_equal(ra["tok"], rb["tok"]), ra["t"]
+        assert np.array_equal(ra["stable"], rb["stable"]), ra["t"]
+        for s in np.flatnonzero(ra["done"]):
+            ended += 1
+            assert ra["stable"][s, ra["q0"]:ra["q0"] + blk].all()
+            assert not np.any(ra["rows"] // L == s)                  # nothing of it refreshed
+            assert np.all(ra["argmax"][s] == -1)
+        assert len(ra["rows"]) <= len(rb["rows"])
+    assert ended > 0
+
+
 def test_multilayer_queries_and_kv_gate():
     """Multi-layer denoiser: the rows that pass through the layers are the
     refresh set plus the active block, and only refresh-set rows rewrite K/V

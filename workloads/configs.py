@@ -30,6 +30,13 @@ class Workload:
     swd_R: int = 2
     swd_R_min: int = -1   # dilation radius at a block's first step (growing to swd_R); -1 = fixed swd_R
     full_every: int = 0   # refresh every row at block-local steps s with s % full_every == 0 (0 = never)
+    # refresh criterion of the active block: "window" (unstable rows dilated by
+    # R) or "confidence" (unstable rows whose cache confidence is below theta)
+    gate: str = "window"
+    conf_alpha: float = 0.7
+    conf_beta: float = 0.3
+    conf_theta: float = 0.5
+    early_exit: int = 0   # 1: a sequence whose active rows are all stable ends its block
     expiry: int = -1      # reject t - version > expiry; -1 = no expiry
     mask_id: int = 0
     rope_theta: float = 10000.0
@@ -141,6 +148,20 @@ MID_MULTI = Workload(
 
 MID_MULTI_SHARP = replace(MID_MULTI, name="mid_multi_sharp", lm_scale=40.0, steps_per_block=10, seed=18)
 
+# The confidence criterion in place of the window, without version expiry:
+# with W_lm x 12 the entropies sit around the threshold's reach, so a
+# position is refreshed once its entry has aged enough for its entropy, and
+# tau = 0.4 lets some positions commit.
+MID_MULTI_CONF = replace(MID_MULTI, name="mid_multi_conf", lm_scale=12.0, steps_per_block=10, seed=21,
+                         gate="confidence", expiry=-1, swd_tau=0.4)
+MID_BF16_CONF = replace(MID_BF16, name="mid_bf16_conf", lm_scale=12.0, steps_per_block=10, seed=22,
+                        gate="confidence", expiry=-1, swd_tau=0.4)
+
+# Early block exit on sharp heads: sequences end their blocks at different
+# steps (batch 3, 12 steps per block).
+MID_BF16_EXIT = replace(MID_BF16_SHARP, name="mid_bf16_exit", batch=3, steps_per_block=12, early_exit=1, seed=23)
+MID_MULTI_EXIT = replace(MID_MULTI_SHARP, name="mid_multi_exit", batch=3, steps_per_block=12, early_exit=1, seed=24)
+
 # More rows than the weight-streaming path takes (256): the projection runs
 # on the large-M kernels.  600 rows = 5 row tiles (an odd count: the last
 # cluster pair has a half past the end), 900 rows = 7 tiles + 4 rows.
@@ -149,7 +170,8 @@ BIG_ROWS_DH64 = replace(MID_BF16_DH64, name="big_rows_dh64", batch=3, seq_len=30
 
 ALL = dict(NAMED)
 for _w in (MID_BF16, MID_BF16_DH64, TINY_FP32_SHARP, MID_BF16_SHARP, MID_SINK, TINY_SINK_F32, MID_MULTI,
-           MID_MULTI_SHARP, BIG_ROWS, BIG_ROWS_DH64, TWELVE_LAYER_SHARP, MID_BF16_SCHED):
+           MID_MULTI_SHARP, BIG_ROWS, BIG_ROWS_DH64, TWELVE_LAYER_SHARP, MID_BF16_SCHED, MID_MULTI_CONF,
+           MID_BF16_CONF, MID_BF16_EXIT, MID_MULTI_EXIT):
     ALL[_w.name] = _w
 
 
