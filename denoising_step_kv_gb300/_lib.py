@@ -12,7 +12,7 @@ LIB_PATH = os.path.join(_HERE, "libdllmkv.so")
 
 DLLM_F32, DLLM_BF16 = 0, 1
 (FIELD_Q, FIELD_K, FIELD_V, FIELD_VERSION, FIELD_TOK_W, FIELD_STABLE, FIELD_HIST_TOK, FIELD_HIST_P, FIELD_HIST_N,
- FIELD_FA_REBUILT) = range(10)
+ FIELD_FA_REBUILT, FIELD_SEQ_DONE) = range(11)
 ERR_ROW, ERR_TOKEN, ERR_TIMEOUT, ERR_POS = 1, 2, 4, 8
 STATUS = {0: "OK", 1: "EINVAL", 2: "ENOMEM", 3: "ECUDA", 4: "EDEVICE", 5: "EUNSUPPORTED"}
 
@@ -28,7 +28,7 @@ class CacheCfg(ctypes.Structure):
         ("max_pos", ctypes.c_int), ("ffn", ctypes.c_int), ("swd_R_min", ctypes.c_int),
         ("steps_per_block", ctypes.c_int), ("full_every", ctypes.c_int), ("gate", ctypes.c_int),
         ("conf_alpha", ctypes.c_float), ("conf_beta", ctypes.c_float), ("conf_lambda", ctypes.c_float),
-        ("conf_theta", ctypes.c_float), ("facache", ctypes.c_int),
+        ("conf_theta", ctypes.c_float), ("early_exit", ctypes.c_int), ("facache", ctypes.c_int),
     ]
 
 
@@ -57,6 +57,8 @@ _SIGS = {
     "dllm_profile_events": [_VP, _I, _VP, _VP],
     "lmhead_conf_noalloc": [_VP, _VP, _I, _I, _I, _I, _I, ctypes.c_float, _VP, _VP, _VP, _VP],
     "dllm_wait_selftest": [_VP, ctypes.c_uint64, _VP],
+    "kv_project": [_VP, _I, _VP, _VP, _VP, _I, _VP, _VP],
+    "ring_append": [_VP, _I, _VP, _I, _I, _VP],
 }
 PROF_QKV_GEMM, PROF_ATTN, PROF_LM_GEMM, PROF_OUT_GEMM, PROF_FFN = 1, 2, 3, 4, 5
 EXPORTS = list(_SIGS) + ["dllm_last_error"]
@@ -113,6 +115,7 @@ def make_cfg(w, vocab=None, facache=False):
     c.gate = 1 if w.gate == "confidence" else 0
     c.conf_alpha, c.conf_beta, c.conf_theta = w.conf_alpha, w.conf_beta, w.conf_theta
     c.conf_lambda = 3.0 / w.steps_per_block if w.steps_per_block else 0.0
+    c.early_exit = w.early_exit
     return c
 
 
@@ -226,3 +229,11 @@ def lmhead_conf_noalloc(h, w_lm, M, V, d, dtype, mask_id, rms_eps, argmax, p_top
 def dllm_wait_selftest(c, limit_ns, stream=None):
     """One bounded wait on a barrier nothing arrives on (sets ERR_TIMEOUT)."""
     _check("dllm_wait_selftest", lib().dllm_wait_selftest(c, ctypes.c_uint64(limit_ns), _s(stream)))
+
+
+def kv_project(c, layer, tok, embed, w_qkv, n, staged, stream=None):
+    _check("kv_project", lib().kv_project(c, layer, _p(tok), _p(embed), _p(w_qkv), n, _p(staged), _s(stream)))
+
+
+def ring_append(c, layer, staged, n0, count, stream=None):
+    _check("ring_append", lib().ring_append(c, layer, _p(staged), n0, count, _s(stream)))

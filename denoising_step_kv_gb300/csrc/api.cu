@@ -60,7 +60,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 void free_all(dllm_cache* c) {
   void* bufs[] = {c->q, c->k, c->v, c->version, c->tok_w, c->stable, c->hist_tok, c->hist_p, c->hist_n, c->words,
                   c->rope, c->err, c->ticket, c->X, c->rs, c->lm_part, c->lm_rs, c->ffn_buf,
-                  c->fa_state, c->fa_key, c->fa_rebuilt};
+                  c->fa_state, c->fa_key, c->fa_rebuilt, c->seq_done, c->m_live};
   for (void* b : bufs)
     if (b) cudaFree(b);
 }
@@ -169,6 +169,8 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
             dalloc(&c->lm_part, static_cast<size_t>(c->lm_rows_cap) * c->lm_tiles_cap * 16) &&
             dalloc(&c->lm_rs, static_cast<size_t>(c->lm_rows_cap) * sizeof(float)) &&
             dalloc(&c->ffn_buf, sr * static_cast<size_t>(g.ffn) * c->elem);
+  if (ok && !streaming)
+    ok = dalloc(&c->seq_done, static_cast<size_t>(g.batch)) && dalloc(&c->m_live, sizeof(int));
   if (ok && g.facache) {
     const size_t bh = static_cast<size_t>(g.batch) * g.n_heads;
     ok = dalloc(&c->fa_state, bh * 64 * (g.head_dim + 4) * sizeof(float)) &&
@@ -278,6 +280,10 @@ dllm_status dllm_state_copy(dllm_cache* c, int field, int layer, void* host, siz
   } else if (field == DLLM_FIELD_HIST_N) {
     ptr = c->hist_n;
     size = g.batch * blk * sizeof(int);
+  } else if (field == DLLM_FIELD_SEQ_DONE) {
+    if (!c->seq_done) return fail(DLLM_EINVAL, "dllm_state_copy: streaming caches have no block state");
+    ptr = c->seq_done;
+    size = g.batch;
   } else if (field == DLLM_FIELD_FA_REBUILT) {
     if (!c->fa_rebuilt) return fail(DLLM_EINVAL, "dllm_state_copy: the cache keeps no attention state");
     ptr = c->fa_rebuilt;
@@ -327,6 +333,41 @@ dllm_status kv_refresh(dllm_cache* c, int layer, const void* x_dev, const int32_
     DLLM_LAUNCH(gemm_qkv(c, layer, A, c->seq_rows, rows_dev ? n_rows_dev : nullptr, rows_dev, w_qkv_dev, st),
                 "kv_refresh: projection");
   }
+  return DLLM_OK;
+}
+
+dllm_status kv_project(dllm_cache* c, int layer, const int32_t* tok_dev, const void* embed_dev, const void* w_qkv_dev,
+                       int n, void* staged_dev, void* stream) {
+  DLLM_CHECK_HANDLE(c);
+  const dllm_cache_cfg& g = c->cfg;
+  if (g.sink <= 0) return fail(DLLM_EINVAL, "kv_project: streaming caches only");
+  if (layer < 0 || layer >= g.n_layers) return fail(DLLM_EINVAL, "kv_project: layer out of range");
+  if (!tok_dev || !embed_dev || !w_qkv_dev || !staged_dev) return fail(DLLM_EINVAL, "kv_project: null pointer");
+  if (n < 0 || n > c->max_pos) return fail(DLLM_EINVAL, "kv_project: n outside [0, max_pos]");
+  if (!aligned16(w_qkv_dev) || !aligned16(embed_dev) || !aligned16(staged_dev))
+    return fail(DLLM_EINVAL, "kv_project: pointers must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // chunks of the compact buffer's rows: gather (embedding, RMS scale), then
+  // the projection with the staging epilogue
+  for (int r0 = 0; r0 < n; r0 += c->seq_rows) {
+    const int cn = std::min(c->seq_rows, n - r0);
+    DLLM_LAUNCH(launch_gather(c, layer, nullptr, nullptr, cn, nullptr, tok_dev, embed_dev, 0, st, r0),
+                "kv_project: gather");
+    ProfScope prof(c, DLLM_PROF_QKV_GEMM, st);
+    DLLM_LAUNCH(gemm_qkv(c, layer, c->X, cn, nullptr, nullptr, w_qkv_dev, st, staged_dev, r0), "kv_project: projection");
+  }
+  return DLLM_OK;
+}
+
+dllm_status ring_append(dllm_cache* c, int layer, const void* staged_dev, int n0, int count, void* stream) {
+  DLLM_CHECK_HANDLE(c);
+  const dllm_cache_cfg& g = c->cfg;
+  if (g.sink <= 0) return fail(DLLM_EINVAL, "ring_append: streaming caches only");
+  if (layer < 0 || layer >= g.n_layers) return fail(DLLM_EINVAL, "ring_append: layer out of range");
+  if (!staged_dev || !aligned16(staged_dev)) return fail(DLLM_EINVAL, "ring_append: staged must be 16-byte aligned");
+  if (count < 0 || n0 < 0 || n0 + count > c->max_pos) return fail(DLLM_EINVAL, "ring_append: tokens outside [0, max_pos)");
+  if (count > g.window) return fail(DLLM_EINVAL, "ring_append: more tokens than the rolling window in one call");
+  DLLM_LAUNCH(launch_ring_append(c, layer, staged_dev, n0, count, static_cast<cudaStream_t>(stream)), "ring_append");
   return DLLM_OK;
 }
 
@@ -405,6 +446,13 @@ dllm_status attn_out(dllm_cache* c, const void* o_dev, const void* w_o_dev, cons
     return fail(DLLM_EINVAL, "attn_out: pointers must be 16-byte aligned");
   const int M = g.batch * std::max(q_len, 1);
   ProfScope prof(c, DLLM_PROF_OUT_GEMM, static_cast<cudaStream_t>(stream));
+  if (!m_dev && g.early_exit && g.sink == 0 && q_len == g.block_len) {
+    // the active block's rows: none once every sequence has ended its block
+    DLLM_LAUNCH(gemm_resid(c, o_dev, w_o_dev, M, M, c->m_live, c->d, c->d, x_res_dev, tok_dev, embed_dev, q_start,
+                           q_len, h_dev, static_cast<cudaStream_t>(stream)),
+                "attn_out");
+    return DLLM_OK;
+  }
   DLLM_LAUNCH(gemm_resid(c, o_dev, w_o_dev, M, c->seq_rows, m_dev, c->d, c->d, x_res_dev, tok_dev, embed_dev,
                          q_start, std::max(q_len, 1), h_dev, static_cast<cudaStream_t>(stream)),
               "attn_out");
@@ -441,13 +489,16 @@ dllm_status lmhead_conf(dllm_cache* c, const void* h_dev, const void* w_lm_dev, 
   if (M == 0) return DLLM_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int n_tiles = cdiv(V, lm_tile_cols(c, M, V));
-  DLLM_LAUNCH(launch_rownorm(c, h_dev, M, nullptr, d, c->lm_rs, st), "lmhead_conf: norm");
+  // with early exit, a device count: 0 once every sequence has ended its block
+  const int* M_dev = (c->cfg.early_exit && c->m_live && M == c->lm_rows_cap) ? c->m_live : nullptr;
+  DLLM_LAUNCH(launch_rownorm(c, h_dev, M, M_dev, d, c->lm_rs, st), "lmhead_conf: norm");
   {
     ProfScope prof(c, DLLM_PROF_LM_GEMM, st);
-    DLLM_LAUNCH(gemm_lm(c, h_dev, w_lm_dev, M, V, d, c->lm_rs, mask_id, c->lm_part, n_tiles, st),
+    DLLM_LAUNCH(gemm_lm(c, h_dev, w_lm_dev, M, M_dev, V, d, c->lm_rs, mask_id, c->lm_part, n_tiles, st),
                 "lmhead_conf: gemm");
   }
-  DLLM_LAUNCH(launch_lm_merge(c->lm_part, M, n_tiles, argmax_dev, p_top1_dev, entropy_dev, nullptr, st), "lmhead_conf: merge");
+  DLLM_LAUNCH(launch_lm_merge(c->lm_part, M, M_dev, n_tiles, argmax_dev, p_top1_dev, entropy_dev, nullptr, st),
+              "lmhead_conf: merge");
   return DLLM_OK;
 }
 

@@ -21,9 +21,11 @@ __device__ __forceinline__ float kv_at(const uint8_t* base, const KvLayout& kv, 
 template <int DH>
 __global__ void __launch_bounds__(32)
     attn_f32_kernel(const uint8_t* __restrict__ Ql, const uint8_t* __restrict__ Kl, const uint8_t* __restrict__ Vl,
-                    KvLayout kv, int ld, int q_pos0, int q_len, int kv_len, float scale, float* __restrict__ out) {
+                    KvLayout kv, int ld, int q_pos0, int q_len, int kv_len, float scale,
+                    const uint8_t* __restrict__ seq_done, float* __restrict__ out) {
   constexpr int PER = DH / 32;
   const int qi = blockIdx.x, h = blockIdx.y, b = blockIdx.z, lane = threadIdx.x;
+  if (seq_done && seq_done[b]) return;       // the sequence has ended its block
   float q[PER], acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
@@ -68,8 +70,9 @@ cudaError_t launch_tc_r(dllm_cache* c, const uint8_t* Ql, const uint8_t* Kl, con
     if (e != cudaSuccess) return e;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(DH));
+  const uint8_t* done = c->cfg.sink == 0 ? done_flags(c) : nullptr;
   return launch_ex(attn_tc::attn_tc_kernel<DH, R>, dim3(n_split, H, n_seq), dim3(192), S::SMEM, st, n_split, Ql, Kl,
-                   Vl, c->kv, c->d, q_pos0, q_len, kv_len, keys_per_split, scale_log2, out, c->err);
+                   Vl, c->kv, c->d, q_pos0, q_len, kv_len, keys_per_split, scale_log2, done, out, c->err);
 }
 
 // Replicas R of the queries in the 128 MMA rows: as many as fit.
@@ -127,7 +130,7 @@ cudaError_t launch_fa_r(dllm_cache* c, int q_pos0, int q_len, bf16* out, cudaStr
   const uint8_t* Vl = static_cast<const uint8_t*>(c->v);
   return launch_ex(attn_fa::attn_fa_kernel<DH, R>, dim3(c->cfg.n_heads, c->cfg.batch), dim3(192), S::SMEM, st, 0, Ql,
                    Kl, Vl, c->kv, c->d, q_pos0, q_len, L, w_lo, w_hi, scale_log2, c->tok_w, L, c->fa_state,
-                   c->fa_key, out, c->err, c->fa_rebuilt);
+                   c->fa_key, done_flags(c), out, c->err, c->fa_rebuilt);
 }
 
 cudaError_t attn_facache(dllm_cache* c, int q_pos0, int q_len, void* out, cudaStream_t st) {
@@ -152,14 +155,16 @@ cudaError_t attn_dense(dllm_cache* c, int layer, int q_pos0, int q_len, int kv_l
   const uint8_t* Ql = static_cast<const uint8_t*>(c->q) + off;
   const uint8_t* Kl = static_cast<const uint8_t*>(c->k) + off;
   const uint8_t* Vl = static_cast<const uint8_t*>(c->v) + off;
+  // early exit applies to the active block of a dense cache, not to a stream
+  const uint8_t* done = c->cfg.sink == 0 ? done_flags(c) : nullptr;
   if (c->cfg.dtype == DLLM_F32) {
     const dim3 grid(q_len, c->cfg.n_heads, n_seq);
     const float scale = 1.f / sqrtf(static_cast<float>(dh));
     float* o = static_cast<float*>(out);
     switch (dh) {
-      case 32: attn_f32_kernel<32><<<grid, 32, 0, st>>>(Ql, Kl, Vl, c->kv, c->d, q_pos0, q_len, kv_len, scale, o); break;
-      case 64: attn_f32_kernel<64><<<grid, 32, 0, st>>>(Ql, Kl, Vl, c->kv, c->d, q_pos0, q_len, kv_len, scale, o); break;
-      case 128: attn_f32_kernel<128><<<grid, 32, 0, st>>>(Ql, Kl, Vl, c->kv, c->d, q_pos0, q_len, kv_len, scale, o); break;
+      case 32: attn_f32_kernel<32><<<grid, 32, 0, st>>>(Ql, Kl, Vl, c->kv, c->d, q_pos0, q_len, kv_len, scale, done, o); break;
+      case 64: attn_f32_kernel<64><<<grid, 32, 0, st>>>(Ql, Kl, Vl, c->kv, c->d, q_pos0, q_len, kv_len, scale, done, o); break;
+      case 128: attn_f32_kernel<128><<<grid, 32, 0, st>>>(Ql, Kl, Vl, c->kv, c->d, q_pos0, q_len, kv_len, scale, done, o); break;
       default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(192, 2)
     attn_fa_kernel(const uint8_t* __restrict__ Ql, const uint8_t* __restrict__ Kl, const uint8_t* __restrict__ Vl,
                    KvLayout kv, int ld, int q_pos0, int q_len, int kv_len, int w_lo, int w_hi, float scale_log2,
                    const int* __restrict__ tok_w, int L, float* __restrict__ state, int* __restrict__ key,
-                   bf16* __restrict__ out, unsigned* err, int* __restrict__ rebuilt) {
+                   const uint8_t* __restrict__ seq_done, bf16* __restrict__ out, unsigned* err,
+                   int* __restrict__ rebuilt) {
   using S = Shape<DH, R>;
   using attn_tc::Bars;
   constexpr int QP = S::QP, KG = S::KG;
@@ -115,6 +116,7 @@ __global__ void __launch_bounds__(192, 2)
   }
   pdl_launch();
   pdl_wait();     // the cache rows and tokens of this step are written
+  if (seq_done && seq_done[b]) return;     // the sequence has ended its block (no TMEM held yet)
 
   // ---- is the kept state valid for this block and these query tokens?
   int* mykey = key + static_cast<size_t>(b * H + h) * KEY_INTS;

@@ -187,7 +187,7 @@ template <int DH, int R>
 __global__ void __launch_bounds__(192, 1)
     attn_tc_kernel(const uint8_t* __restrict__ Ql, const uint8_t* __restrict__ Kl, const uint8_t* __restrict__ Vl,
                    KvLayout kv, int ld, int q_pos0, int q_len, int kv_len, int keys_per_split, float scale_log2,
-                   bf16* __restrict__ out, unsigned* err) {
+                   const uint8_t* __restrict__ seq_done, bf16* __restrict__ out, unsigned* err) {
   using S = Shape<DH, R>;
   constexpr int QP = S::QP, KG = S::KG;
   static_assert(sizeof(Bars) <= 256, "barrier block");
@@ -234,6 +234,16 @@ __global__ void __launch_bounds__(192, 1)
   }
   pdl_launch();
   pdl_wait();     // the cache rows of this step are written by the projection
+  // a sequence that has ended its block (every CTA of the cluster shares b):
+  // no attention, leave before any cluster barrier
+  if (seq_done && seq_done[b]) {
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, S::TMEM_COLS);
+    }
+    return;
+  }
 
   // per-row results of the softmax warps (kept for the merge)
   float m_ref = -INFINITY, l_sum = 0.f;

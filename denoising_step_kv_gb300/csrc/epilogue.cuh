@@ -63,6 +63,11 @@ struct EpiQKV {
   const float2* rope;   // [DH/2] frequencies theta^(-2i/DH) as (hi, lo)
   const uint32_t* gate; // refresh-set flag words [B][Lw] (null: every row writes K/V)
   int L, d, rows_cap, streaming, S, W, max_pos, Lw;
+  // staging instead of the cache (streaming pre-projection): row m is stream
+  // token row0 + m (without a row list) and its q | k | v go to
+  // stage[(row0 + m) * 3d ...] row-major, RoPE applied
+  T* stage;
+  int row0;
 
   // does row (b, pos) rewrite its K and V (a query-only row stores Q alone)
   __device__ __forceinline__ bool writes_kv(int b, int pos) const {
@@ -73,7 +78,7 @@ struct EpiQKV {
   __device__ __forceinline__ bool locate(int m, int M, int& b, int& slot, int& pos, float& sc) const {
     b = 0; slot = 0; pos = 0; sc = 0.f;
     if (m >= M) return false;
-    const int row = rows ? rows[m] : m;
+    const int row = rows ? rows[m] : row0 + m;
     bool ok;
     if (streaming) {
       ok = row >= 0 && row < max_pos;
@@ -100,6 +105,10 @@ struct EpiQKV {
     uint8_t* base = part == 0 ? q : part == 1 ? k : v;
     const bool ok = ok_row && (part == 0 || writes_kv(b, pos));
     auto put = [&](int col, const float* vals) {    // col: column inside the part
+      if (stage) {
+        store_row(stage + static_cast<size_t>(pos) * 3 * d + part * d + col, vals, 32);
+        return;
+      }
       const int h = col / DH;
       store_kv32<T>(base, kv, b, h, slot, col - h * DH, vals);
     };
@@ -170,7 +179,10 @@ struct EpiQKV {
           for (int j = 0; j < 32; ++j) a[j] *= sc;
         }
         const int col = c0 + c * 32, h = col / DH;
-        store_kv32<T>(base, kv, b, h, slot, col - h * DH, a);
+        if (stage)
+          store_row(stage + static_cast<size_t>(pos) * 3 * d + part * d + col, a, 32);
+        else
+          store_kv32<T>(base, kv, b, h, slot, col - h * DH, a);
       }
     }
   }

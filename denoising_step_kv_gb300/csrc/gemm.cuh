@@ -368,7 +368,7 @@ constexpr size_t sharea_smem_bytes() { return 1024 + STAGES * (A_BYTES + SBN * B
 template <class Epi, int STAGES, int CS, int SBN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_sharea_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M,
-                       int N, int K, Epi epi, unsigned* err) {
+                       const int* __restrict__ M_dev, int N, int K, Epi epi, unsigned* err) {
   static_assert(CS == 2 || CS == 4, "the rows' tile splits into CS whole 8-row swizzle groups");
   static_assert(SBN == 128 || SBN == 256, "one MMA per 16-deep slice (N <= 256)");
   constexpr int SB_BYTES = SBN * BK * 2, S_BYTES = A_BYTES + SB_BYTES, PREF = 8;
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int cl = blockIdx.x / CS, n_cl = gridDim.x / CS;
   const int nM = (M + BM - 1) / BM, nN = (N + SBN - 1) / SBN, nK = (K + BK - 1) / BK;
   const int nG = (nN + CS - 1) / CS;
-  const int tiles = M > 0 ? nM * nG : 0;          // cluster tiles (row tile, group of CS column tiles)
+  int tiles = M > 0 ? nM * nG : 0;                // cluster tiles (row tile, group of CS column tiles)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -420,6 +420,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort = &bars->abort;
   pdl_launch();
   pdl_wait();
+  if (M_dev && *M_dev <= 0) tiles = 0;            // a device count of 0 (the same in every CTA): no work
 
   if (warp == 0) {
     if (lane == 0) {

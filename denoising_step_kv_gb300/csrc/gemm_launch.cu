@@ -43,8 +43,8 @@ cudaError_t launch_pair(dllm_cache* c, const CUtensorMap& ta, const CUtensorMap&
 }
 
 template <class Epi, int STAGES, int CS, int SBN>
-cudaError_t launch_sharea(dllm_cache* c, const void* A, int M, const void* B, int N, int K, const Epi& epi,
-                          cudaStream_t st) {
+cudaError_t launch_sharea(dllm_cache* c, const void* A, int M, const int* M_dev, const void* B, int N, int K,
+                          const Epi& epi, cudaStream_t st) {
   constexpr size_t smem = tc::sharea_smem_bytes<STAGES, SBN>();
   static PerDeviceOnce attr;
   {
@@ -59,7 +59,7 @@ cudaError_t launch_sharea(dllm_cache* c, const void* A, int M, const void* B, in
   const int per_sm = 2 * tc::sharea_smem_bytes<STAGES, SBN>() <= 227 * 1024 ? 2 : 1;
   const int clusters = std::max(1, std::min(tiles, per_sm * c->num_sms / CS));
   return launch_ex(tc::gemm_sharea_kernel<Epi, STAGES, CS, SBN>, dim3(CS * clusters), dim3(tc::THREADS), smem, st, CS, ta,
-                   tb, M, N, K, epi, c->err);
+                   tb, M, M_dev, N, K, epi, c->err);
 }
 
 template <class Epi, int S>
@@ -196,23 +196,31 @@ EpiQKV<T, DH> make_qkv(dllm_cache* c, int layer, const int* rows) {
   e.max_pos = c->max_pos;
   e.gate = kv_gate(c);
   e.Lw = c->Lw;
+  e.stage = nullptr;
+  e.row0 = 0;
   return e;
 }
 
 template <int DH>
 cudaError_t qkv_dh(dllm_cache* c, int layer, const void* A, int M_cap, const int* M_dev, const int* rows,
-                   const void* w, cudaStream_t st) {
+                   const void* w, void* stage, int row0, cudaStream_t st) {
   const int d = c->d, N = 3 * d;
   const int M_host = M_dev ? 0 : M_cap;
   if (c->cfg.dtype == DLLM_BF16) {
-    if constexpr (DH >= 64)    // bf16 caches have head_dim 64 or 128
-      return run_tc(c, A, M_cap, M_host, M_dev, w, N, d, make_qkv<bf16, DH>(c, layer, rows), st,
+    if constexpr (DH >= 64) {  // bf16 caches have head_dim 64 or 128
+      auto e = make_qkv<bf16, DH>(c, layer, rows);
+      e.stage = static_cast<bf16*>(stage);
+      e.row0 = row0;
+      return run_tc(c, A, M_cap, M_host, M_dev, w, N, d, e, st,
                     d % tc::PBN == 0);   // a 256-wide tile stays inside q, k or v
+    }
     return cudaErrorInvalidValue;
   }
-  if (d % 128 == 0) return run_simt<4>(A, M_cap, M_host, M_dev, w, N, d, make_qkv<float, DH>(c, layer, rows), st);
-  if constexpr (DH <= 64)
-    return run_simt<2>(A, M_cap, M_host, M_dev, w, N, d, make_qkv<float, DH>(c, layer, rows), st);
+  auto e = make_qkv<float, DH>(c, layer, rows);
+  e.stage = static_cast<float*>(stage);
+  e.row0 = row0;
+  if (d % 128 == 0) return run_simt<4>(A, M_cap, M_host, M_dev, w, N, d, e, st);
+  if constexpr (DH <= 64) return run_simt<2>(A, M_cap, M_host, M_dev, w, N, d, e, st);
   return cudaErrorInvalidValue;
 }
 
@@ -228,11 +236,11 @@ int lm_tile_cols(const dllm_cache* c, int M, int V) {
 }
 
 cudaError_t gemm_qkv(dllm_cache* c, int layer, const void* A, int M_cap, const int* M_dev, const int* rows,
-                     const void* w_qkv, cudaStream_t st) {
+                     const void* w_qkv, cudaStream_t st, void* stage, int row0) {
   switch (c->cfg.head_dim) {
-    case 32: return qkv_dh<32>(c, layer, A, M_cap, M_dev, rows, w_qkv, st);
-    case 64: return qkv_dh<64>(c, layer, A, M_cap, M_dev, rows, w_qkv, st);
-    case 128: return qkv_dh<128>(c, layer, A, M_cap, M_dev, rows, w_qkv, st);
+    case 32: return qkv_dh<32>(c, layer, A, M_cap, M_dev, rows, w_qkv, stage, row0, st);
+    case 64: return qkv_dh<64>(c, layer, A, M_cap, M_dev, rows, w_qkv, stage, row0, st);
+    case 128: return qkv_dh<128>(c, layer, A, M_cap, M_dev, rows, w_qkv, stage, row0, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -265,8 +273,8 @@ cudaError_t gemm_gelu(dllm_cache* c, const void* A, const void* W, int M, int M_
   return run_simt<1>(A, M_cap, M, M_dev, W, N, K, e, st);
 }
 
-cudaError_t gemm_lm(dllm_cache* c, const void* A, const void* W, int M, int V, int d, const float* rs,
-                    int mask_id, void* part, int n_tiles, cudaStream_t st) {
+cudaError_t gemm_lm(dllm_cache* c, const void* A, const void* W, int M, const int* M_dev, int V, int d,
+                    const float* rs, int mask_id, void* part, int n_tiles, cudaStream_t st) {
   EpiLM e{rs, mask_id, static_cast<LMPart*>(part), n_tiles};
   if (c->cfg.dtype == DLLM_BF16) {
     if (M > tc::BM) {   // pairs of row tiles share each 256-column weight tile
@@ -274,14 +282,14 @@ cudaError_t gemm_lm(dllm_cache* c, const void* A, const void* W, int M, int V, i
       if (!make_tmap_2d(&ta, A, d, M, static_cast<uint64_t>(d) * 2, tc::BK, tc::BM, true) ||
           !make_tmap_2d(&tb, W, d, V, static_cast<uint64_t>(d) * 2, tc::BK, tc::BN, true))
         return cudaErrorInvalidValue;
-      return launch_pair<EpiLM, 4>(c, ta, tb, M, M, nullptr, 0, V, d, e, st);
+      return launch_pair<EpiLM, 4>(c, ta, tb, M, M_dev ? 0 : M, M_dev, 0, V, d, e, st);
     }
     // one row tile, many vocab tiles: clusters of 4 share the rows' tile,
     // one 128 x 256 tile per CTA and SM
-    if (M > 0 && cdiv(V, tc::PBN) >= 8) return launch_sharea<EpiLM, 4, 4, tc::PBN>(c, A, M, W, V, d, e, st);
-    return run_tc(c, A, M, M, nullptr, W, V, d, e, st);
+    if (M > 0 && cdiv(V, tc::PBN) >= 8) return launch_sharea<EpiLM, 4, 4, tc::PBN>(c, A, M, M_dev, W, V, d, e, st);
+    return run_tc(c, A, M, M_dev ? 0 : M, M_dev, W, V, d, e, st);
   }
-  return run_simt<4>(A, M, M, nullptr, W, V, d, e, st);
+  return run_simt<4>(A, M, M_dev ? 0 : M, M_dev, W, V, d, e, st);
 }
 
 }  // namespace dllm

@@ -48,6 +48,10 @@ struct dllm_cache {
   float* fa_state = nullptr;  // [B][H][64][head_dim + 4]: O~, m (log2 domain), l
   int* fa_key = nullptr;      // [B][H][66]: block start, block length, token-at-write of the queries
   int* fa_rebuilt = nullptr;  // (sequence, head) states rebuilt since the last reset
+  // early block exit: sequences whose block has ended, and the row count of
+  // W_o and the LM head (B * block_len, or 0 once every sequence has ended)
+  uint8_t* seq_done = nullptr;  // [B]
+  int* m_live = nullptr;        // [1]
   // measurement hook: events bracketing a kernel (index = dllm_prof_kernel)
   cudaEvent_t prof_begin[8] = {};
   cudaEvent_t prof_end[8] = {};
@@ -79,6 +83,9 @@ struct ProfScope {
   }
 };
 
+// Early block exit: the ended-sequence flags, or null when it is off.
+inline const uint8_t* done_flags(const dllm_cache* c) { return c->cfg.early_exit ? c->seq_done : nullptr; }
+
 // Refresh-set flag words that gate K/V writes: with active queries the row
 // list of a step also holds query-only rows (dense mode only).
 inline const uint32_t* kv_gate(const dllm_cache* c) {
@@ -92,15 +99,18 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t o
 // gemm_launch.cu -----------------------------------------------------------
 // bf16 or fp32 D = A . B^T with the named epilogue.  M: host rows, or the
 // device count M_dev (then M_cap bounds the grid and A's row extent).
+// stage (streaming pre-projection): rows row0 .. row0 + M_cap - 1 go to the
+// row-major staging buffer instead of the cache
 cudaError_t gemm_qkv(dllm_cache* c, int layer, const void* A, int M_cap, const int* M_dev, const int* rows,
-                     const void* w_qkv, cudaStream_t st);
+                     const void* w_qkv, cudaStream_t st, void* stage = nullptr, int row0 = 0);
 cudaError_t gemm_resid(dllm_cache* c, const void* A, const void* W, int M, int M_cap, const int* M_dev, int N,
                        int K, const void* xres, const int* tok, const void* embed, int q_start, int q_len,
                        void* out, cudaStream_t st);
 cudaError_t gemm_gelu(dllm_cache* c, const void* A, const void* W, int M, int M_cap, const int* M_dev, int N,
                       int K, const float* rs, void* out, cudaStream_t st);
-cudaError_t gemm_lm(dllm_cache* c, const void* A, const void* W, int M, int V, int d, const float* rs,
-                    int mask_id, void* part, int n_tiles, cudaStream_t st);
+// M_dev (may be null): 0 skips every row, else M rows
+cudaError_t gemm_lm(dllm_cache* c, const void* A, const void* W, int M, const int* M_dev, int V, int d,
+                    const float* rs, int mask_id, void* part, int n_tiles, cudaStream_t st);
 int lm_tile_cols(const dllm_cache* c, int M, int V);
 
 // attn.cu ------------------------------------------------------------------
@@ -141,6 +151,7 @@ cudaError_t attn_rows_dense(dllm_cache* c, int layer, const int* rows, const int
                             cudaStream_t st);
 cudaError_t launch_active_rows(dllm_cache* c, const void* src, const int* rows, const int* n_rows, int q_start,
                                int q_len, void* dst, cudaStream_t st);
+// (the active rows of an ended sequence are skipped without an error)
 cudaError_t attn_dense(dllm_cache* c, int layer, int q_pos0, int q_len, int kv_len, int n_seq, void* out,
                        cudaStream_t st);
 // Layer-0 attention of the active block with the kept state of the
@@ -149,12 +160,15 @@ cudaError_t attn_facache(dllm_cache* c, int q_pos0, int q_len, void* out, cudaSt
 
 // misc.cu ------------------------------------------------------------------
 cudaError_t launch_gather(dllm_cache* c, int layer, const int* rows, const int* n_rows, int n_host,
-                          const void* x, const int* tok, const void* embed, int t, cudaStream_t st);
+                          const void* x, const int* tok, const void* embed, int t, cudaStream_t st, int row0 = 0);
+// Copy stream tokens n0 .. n0 + count - 1 from a row-major staging buffer
+// [n][3d] into their ring slots of `layer`.
+cudaError_t launch_ring_append(dllm_cache* c, int layer, const void* staged, int n0, int count, cudaStream_t st);
 cudaError_t launch_rownorm(dllm_cache* c, const void* h, int M, const int* M_dev, int d, float* rs,
                            cudaStream_t st);
 // fail_word: see lm_merge_kernel (null: always merge)
-cudaError_t launch_lm_merge(const void* part, int M, int n_tiles, int* argmax, float* p1, float* ent,
-                            const unsigned* fail_word, cudaStream_t st);
+cudaError_t launch_lm_merge(const void* part, int M, const int* M_dev, int n_tiles, int* argmax, float* p1,
+                            float* ent, const unsigned* fail_word, cudaStream_t st);
 // R: dilation radius of the next step's refresh set; full: the next step
 // refreshes every row (the schedules of stab_update)
 // ent: the active rows' entropies with the confidence criterion, else null

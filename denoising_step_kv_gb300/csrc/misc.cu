@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const int* __restrict__ row
                                                      float* __restrict__ rs, int* __restrict__ tok_w,
                                                      int* __restrict__ version, int t, int d, int rows_cap,
                                                      int max_pos, int streaming, int vocab, float eps, int x_cap,
-                                                     const uint32_t* __restrict__ gate, int L, int Lw,
+                                                     const uint32_t* __restrict__ gate, int L, int Lw, int row0,
                                                      unsigned* err) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * 8 + warp;
@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const int* __restrict__ row
     n = x_cap;
   }
   if (i >= n) return;
-  const int row = rows ? rows[i] : i;
+  const int row = rows ? rows[i] : row0 + i;
   const bool row_ok = streaming ? (row >= 0 && row < max_pos) : (row >= 0 && row < rows_cap);
   if (!row_ok) {
     if (lane == 0) {
@@ -134,15 +134,16 @@ __global__ void __launch_bounds__(256) rownorm_kernel(const T* __restrict__ h, i
 // row gets argmax -1 and NaN probability and entropy instead.
 constexpr int MERGE_THREADS = 128;
 __global__ void __launch_bounds__(MERGE_THREADS) lm_merge_kernel(const LMPart* __restrict__ part, int M,
-                                                                 int n_tiles, int* __restrict__ argmax,
-                                                                 float* __restrict__ p1, float* __restrict__ ent,
+                                                                 const int* __restrict__ M_dev, int n_tiles,
+                                                                 int* __restrict__ argmax, float* __restrict__ p1,
+                                                                 float* __restrict__ ent,
                                                                  const unsigned* __restrict__ fail_word) {
   __shared__ float s_m[MERGE_THREADS / 32], s_s[MERGE_THREADS / 32], s_a[MERGE_THREADS / 32];
   __shared__ int s_i[MERGE_THREADS / 32];
   const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_launch();
   pdl_wait();
-  if (i >= M) return;
+  if (i >= M || (M_dev && i >= *M_dev)) return;
   if (fail_word && *fail_word != 0u) {
     if (tid == 0) {
       argmax[i] = -1;
@@ -178,7 +179,8 @@ __global__ void __launch_bounds__(MERGE_THREADS) lm_merge_kernel(const LMPart* _
 }
 
 __device__ void compact_words(const uint32_t* __restrict__ words, int nw, int L, int Lw, int q0, int nac,
-                              int* __restrict__ rows, int* __restrict__ n_rows);
+                              const uint8_t* __restrict__ seq_done, int* __restrict__ rows,
+                              int* __restrict__ n_rows);
 
 // Stable-Window-Decoding update of the active block of sequence blockIdx.x,
 // then one flag bit per position for the next step's refresh set.
@@ -195,8 +197,10 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
     uint8_t* __restrict__ stable, int* __restrict__ hist_tok, float* __restrict__ hist_p, int* __restrict__ hist_n,
     const int* __restrict__ tok_w, const int* __restrict__ version, uint32_t* __restrict__ words, int L, int Lw,
     int seq_rows, int n_layers, int blk, int K, float tau, int R, int q0, int t, int last, int full, int expiry,
-    int active_queries, unsigned* __restrict__ ticket, int* __restrict__ rows, int* __restrict__ n_rows) {
+    int active_queries, uint8_t* __restrict__ seq_done, int* __restrict__ m_live, unsigned* __restrict__ ticket,
+    int* __restrict__ rows, int* __restrict__ n_rows) {
   __shared__ uint8_t s_unst[64];
+  __shared__ uint8_t s_open[64];     // unstable after this update
   __shared__ int s_last;
   const int b = blockIdx.x;
   pdl_launch();
@@ -263,6 +267,7 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
       if (!st) tok[r] = a;
       hist_n[h] = 0;
     }
+    s_open[j] = st ? 0 : 1;
     bool flag = !st;
     if (ent && flag) {   // cache confidence at step t + 1 of this row's layer-0 entry
       const float age = static_cast<float>(t + 1 - version[r]);
@@ -271,13 +276,18 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
     }
     s_unst[j] = flag ? 1 : 0;
   }
-  __syncthreads();
+  // early exit: every active row stable after a step that is not the
+  // block's last ends this sequence's block (no refresh from now on)
+  const int n_open = __syncthreads_count(threadIdx.x < nac && s_open[threadIdx.x]);
+  const bool ended = seq_done && !last && n_open == 0;
   for (int base = 0; base < L; base += blockDim.x) {
     const int p = base + threadIdx.x;
     bool f = false;
     if (p < L) {
       const int r = b * L + p;
-      if (last || full) {
+      if (ended) {
+        f = false;
+      } else if (last || full) {
         f = true;
       } else {
         // independent loads (no short-circuit between them): any layer's
@@ -296,6 +306,7 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
     const int w = (base + (threadIdx.x & ~31)) >> 5;
     if ((threadIdx.x & 31) == 0 && w < Lw) words[b * Lw + w] = word;
   }
+  if (seq_done && threadIdx.x == 0) seq_done[b] = ended ? 1 : 0;
   // the last sequence block to finish compacts every sequence's flags
   __threadfence();
   __syncthreads();
@@ -303,8 +314,16 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // the row list: the refresh set, plus every active row when they all query
-  compact_words(words, gridDim.x * Lw, L, Lw, q0, active_queries && !last && !full ? nac : 0, rows, n_rows);
+  // the row list: the refresh set, plus the active rows of the running
+  // sequences when they all query
+  compact_words(words, gridDim.x * Lw, L, Lw, q0, active_queries && !last && !full ? nac : 0, seq_done, rows,
+                n_rows);
+  if (seq_done) {   // W_o and the LM head run while any sequence's block runs
+    int open = 0;
+    for (int i = threadIdx.x; i < gridDim.x; i += blockDim.x) open |= seq_done[i] == 0;
+    open = __syncthreads_or(open);
+    if (threadIdx.x == 0) *m_live = open ? gridDim.x * blk : 0;
+  }
   if (threadIdx.x == 0) *ticket = 0u;
 }
 
@@ -322,7 +341,8 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi) {
 // per-word popcounts, one word per thread per pass).  Run by one whole block
 // of blockDim.x (a multiple of 32, <= 1024) threads.
 __device__ void compact_words(const uint32_t* __restrict__ words, int nw, int L, int Lw, int q0, int nac,
-                              int* __restrict__ rows, int* __restrict__ n_rows) {
+                              const uint8_t* __restrict__ seq_done, int* __restrict__ rows,
+                              int* __restrict__ n_rows) {
   __shared__ int s_warp[32];
   __shared__ int s_base;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -330,7 +350,11 @@ __device__ void compact_words(const uint32_t* __restrict__ words, int nw, int L,
   __syncthreads();
   for (int base = 0; base < nw; base += blockDim.x) {
     const int w = base + tid;
-    uint32_t word = w < nw ? words[w] | range_bits(q0 - (w % Lw) * 32, q0 + nac - (w % Lw) * 32) : 0u;
+    uint32_t word = 0u;
+    if (w < nw) {
+      const bool run = !seq_done || !seq_done[w / Lw];      // an ended sequence adds no active rows
+      word = words[w] | (run ? range_bits(q0 - (w % Lw) * 32, q0 + nac - (w % Lw) * 32) : 0u);
+    }
     const int cnt = __popc(word);
     int incl = cnt;
 #pragma unroll
@@ -376,7 +400,7 @@ __global__ void __launch_bounds__(256) all_rows_kernel(int* __restrict__ rows, i
 }
 
 __global__ void reset_kernel(int* version, int n_version, int* tok_w, uint8_t* stable, int n_rows, int* hist_n,
-                             int n_hist, unsigned* err) {
+                             int n_hist, int* m_live, unsigned* err) {
   const int i0 = blockIdx.x * blockDim.x + threadIdx.x, step = gridDim.x * blockDim.x;
   for (int i = i0; i < n_version; i += step) version[i] = NEVER;
   for (int i = i0; i < n_rows; i += step) {
@@ -384,7 +408,10 @@ __global__ void reset_kernel(int* version, int n_version, int* tok_w, uint8_t* s
     stable[i] = 0;
   }
   for (int i = i0; i < n_hist; i += step) hist_n[i] = 0;
-  if (i0 == 0) *err = 0u;
+  if (i0 == 0) {
+    *err = 0u;
+    if (m_live) *m_live = n_hist;     // every active row of every sequence
+  }
 }
 
 // Active-block rows out of a compact row-list buffer: dst[b * q_len + j] =
@@ -394,12 +421,14 @@ __global__ void reset_kernel(int* version, int n_version, int* tok_w, uint8_t* s
 __global__ void __launch_bounds__(256) active_rows_kernel(const uint4* __restrict__ src, const int* __restrict__ rows,
                                                           const int* __restrict__ n_rows, int cap, int L,
                                                           int q_start, int q_len, int n_out, int row_vec,
+                                                          const uint8_t* __restrict__ seq_done,
                                                           uint4* __restrict__ dst, unsigned* err) {
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   pdl_launch();
   pdl_wait();
   if (w >= n_out) return;
   const int b = w / q_len, j = w - b * q_len;
+  if (seq_done && seq_done[b]) return;       // an ended sequence's rows are not in the list
   const int key = b * L + q_start + j;
   const int n = min(*n_rows, cap);
   int lo = 0, hi = n;
@@ -435,7 +464,41 @@ __global__ void __launch_bounds__(128) wait_selftest_kernel(uint64_t limit_ns, u
   __syncthreads();
 }
 
+// One warp per (token, part q/k/v, head): the head's dh values of the
+// token's staging row (row-major [n][3d], RoPE applied) into the ring slot of
+// the layer's tiled cache, 16 bytes per lane.
+__global__ void __launch_bounds__(256) ring_append_kernel(const uint8_t* __restrict__ staged, uint8_t* __restrict__ q,
+                                                          uint8_t* __restrict__ k, uint8_t* __restrict__ v,
+                                                          KvLayout kv, int n0, int count, int H, int row_bytes,
+                                                          int S, int W, int max_pos, unsigned* err) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  pdl_launch();
+  pdl_wait();
+  if (w >= count * 3 * H) return;
+  const int i = w / (3 * H), part = (w / H) % 3, h = w % H;
+  const int n = n0 + i;
+  if (n < 0 || n >= max_pos) {
+    if (lane == 0 && part == 0 && h == 0) set_err(err, DLLM_ERR_ROW);
+    return;
+  }
+  const int slot = ring_slot(n, S, W);
+  const uint8_t* src = staged + (static_cast<size_t>(n) * 3 * H + part * H + h) * row_bytes;
+  uint8_t* base = part == 0 ? q : part == 1 ? k : v;
+  for (int c = lane; c < row_bytes / 16; c += 32)
+    *reinterpret_cast<uint4*>(base + kv.chunk_off(0, h, slot, c)) = *reinterpret_cast<const uint4*>(src + c * 16);
+}
+
 }  // namespace
+
+cudaError_t launch_ring_append(dllm_cache* c, int layer, const void* staged, int n0, int count, cudaStream_t st) {
+  if (count <= 0) return cudaSuccess;
+  const size_t off = static_cast<size_t>(layer) * c->kv_layer_bytes;
+  const int H = c->cfg.n_heads, warps = count * 3 * H;
+  return launch_ex(ring_append_kernel, dim3(cdiv(warps * 32, 256)), dim3(256), 0, st, 0,
+                   static_cast<const uint8_t*>(staged), static_cast<uint8_t*>(c->q) + off,
+                   static_cast<uint8_t*>(c->k) + off, static_cast<uint8_t*>(c->v) + off, c->kv, n0, count, H,
+                   c->kv.row_bytes, c->cfg.sink, c->cfg.window, c->max_pos, c->err);
+}
 
 cudaError_t launch_wait_selftest(dllm_cache* c, uint64_t limit_ns, cudaStream_t st) {
   wait_selftest_kernel<<<1, 128, 0, st>>>(limit_ns, c->err);
@@ -449,11 +512,11 @@ cudaError_t launch_active_rows(dllm_cache* c, const void* src, const int* rows, 
   const int row_vec = c->d * c->elem / 16;
   return launch_ex(active_rows_kernel, dim3(cdiv(n_out * 32, 256)), dim3(256), 0, st, 0,
                    static_cast<const uint4*>(src), rows, n_rows, c->seq_rows, c->cfg.seq_len, q_start, q_len, n_out,
-                   row_vec, static_cast<uint4*>(dst), c->err);
+                   row_vec, done_flags(c), static_cast<uint4*>(dst), c->err);
 }
 
 cudaError_t launch_gather(dllm_cache* c, int layer, const int* rows, const int* n_rows, int n_host, const void* x,
-                          const int* tok, const void* embed, int t, cudaStream_t st) {
+                          const int* tok, const void* embed, int t, cudaStream_t st, int row0) {
   const bool dense = c->cfg.sink == 0;
   const int cap = rows ? c->seq_rows : n_host;    // rows of the compact buffers
   if (cap <= 0) return cudaSuccess;
@@ -467,11 +530,12 @@ cudaError_t launch_gather(dllm_cache* c, int layer, const int* rows, const int* 
   if (c->cfg.dtype == DLLM_BF16)
     return launch_ex(gather_kernel<bf16>, grid, dim3(256), 0, st, 0, rows, nr, n_host, static_cast<const bf16*>(x), tok,
                      static_cast<const bf16*>(embed), static_cast<bf16*>(c->X), c->rs, tok_w, version, t, c->d,
-                     c->rows, c->max_pos, streaming, c->cfg.vocab, c->cfg.rms_eps, c->seq_rows, gate, L, c->Lw,
+                     c->rows, c->max_pos, streaming, c->cfg.vocab, c->cfg.rms_eps, c->seq_rows, gate, L, c->Lw, row0,
                      c->err);
   return launch_ex(gather_kernel<float>, grid, dim3(256), 0, st, 0, rows, nr, n_host, static_cast<const float*>(x), tok,
                    static_cast<const float*>(embed), static_cast<float*>(c->X), c->rs, tok_w, version, t, c->d,
-                   c->rows, c->max_pos, streaming, c->cfg.vocab, c->cfg.rms_eps, c->seq_rows, gate, L, c->Lw, c->err);
+                   c->rows, c->max_pos, streaming, c->cfg.vocab, c->cfg.rms_eps, c->seq_rows, gate, L, c->Lw, row0,
+                   c->err);
 }
 
 cudaError_t launch_rownorm(dllm_cache* c, const void* h, int M, const int* M_dev, int d, float* rs,
@@ -484,11 +548,11 @@ cudaError_t launch_rownorm(dllm_cache* c, const void* h, int M, const int* M_dev
                    M_dev, d, c->cfg.rms_eps, rs);
 }
 
-cudaError_t launch_lm_merge(const void* part, int M, int n_tiles, int* argmax, float* p1, float* ent,
-                            const unsigned* fail_word, cudaStream_t st) {
+cudaError_t launch_lm_merge(const void* part, int M, const int* M_dev, int n_tiles, int* argmax, float* p1,
+                            float* ent, const unsigned* fail_word, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
   return launch_ex(lm_merge_kernel, dim3(M), dim3(MERGE_THREADS), 0, st, 0, static_cast<const LMPart*>(part), M,
-                   n_tiles, argmax, p1, ent, fail_word);
+                   M_dev, n_tiles, argmax, p1, ent, fail_word);
 }
 
 cudaError_t launch_stab(dllm_cache* c, const int* argmax, const float* p1, const float* ent, int* tok, int q_start,
@@ -496,9 +560,11 @@ cudaError_t launch_stab(dllm_cache* c, const int* argmax, const float* p1, const
   const dllm_cache_cfg& g = c->cfg;
   const ConfGate cg{g.conf_alpha, g.conf_beta, g.conf_lambda, g.conf_theta,
                     static_cast<float>(std::log(static_cast<double>(g.vocab - 1)))};
+  uint8_t* done = g.early_exit ? c->seq_done : nullptr;
   return launch_ex(swd_kernel, dim3(g.batch), dim3(1024), 0, st, 0, argmax, p1, ent, cg, tok, c->stable, c->hist_tok, c->hist_p,
                    c->hist_n, c->tok_w, c->version, c->words, g.seq_len, c->Lw, c->seq_rows, g.n_layers, g.block_len,
-                   g.swd_K, g.swd_tau, R, q_start, t, last, full, g.expiry, g.active_queries, c->ticket, rows,
+                   g.swd_K, g.swd_tau, R, q_start, t, last, full, g.expiry, g.active_queries, done, c->m_live,
+                   c->ticket, rows,
                    n_rows);
 }
 
@@ -511,6 +577,10 @@ cudaError_t launch_refresh_all(dllm_cache* c, int q_start, int* rows, int* n_row
 
 cudaError_t launch_reset(dllm_cache* c, cudaStream_t st) {
   const dllm_cache_cfg& g = c->cfg;
+  if (c->seq_done) {   // no block has ended (W_o and the LM head count: reset_kernel)
+    cudaError_t e = cudaMemsetAsync(c->seq_done, 0, static_cast<size_t>(g.batch), st);
+    if (e != cudaSuccess) return e;
+  }
   {  // until a refresh set is built, every row may write its K/V (the gate of active queries)
     cudaError_t e = cudaMemsetAsync(c->words, 0xff, static_cast<size_t>(g.batch) * c->Lw * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
@@ -523,7 +593,7 @@ cudaError_t launch_reset(dllm_cache* c, cudaStream_t st) {
   const int nv = g.n_layers * c->seq_rows;
   const int nh = g.batch * g.block_len;
   reset_kernel<<<std::max(1, std::min(cdiv(std::max(nv, c->seq_rows), 256), 1024)), 256, 0, st>>>(
-      c->version, nv, c->tok_w, c->stable, c->seq_rows, c->hist_n, nh, c->err);
+      c->version, nv, c->tok_w, c->stable, c->seq_rows, c->hist_n, nh, c->m_live, c->err);
   return cudaGetLastError();
 }
 

@@ -100,8 +100,9 @@ extern "C" dllm_status lmhead_conf_noalloc(const void* h_dev, const void* w_lm_d
   // the merge then writes argmax -1 and NaN instead of stale results.
   if ((e = cudaMemsetAsync(ctx.err, 0, sizeof(unsigned), st)) != cudaSuccess ||
       (e = launch_rownorm(&ctx, h_dev, M, nullptr, d, rs, st)) != cudaSuccess ||
-      (e = gemm_lm(&ctx, h_dev, w_lm_dev, M, V, d, rs, mask_id, scratch, n_tiles, st)) != cudaSuccess ||
-      (e = launch_lm_merge(scratch, M, n_tiles, argmax_dev, p_top1_dev, entropy_dev, ctx.err, st)) != cudaSuccess)
+      (e = gemm_lm(&ctx, h_dev, w_lm_dev, M, nullptr, V, d, rs, mask_id, scratch, n_tiles, st)) != cudaSuccess ||
+      (e = launch_lm_merge(scratch, M, nullptr, n_tiles, argmax_dev, p_top1_dev, entropy_dev, ctx.err, st)) !=
+          cudaSuccess)
     return na_fail(DLLM_ECUDA, std::string("lmhead_conf_noalloc: ") + cudaGetErrorString(e));
   return DLLM_OK;
 }

@@ -266,14 +266,20 @@ class StreamGenerator:
     n (sinks keep slots 0..S-1, later tokens cycle through the W rolling
     slots, RoPE at the absolute stream index), then its query attends over
     the min(n + 1, S + W) entries the cache holds.  O_n lands in out[n].
+    preproject: every token's row is projected up front in one pass
+    (kv_project) and each step only copies it into its slot (ring_append);
+    otherwise each step projects its own row (kv_refresh of one row, which
+    streams the whole projection weight).
     """
 
-    def __init__(self, w, weights, device="cuda"):
+    def __init__(self, w, weights, device="cuda", preproject=True):
         assert w.streaming and w.n_layers == 1
         self.w = w
         self.W = weights
+        self.preproject = preproject
         dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
         self.cache = K.dllm_cache_init(K.make_cfg(w))
+        self.staged = torch.empty(w.stream_len if preproject else 0, 3 * w.d_model, dtype=dt, device=device)
         i32 = dict(dtype=torch.int32, device=device)
         self.pos = torch.arange(w.stream_len, **i32)      # row list: token n is row n
         self.one = torch.ones(1, **i32)
@@ -294,7 +300,10 @@ class StreamGenerator:
 
     def step(self, n, stream=None):
         c, W = self.cache, self.W
-        K.kv_refresh(c, 0, None, self.tok, W["embed"], W["w_qkv"][0], self.pos[n:n + 1], self.one, n, stream)
+        if self.preproject:
+            K.ring_append(c, 0, self.staged, n, 1, stream)
+        else:
+            K.kv_refresh(c, 0, None, self.tok, W["embed"], W["w_qkv"][0], self.pos[n:n + 1], self.one, n, stream)
         K.block_attn(c, 0, n, 1, self.out[n:n + 1], stream)
 
     def make_prof_events(self, kernels, n0, n1):
@@ -313,8 +322,11 @@ class StreamGenerator:
         """Run the stream; prof (from make_prof_events(kernels, prof_from, ..))
         brackets both kernels of tokens prof_from onwards."""
         K.dllm_cache_reset(self.cache, stream)
+        n_tok = self.w.stream_len if n_tokens is None else n_tokens
+        if self.preproject:
+            K.kv_project(self.cache, 0, self.tok, self.W["embed"], self.W["w_qkv"][0], n_tok, self.staged, stream)
         n_prof = len(next(iter(prof.values()))) if prof else 0
-        for n in range(self.w.stream_len if n_tokens is None else n_tokens):
+        for n in range(n_tok):
             on = prof_from <= n < prof_from + n_prof
             if on:
                 for k, pairs in prof.items():

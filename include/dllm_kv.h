@@ -119,6 +119,13 @@ typedef struct {
                         conf_theta ("I/O-aware KV cache and self-verifying
                         parallel decoding" 3.1); fp32, in that order */
   float conf_alpha, conf_beta, conf_lambda, conf_theta;
+  int early_exit;    /* 1: a sequence whose active rows are all stable after
+                        a step (not its block's last) ends its block: the
+                        block's later steps refresh none of its rows and skip
+                        its attention, and when every sequence has ended,
+                        W_o and the LM head too ("Stable Window Decoding" 3.2,
+                        4.2: "compute all or end"); its argmax, top-1
+                        probability and entropy are then unspecified */
   int facache;       /* 1: block_attn keeps the online-softmax state of the
                         key tiles outside the block's window and reuses it
                         while the block and its query tokens are unchanged
@@ -165,8 +172,10 @@ typedef enum {
   DLLM_FIELD_HIST_TOK = 6,  /* int32 [B][block_len][swd_K] ring of top-1 ids */
   DLLM_FIELD_HIST_P = 7,    /* float [B][block_len][swd_K] ring of top-1 probs */
   DLLM_FIELD_HIST_N = 8,    /* int32 [B][block_len] records pushed this block */
-  DLLM_FIELD_FA_REBUILT = 9 /* int32 [1]: (sequence, head) attention states
+  DLLM_FIELD_FA_REBUILT = 9, /* int32 [1]: (sequence, head) attention states
                                rebuilt since the last reset (facache) */
+  DLLM_FIELD_SEQ_DONE = 10  /* uint8 [B]: sequences whose block has ended
+                               (early_exit) */
 } dllm_field;
 
 /* Blocking copy of one state field between the handle and HOST memory
@@ -204,6 +213,23 @@ dllm_status refresh_all(dllm_cache* c, int q_start, int32_t* rows_dev, int32_t* 
 dllm_status kv_refresh(dllm_cache* c, int layer, const void* x_dev, const int32_t* tok_dev,
                        const void* embed_dev, const void* w_qkv_dev, const int32_t* rows_dev,
                        const int32_t* n_rows_dev, int t, void* stream);
+
+/* Streaming pre-projection ("Attention Sinks and Where to Cache Them" 3.3:
+   a token's entry depends only on its token and its absolute position, so
+   the layer's Q/K/V of every stream token can be projected at once):
+   stream tokens 0 .. n-1 (tok_dev[i], position i) -> embedding, RMSNorm,
+   [q k v] = x W_qkv^T, RoPE at position i, stored row-major into
+   staged_dev [n][3 * d] (q | k | v, heads contiguous) in the cache dtype,
+   caller-owned.  Streaming caches only; n <= max_pos.  Asynchronous. */
+dllm_status kv_project(dllm_cache* c, int layer, const int32_t* tok_dev, const void* embed_dev,
+                       const void* w_qkv_dev, int n, void* staged_dev, void* stream);
+
+/* Stream tokens n0 .. n0 + count - 1 join the sink + rolling cache: their
+   staged rows (row n of staged_dev, as kv_project writes them) are copied
+   into ring slot n (n < S) or S + (n - S) mod W of `layer`, in order.  A
+   call takes at most W tokens (a later token may reuse an earlier one's
+   slot).  Asynchronous on `stream`. */
+dllm_status ring_append(dllm_cache* c, int layer, const void* staged_dev, int n0, int count, void* stream);
 
 /* Bidirectional attention of cached queries over the cached sequence
    ("LaCache", Problem statement: a block's tokens are updated together over

@@ -15,10 +15,10 @@ from workloads import generate as G
 pytestmark = pytest.mark.gpu
 
 
-def _run(w, n_tokens=None):
+def _run(w, n_tokens=None, preproject=True):
     m = G.model(w)
     stream = G.stream_tokens(w)
-    gen = loop.StreamGenerator(w, {k: loop.to_device(v) for k, v in m.items()})
+    gen = loop.StreamGenerator(w, {k: loop.to_device(v) for k, v in m.items()}, preproject=preproject)
     try:
         gen.tok.copy_(torch.from_numpy(stream))
         out = gen.run(n_tokens).float().cpu().numpy()
@@ -33,10 +33,13 @@ def _slot(p, S, W):
     return p if p < S else S + (p - S) % W
 
 
+@pytest.mark.parametrize("preproject", [True, False])
 @pytest.mark.parametrize("name", ["tiny_sink_f32", "mid_sink"])
-def test_stream_every_token(name):
+def test_stream_every_token(name, preproject):
+    """Each token's row projected up front and copied into its slot, or
+    projected by its own step."""
     w = C.get(name)
-    m, stream, out, ring = _run(w)
+    m, stream, out, ring = _run(w, preproject=preproject)
     W64 = O.weights_f64(w, m)
     ref, held = O.run_stream(w, W64, stream)
     for n in range(w.stream_len):
