@@ -488,7 +488,7 @@ dllm_status lmhead_conf(dllm_cache* c, const void* h_dev, const void* w_lm_dev, 
   if (!aligned16(h_dev) || !aligned16(w_lm_dev)) return fail(DLLM_EINVAL, "lmhead_conf: pointers not 16-byte aligned");
   if (M == 0) return DLLM_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int n_tiles = cdiv(V, lm_tile_cols(c, M, V));
+  const int n_tiles = lm_slots(c, M, V);
   // with early exit, a device count: 0 once every sequence has ended its block
   const int* M_dev = (c->cfg.early_exit && c->m_live && M == c->lm_rows_cap) ? c->m_live : nullptr;
   DLLM_LAUNCH(launch_rownorm(c, h_dev, M, M_dev, d, c->lm_rs, st), "lmhead_conf: norm");

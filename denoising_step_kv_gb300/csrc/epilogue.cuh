@@ -330,6 +330,12 @@ struct EpiLM {
 
   template <class LD>
   __device__ __forceinline__ void run(int m, int n0, int nch, int M, int N, const LD& ld) const {
+    run_slot(m, n0, nch, n0 / (32 * nch), M, N, ld);
+  }
+
+  // statistics of columns [n0, n0 + 32 nch) of row m into partial `slot`
+  template <class LD>
+  __device__ __forceinline__ void run_slot(int m, int n0, int nch, int slot, int M, int N, const LD& ld) const {
     const bool ok = m < M;
     const float sc = ok ? rs[m] : 0.f;
     float mx = -INFINITY, S = 0.f, A = 0.f;
@@ -362,7 +368,7 @@ struct EpiLM {
       }
       lm_merge(mx, S, A, idx, cm, cs, ca, ci);
     }
-    if (ok) part[static_cast<size_t>(m) * n_tiles + n0 / (32 * nch)] = LMPart{mx, S, A, idx};
+    if (ok) part[static_cast<size_t>(m) * n_tiles + slot] = LMPart{mx, S, A, idx};
   }
 
   __device__ __forceinline__ void prefetch(int, int, int, int) const {}

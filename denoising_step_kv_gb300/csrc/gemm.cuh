@@ -520,56 +520,310 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// Weight-streaming GEMM for small M (at most 256 rows): D^T = B . A^T.  The
-// weights B [N][K] are the MMA's A operand (128 output columns per CTA, on
-// the TMEM lanes) and the rows A [M][K] its B operand (M rounded up to 16, on
-// the TMEM columns), so every weight byte is read from HBM once and no MMA
-// work goes to padding rows.  A cluster of SPLITK CTAs splits K.  Rank r owns
-// rows [r * tpr, (r + 1) * tpr) of the tile: after every rank's MMAs are done
-// (cluster barrier), each rank pushes its fp32 partial of those rows into the
-// owner's shared memory (16-byte remote stores, no round trips), and after
-// a second barrier the owner sums the SPLITK partials (rank order) while
-// running the epilogue, spread over (row, piece) items.  The epilogue warps
-// warm L2 with the epilogue's side data while the MMAs run.  The stage ring holds as many
-// stages as fit for this M (rows are loaded in 64-row boxes, only as needed).
-constexpr int SKN_MAX_ROWS = 256;
+// LM head for 128 < M <= 256 rows and a large vocabulary: clusters of two
+// CTAs, one per SM.  Each CTA owns a contiguous range of vocabulary columns
+// and computes all M rows of it (two 128-row accumulators, TMEM columns
+// [0, 256) and [256, 512)), in chunks of up to 256 columns whose widths
+// (multiples of 32) are the same in every CTA.  The two CTAs of a cluster run
+// their chunks in lockstep, so each loads one 128-row half of the rows'
+// k-block and multicasts it into both: a k-block lands 32 KB of rows and at
+// most 32 KB of weights per SM for 2 x 128 rows of MMA work (the pair kernel
+// lands 48 KB per 128 rows), and the rows are read from L2 once per cluster.
+// The weight chunk is loaded in 32-row boxes.  Before the grid dependency
+// each CTA loads the weights of its first LW_STAGES k-blocks (no earlier
+// kernel writes them).  Every MMA commit arrives on both CTAs' empty barriers:
+// a stage is reloaded only once both have read it.  The epilogue releases the
+// first accumulator before it reads the second, so the next chunk's first
+// MMAs overlap it.  Each chunk's statistics go to partial slot
+// cta * n_chunks + chunk.
+constexpr int LW_STAGES = 3;
+constexpr int LW_BOX = 32;                               // weight rows per load
+constexpr int LW_A_BYTES = 2 * A_BYTES;                  // 256 rows x 64
+constexpr int LW_STAGE = LW_A_BYTES + 256 * BK * 2;      // + up to 256 weight rows
+struct LwBars {
+  uint64_t full[LW_STAGES];
+  uint64_t empty[LW_STAGES];
+  uint64_t tfull;
+  uint64_t tempty[2];
+  uint64_t done;
+  uint32_t tmem;
+  int abort;
+};
+constexpr size_t LW_SMEM = 1024 + LW_STAGES * LW_STAGE + sizeof(LwBars);
+
+// 32-column units of chunk k when `units` are split into n_chunks widths
+// that differ by at most one unit; `first` is the chunk's first unit.
+__host__ __device__ __forceinline__ int lw_chunk(int units, int n_chunks, int k, int& first) {
+  const int base = units / n_chunks, extra = units % n_chunks;
+  first = k * base + min(k, extra);
+  return base + (k < extra ? 1 : 0);
+}
+
+template <class Epi>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_lmwide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       int M_host, const int* __restrict__ M_dev, int M_cap, int N, int K, int units,
+                       int n_chunks, Epi epi, unsigned* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  LwBars* bars = reinterpret_cast<LwBars*>(smem + LW_STAGES * LW_STAGE);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_rank());
+  const int col0 = blockIdx.x * units * 32;               // this CTA's first column
+  const int nK = (K + BK - 1) / BK;
+  const int n_early = min(nK, LW_STAGES);                 // chunk 0's first k-blocks
+  int u0_first;
+  const int u0 = lw_chunk(units, n_chunks, 0, u0_first);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < LW_STAGES; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 2);
+    }
+    mbar_init(&bars->tfull, 1);
+    mbar_init(&bars->tempty[0], 4);
+    mbar_init(&bars->tempty[1], 4);
+    mbar_init(&bars->done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&bars->tmem, 512);
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier();       // the peer's barriers exist before any multicast lands
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  volatile int* abort = &bars->abort;
+  // before the grid dependency: the weights only
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    for (int i = 0; i < n_early; ++i) {
+      mbar_expect_tx_only(&bars->full[i], u0 * LW_BOX * 128);
+      for (int j = 0; j < u0; ++j)
+        tma_load_2d(smem + i * LW_STAGE + LW_A_BYTES + j * (LW_BOX * 128), &tmB, i * BK, col0 + j * LW_BOX,
+                    &bars->full[i]);
+    }
+  }
+  pdl_launch();
+  pdl_wait();
+  const int M = M_dev ? min(*M_dev, M_cap) : M_host;
+  const int chunks = M > 0 ? n_chunks : 0;                 // the same in both CTAs
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0, i = 0;
+      uint32_t phase = 0, issued = 0, par = 0;
+      for (int k = 0; k < chunks && !*abort; ++k) {
+        int uf;
+        const int u = lw_chunk(units, n_chunks, k, uf);
+        const int n0 = col0 + uf * 32;
+        for (int kb = 0; kb < nK; ++kb, ++i) {
+          if (i >= n_early) {
+            if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort, err)) break;
+            mbar_expect_tx(&bars->full[stage], LW_A_BYTES + u * LW_BOX * 128);
+            for (int j = 0; j < u; ++j)
+              tma_load_2d(smem + stage * LW_STAGE + LW_A_BYTES + j * (LW_BOX * 128), &tmB, kb * BK,
+                          n0 + j * LW_BOX, &bars->full[stage]);
+          } else {
+            mbar_expect_tx(&bars->full[stage], LW_A_BYTES);   // its weight bytes are already expected
+          }
+          tma_load_2d_mc(smem + stage * LW_STAGE + rank * A_BYTES, &tmA, kb * BK, rank * BM, &bars->full[stage],
+                         0x3);
+          issued |= 1u << stage;
+          par = (par & ~(1u << stage)) | (phase << stage);
+          if (++stage == LW_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (chunks == 0 || *abort) {
+        for (int s = 0; s < LW_STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait(&bars->full[s], (par >> s) & 1u, nullptr, err);
+        for (int s = 0; s < n_early; ++s)      // early weight loads the loop never reached
+          if (!(issued & (1u << s))) {
+            mbar_arrive(&bars->full[s]);
+            mbar_wait(&bars->full[s], 0, nullptr, err);
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int k = 0; k < chunks && !*abort; ++k) {
+        int uf;
+        const int u = lw_chunk(units, n_chunks, k, uf);
+        const uint32_t idesc = idesc_bf16(BM, u * 32);
+        const uint32_t tpar = (static_cast<uint32_t>(k) & 1u) ^ 1u;   // the previous chunk's release
+        bool ok = mbar_wait(&bars->tempty[0], tpar, abort, err);
+        bool ok1 = false;                                               // second accumulator released
+        for (int kb = 0; kb < nK && ok; ++kb) {
+          if (!mbar_wait(&bars->full[stage], phase, abort, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + stage * LW_STAGE), b0 = a0 + LW_A_BYTES;
+#pragma unroll
+          for (int k16 = 0; k16 < BK / 16; ++k16)
+            tc_mma_bf16(tmem, sdesc_sw128(a0 + k16 * 32), sdesc_sw128(b0 + k16 * 32), idesc,
+                        (kb | k16) != 0 ? 1u : 0u);
+          if (!ok1) {
+            if (!mbar_wait(&bars->tempty[1], tpar, abort, err)) {
+              ok = false;
+              break;
+            }
+            ok1 = true;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int k16 = 0; k16 < BK / 16; ++k16)
+            tc_mma_bf16(tmem + 256, sdesc_sw128(a0 + A_BYTES + k16 * 32), sdesc_sw128(b0 + k16 * 32), idesc,
+                        (kb | k16) != 0 ? 1u : 0u);
+          tc_commit_mc(&bars->empty[stage], 0x3);
+          if (++stage == LW_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&bars->tfull);
+      }
+      // all MMAs (and the empty-barrier arrivals they owe the peer) complete
+      // before the cluster barrier below
+      tc_commit(&bars->done);
+      mbar_wait(&bars->done, 0, nullptr, err);
+    }
+  } else {
+    const int q = warp & 3;
+    const uint32_t lane_tm = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    for (int k = 0; k < chunks; ++k) {
+      int uf;
+      const int u = lw_chunk(units, n_chunks, k, uf);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&bars->tfull, static_cast<uint32_t>(k) & 1u, abort, err) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const int slot = blockIdx.x * n_chunks + k;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        TmemLoader ld{lane_tm + static_cast<uint32_t>(h * 256)};
+        epi.run_slot(h * BM + q * 32 + lane, col0 + uf * 32, u, slot, M, N, ld);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->tempty[h]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier();       // no multicast copy or commit still targets this CTA
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Weight-streaming GEMM for few rows: D^T = B . A^T.  The weights B [N][K]
+// are the MMA's A operand (128 output columns per CTA, on the TMEM lanes) and
+// the rows A [M][K] its B operand (on the TMEM columns: one MMA of N = M
+// rounded up to 16, or two past 256 rows), so every weight byte is read from
+// HBM once and no MMA work goes to padding rows.
+//
+// Before the grid dependency (the weights are no earlier kernel's output)
+// each CTA loads its first SKN_EARLY weight k-blocks into the stage ring and
+// asks L2 for the next ones; the rows and the device row count wait for the
+// dependency.  A stage holds a weight tile at a fixed offset and the rows'
+// tile (32-row boxes, only as many as M needs) after all weight tiles.
+//
+// A cluster of SPLITK CTAs splits K.  Rank r owns rows [r * tpr, (r + 1) *
+// tpr) (tpr a multiple of 32).  Once every rank's MMAs are done (cluster
+// barrier) each rank writes its fp32 partial of every other owner's rows
+// from TMEM into a local send block and hands the block to the owner with
+// one bulk shared::cluster copy that completes on the owner's receive
+// barrier; the owner adds the partials in rank order (its own from TMEM)
+// into its first receive block and runs the epilogue over (row, piece)
+// items.  Without a split the accumulator is staged through shared memory
+// 128 rows at a time.  Blocks are [128 columns][tpr rows] fp32 with each
+// column's 16-byte chunks rotated by the column index, so that a warp's
+// column-wise writes and its row-wise reads both spread over all banks.
+constexpr int SKN_MAX_ROWS = 512;                // without a split of K
+constexpr int SKN_SPLIT_ROWS = 256;              // with one
 constexpr int SKN_W_BYTES = 128 * BK * 2;        // 16 KB of weights per k-block
-constexpr int SKN_XBOX = 64;                     // rows per load of A
+constexpr int SKN_XBOX = 32;                     // rows per load of A
 constexpr int SKN_RING = 192 * 1024;
 constexpr int SKN_MAX_ST = 8;
+constexpr int SKN_EARLY = 2;                     // weight k-blocks loaded before the grid dependency
+constexpr int SKN_PF = 16;                       // weight k-blocks warmed in L2 before it
+constexpr int SKN_CHUNK = 128;                   // rows staged per pass without a split
+constexpr uint32_t SKN_TMEM_COLS = 512;
 struct SknBars {
   uint64_t full[SKN_MAX_ST];
   uint64_t empty[SKN_MAX_ST];
   uint64_t tfull;
+  uint64_t recv;
   uint32_t tmem;
   int abort;
 };
 constexpr size_t SKN_SMEM = 1024 + SKN_RING + sizeof(SknBars);
 
-// Rows per rank (a multiple of 4) and the row stride of the receive buffer
-// recv[rank][column][ldr], padded so that ldr / 4 is odd: a warp's 16-byte
-// pushes (a lane per column, four rows each) spread over all banks.
-__host__ __device__ constexpr int skn_tpr(int M, int S) { return ((M + S - 1) / S + 3) & ~3; }
-__host__ __device__ constexpr int skn_ldr(int tpr) { return (tpr / 4) % 2 ? tpr : tpr + 4; }
-static_assert(4 * 128 * skn_ldr(skn_tpr(SKN_MAX_ROWS, 4)) * 4 <= SKN_RING, "receive buffer fits in the ring");
-static_assert(3 * 128 * skn_ldr(skn_tpr(SKN_MAX_ROWS, 3)) * 4 <= SKN_RING, "receive buffer fits in the ring");
-static_assert(2 * 128 * skn_ldr(skn_tpr(SKN_MAX_ROWS, 2)) * 4 <= SKN_RING, "receive buffer fits in the ring");
+__host__ __device__ constexpr int skn_max_rows(int S) { return S == 1 ? SKN_MAX_ROWS : SKN_SPLIT_ROWS; }
+__host__ __device__ constexpr int skn_tpr(int M, int S) { return ((M + S - 1) / S + 31) & ~31; }
+// send and receive blocks of every other rank
+static_assert(2 * 3 * 128 * skn_tpr(SKN_SPLIT_ROWS, 4) * 4 <= SKN_RING, "exchange blocks fit in the ring");
+static_assert(2 * 2 * 128 * skn_tpr(SKN_SPLIT_ROWS, 3) * 4 <= SKN_RING, "exchange blocks fit in the ring");
+static_assert(2 * 1 * 128 * skn_tpr(SKN_SPLIT_ROWS, 2) * 4 <= SKN_RING, "exchange blocks fit in the ring");
+static_assert(128 * SKN_CHUNK * 4 <= SKN_RING, "a staged chunk fits in the ring");
+static_assert(SKN_RING / (SKN_W_BYTES + SKN_MAX_ROWS * 128) >= SKN_EARLY, "the early loads' stages exist for any M");
 
-// Columns [col, col + 32) of local row rr of the owner's tile: the sum, in
-// rank order, of the SPLITK partials pushed into recv.
-template <int SPLITK>
-struct RecvSumLoader {
-  const float* recv;
-  int ldr, rr;
+// Element (column f, row rr) of a [128][tpr] block: column f's 16-byte
+// chunks rotated by f mod 8 (tpr / 4 is a multiple of 8).
+__device__ __forceinline__ int skn_at(int f, int rr, int tpr) {
+  int c = (rr >> 2) + (f & 7);
+  if (c >= (tpr >> 2)) c -= tpr >> 2;
+  return f * tpr + (c << 2) + (rr & 3);
+}
+
+// Columns [col, col + 32) of row rr of a staged block (col a multiple of 32).
+struct SknLoader {
+  const float* blk;
+  int tpr, rr;
   __device__ __forceinline__ void operator()(int col, float (&v)[32]) const {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = recv[(col + j) * ldr + rr];
-#pragma unroll
-    for (int p = 1; p < SPLITK; ++p)
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] += recv[((p * 128) + col + j) * ldr + rr];
+    for (int j = 0; j < 32; ++j) v[j] = blk[skn_at(col + j, rr, tpr)];
   }
 };
+
+// TMEM columns [c0, c0 + 32) of this thread's lane (column f) into a block's
+// rows [r0, r0 + 32).
+__device__ __forceinline__ void skn_put32(float* blk, int f, int r0, int tpr, const float (&v)[32]) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    *reinterpret_cast<float4*>(blk + skn_at(f, r0 + 4 * u, tpr)) =
+        make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+}
+
+// Local shared memory -> a cluster peer's shared memory, completing on the
+// peer's barrier (both addresses in the peer, mapped with mapa).
+__device__ __forceinline__ void bulk_s2c(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                         uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t mapa_u32(const void* p, int rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(p)), "r"(rank));
+  return ra;
+}
 
 template <class Epi, int SPLITK>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -580,82 +834,114 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   SknBars* bars = reinterpret_cast<SknBars*>(smem + SKN_RING);
-  float* recv = reinterpret_cast<float*>(smem);    // [SPLITK][128][ldr], after the mainloop
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_launch();
-  pdl_wait();
-  const int M = M_dev ? min(*M_dev, M_cap) : M_host;
-  // the same decision in every CTA of the cluster
-  if (M <= 0 || M > SKN_MAX_ROWS) return;
-  const int rank = static_cast<int>(cluster_rank());
+  const int rank = SPLITK > 1 ? static_cast<int>(cluster_rank()) : 0;
   const int nb = blockIdx.x / SPLITK;
   const int nK = (K + BK - 1) / BK, kpc = (nK + SPLITK - 1) / SPLITK;
-  const int kb0 = rank * kpc, kb1 = min(nK, kb0 + kpc);
-  const bool has_k = kb1 > kb0;
-  const int xrows = (M + SKN_XBOX - 1) / SKN_XBOX * SKN_XBOX;   // rows loaded per k-block
-  const int nx = xrows / SKN_XBOX;
-  const int n_mma = (M + 15) / 16 * 16;
-  const int stage_bytes = SKN_W_BYTES + xrows * 128;
-  const int n_st = min(SKN_MAX_ST, SKN_RING / stage_bytes);
-  const int tpr = skn_tpr(M, SPLITK), ldr = skn_ldr(tpr);
-  const int r0 = rank * tpr, r1 = min(M, r0 + tpr);
+  const int kb0 = rank * kpc, n_kb = max(0, min(nK, kb0 + kpc) - kb0);
+  const int n_early = min(n_kb, SKN_EARLY);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < n_st; ++s) {
+    for (int s = 0; s < SKN_MAX_ST; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
     mbar_init(&bars->tfull, 1);
+    mbar_init(&bars->recv, 1);
     bars->abort = 0;
     fence_barrier_init();
   }
+  if (warp == 1) tmem_alloc(&bars->tmem, SKN_TMEM_COLS);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
   volatile int* abort = &bars->abort;
-  // the producer starts at once; warps 1-5 meet after the TMEM allocation
-  uint32_t tmem = 0;
-  if (warp >= 1) {
-    if (warp == 1) tmem_alloc(&bars->tmem, 256);
-    tc_fence_before();
-    asm volatile("bar.sync 1, %0;" ::"n"(THREADS - 32) : "memory");
-    tc_fence_after();
-    tmem = bars->tmem;
+  // before the grid dependency: the weights only
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmX);
+    for (int i = 0; i < n_early; ++i) {
+      mbar_expect_tx_only(&bars->full[i], SKN_W_BYTES);
+      tma_load_2d(smem + i * SKN_W_BYTES, &tmW, (kb0 + i) * BK, nb * 128, &bars->full[i]);
+    }
+    for (int i = n_early; i < min(n_kb, SKN_PF); ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, nb * 128);
   }
+  pdl_launch();
+  pdl_wait();
+  const int M = M_dev ? min(*M_dev, M_cap) : M_host;
+  // the same decision in every CTA of the cluster
+  if (M <= 0 || M > skn_max_rows(SPLITK)) {
+    if (threadIdx.x == 0)      // the early loads land before the CTA ends
+      for (int i = 0; i < n_early; ++i) {
+        mbar_arrive(&bars->full[i]);
+        mbar_wait(&bars->full[i], 0, nullptr, err);
+      }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, SKN_TMEM_COLS);
+    }
+    return;
+  }
+  const int xrows = (M + SKN_XBOX - 1) / SKN_XBOX * SKN_XBOX;   // rows loaded per k-block
+  const int x_bytes = xrows * 128;
+  const int n_st = min(SKN_MAX_ST, SKN_RING / (SKN_W_BYTES + x_bytes));
+  uint8_t* xring = smem + n_st * SKN_W_BYTES;
+  const int n1 = (min(M, 256) + 15) / 16 * 16;                   // the MMAs' N
+  const int n2 = M > 256 ? (M - 256 + 15) / 16 * 16 : 0;
+  const int tpr = SPLITK > 1 ? skn_tpr(M, SPLITK) : SKN_CHUNK;
+  const int r0 = rank * tpr, r1 = SPLITK > 1 ? min(M, r0 + tpr) : M;   // rows this CTA finishes
 
   int ok = 1;
   if (warp == 0) {
     if (lane == 0) {
-      prefetch_tmap(&tmW);
-      prefetch_tmap(&tmX);
       uint32_t issued = 0, par = 0;
-      for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
-        const int stage = i % n_st;
+      for (int i = 0; i < n_kb; ++i) {
+        const int kb = kb0 + i, stage = i % n_st;
         const uint32_t phase = (i / n_st) & 1u;
-        if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort, err)) break;
-        uint8_t* st = smem + stage * stage_bytes;
-        mbar_expect_tx(&bars->full[stage], stage_bytes);
-        tma_load_2d(st, &tmW, kb * BK, nb * 128, &bars->full[stage]);
-        for (int j = 0; j < nx; ++j)
-          tma_load_2d(st + SKN_W_BYTES + j * SKN_XBOX * 128, &tmX, kb * BK, j * SKN_XBOX, &bars->full[stage]);
+        if (i >= n_early) {
+          if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort, err)) break;
+          mbar_expect_tx(&bars->full[stage], SKN_W_BYTES + x_bytes);
+          tma_load_2d(smem + stage * SKN_W_BYTES, &tmW, kb * BK, nb * 128, &bars->full[stage]);
+        } else {
+          mbar_expect_tx(&bars->full[stage], x_bytes);   // its weight bytes are already expected
+        }
+        for (int j = 0; j < xrows / SKN_XBOX; ++j)
+          tma_load_2d(xring + stage * x_bytes + j * (SKN_XBOX * 128), &tmX, kb * BK, j * SKN_XBOX,
+                      &bars->full[stage]);
         issued |= 1u << stage;
         par = (par & ~(1u << stage)) | (phase << stage);
       }
-      if (*abort)
+      if (*abort) {
         for (int s = 0; s < n_st; ++s)
           if (issued & (1u << s)) mbar_wait(&bars->full[s], (par >> s) & 1u, nullptr, err);
+        // early loads the loop never reached
+        for (int i = 0; i < n_early; ++i)
+          if (!(issued & (1u << i))) {
+            mbar_arrive(&bars->full[i]);
+            mbar_wait(&bars->full[i], 0, nullptr, err);
+          }
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, n_mma);
-      for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
+      const uint32_t id1 = idesc_bf16(128, n1), id2 = idesc_bf16(128, n2 > 0 ? n2 : 16);
+      for (int i = 0; i < n_kb; ++i) {
         const int stage = i % n_st;
         const uint32_t phase = (i / n_st) & 1u;
         if (!mbar_wait(&bars->full[stage], phase, abort, err)) break;
         tc_fence_after();
-        const uint32_t w0 = smem_u32(smem + stage * stage_bytes), x0 = w0 + SKN_W_BYTES;
+        const uint32_t w0 = smem_u32(smem + stage * SKN_W_BYTES), x0 = smem_u32(xring + stage * x_bytes);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k)
-          tc_mma_bf16(tmem, sdesc_sw128(w0 + k * 32), sdesc_sw128(x0 + k * 32), idesc, (i | k) != 0 ? 1u : 0u);
+        for (int k = 0; k < BK / 16; ++k) {
+          tc_mma_bf16(tmem, sdesc_sw128(w0 + k * 32), sdesc_sw128(x0 + k * 32), id1, (i | k) != 0 ? 1u : 0u);
+          if (n2 > 0)
+            tc_mma_bf16(tmem + 256, sdesc_sw128(w0 + k * 32), sdesc_sw128(x0 + 256 * 128 + k * 32), id2,
+                        (i | k) != 0 ? 1u : 0u);
+        }
         tc_commit(&bars->empty[stage]);
       }
       tc_commit(&bars->tfull);   // completes once every MMA above is done
@@ -666,44 +952,113 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) ok = mbar_wait(&bars->tfull, 0, abort, err) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
   }
-  // every rank's MMAs are done: the stage rings are free to receive partials
+  const int q = warp & 3, f = q * 32 + lane;                 // epilogue warps: this thread's output column
+  const uint32_t lane_tm = tmem + (static_cast<uint32_t>(q * 32) << 16);
+  const bool live = ok && n_kb > 0 && !*abort;               // a rank with no k-blocks adds zeros
+  float* blk0 = reinterpret_cast<float*>(smem);
   tc_fence_before();
-  cluster_barrier();
-  if (warp >= 2) {
-    tc_fence_after();
-    const int q = warp & 3, f = q * 32 + lane;   // this thread's output column
-    const bool live = ok && has_k;
-    float v[32];
+  if constexpr (SPLITK > 1) {
+    const int bsz = 128 * tpr;                               // floats per block
+    float* send = blk0;                                      // [SPLITK - 1][128][tpr]
+    float* recv = blk0 + (SPLITK - 1) * bsz;                 // [SPLITK - 1][128][tpr], by sender
+    cluster_barrier();   // every rank's MMAs are done: the rings are free for the exchange
+    if (warp >= 2) {
+      tc_fence_after();
 #pragma unroll 1
-    for (int c = 0; c < xrows / 32; ++c) {
-      tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v);
+      for (int o = 0, oi = 0; o < SPLITK; ++o) {
+        if (o == rank) continue;
+        float* dst = send + (oi++) * bsz;
+#pragma unroll 1
+        for (int c = 0; c < tpr / 32; ++c) {
+          float v[32];
+          tmem_ld32(lane_tm + o * tpr + c * 32, v);
+          if (!live)
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        const int r = c * 32 + j;   // four rows, never split between owners
-        if (r >= M) break;
-        const int owner = r / tpr, rr = r - owner * tpr;
-        const uint32_t la = smem_u32(recv + (rank * 128 + f) * ldr + rr);
-        uint32_t ra;
-        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(owner));
-        const float4 x = live ? make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
-        asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ra), "f"(x.x), "f"(x.y),
-                     "f"(x.z), "f"(x.w)
-                     : "memory");
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+          skn_put32(dst, f, c * 32, tpr, v);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // writes visible to the bulk copies
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (threadIdx.x == 64) {
+        mbar_expect_tx(&bars->recv, static_cast<uint32_t>((SPLITK - 1) * bsz * 4));
+#pragma unroll 1
+        for (int o = 0, oi = 0; o < SPLITK; ++o) {
+          if (o == rank) continue;
+          const int slot = rank < o ? rank : rank - 1;        // senders skip the owner
+          bulk_s2c(mapa_u32(recv + slot * bsz, o), send + (oi++) * bsz, static_cast<uint32_t>(bsz * 4),
+                   mapa_u32(&bars->recv, o));
+        }
+      }
+      int w_ok = 1;
+      if (lane == 0) w_ok = mbar_wait(&bars->recv, 0, abort, err) ? 1 : 0;
+      w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+      // the rank-order sum of this CTA's rows into the first receive block
+#pragma unroll 1
+      for (int c = 0; c < (r1 - r0 + 31) / 32 && w_ok; ++c) {
+        float acc[32], v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+#pragma unroll 1
+        for (int s = 0; s < SPLITK; ++s) {
+          if (s == rank) {
+            tmem_ld32(lane_tm + r0 + c * 32, v);
+            if (!live)
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = 0.f;
+          } else {
+            const float* src = recv + (s < rank ? s : s - 1) * bsz;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float4 x = *reinterpret_cast<const float4*>(src + skn_at(f, c * 32 + 4 * u, tpr));
+              v[4 * u] = x.x;
+              v[4 * u + 1] = x.y;
+              v[4 * u + 2] = x.z;
+              v[4 * u + 3] = x.w;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[j] += v[j];
+        }
+        skn_put32(recv, f, c * 32, tpr, acc);
       }
     }
+    __syncthreads();
+    const int nrows = r1 - r0;
+    if (!*abort)
+      for (int it = threadIdx.x; it < nrows * Epi::PARTS; it += THREADS) {
+        const int rr = it % nrows, piece = it / nrows;
+        epi.run_part(r0 + rr, nb * 128, piece, M, N, SknLoader{recv, tpr, rr});
+      }
+    tc_fence_before();
+    cluster_barrier();   // every copy into this CTA has landed and every copy out of it was read
+  } else {
+    __syncthreads();     // the MMAs are done: the ring is free for staging
+#pragma unroll 1
+    for (int c0 = 0; c0 < M; c0 += SKN_CHUNK) {
+      const int nrows = min(SKN_CHUNK, M - c0);
+      if (warp >= 2) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < (nrows + 31) / 32; ++c) {
+          float v[32];
+          tmem_ld32(lane_tm + c0 + c * 32, v);
+          skn_put32(blk0, f, c * 32, SKN_CHUNK, v);
+        }
+      }
+      __syncthreads();
+      if (live)
+        for (int it = threadIdx.x; it < nrows * Epi::PARTS; it += THREADS) {
+          const int rr = it % nrows, piece = it / nrows;
+          epi.run_part(c0 + rr, nb * 128, piece, M, N, SknLoader{blk0, SKN_CHUNK, rr});
+        }
+      __syncthreads();
+    }
+    tc_fence_before();
   }
-  tc_fence_before();
-  cluster_barrier();       // every partial has landed; no remote access follows
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
-  }
-  // (row, piece) items, rows fastest so a warp reads consecutive rows
-  const int nrows = r1 - r0;
-  for (int it = threadIdx.x; it < nrows * Epi::PARTS; it += THREADS) {
-    const int rr = it % nrows, piece = it / nrows;
-    RecvSumLoader<SPLITK> ldr_{recv, ldr, rr};
-    epi.run_part(r0 + rr, nb * 128, piece, M, N, ldr_);
+    tmem_dealloc(tmem, SKN_TMEM_COLS);
   }
 }
 

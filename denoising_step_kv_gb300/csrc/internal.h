@@ -112,6 +112,8 @@ cudaError_t gemm_gelu(dllm_cache* c, const void* A, const void* W, int M, int M_
 cudaError_t gemm_lm(dllm_cache* c, const void* A, const void* W, int M, const int* M_dev, int V, int d,
                     const float* rs, int mask_id, void* part, int n_tiles, cudaStream_t st);
 int lm_tile_cols(const dllm_cache* c, int M, int V);
+// partial statistics per row of the LM head for M rows and V columns
+int lm_slots(const dllm_cache* c, int M, int V);
 
 // attn.cu ------------------------------------------------------------------
 // Queries: positions [q_pos0, q_pos0 + q_len) (ring slot in streaming mode)

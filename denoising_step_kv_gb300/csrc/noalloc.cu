@@ -93,7 +93,7 @@ extern "C" dllm_status lmhead_conf_noalloc(const void* h_dev, const void* w_lm_d
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float* rs = reinterpret_cast<float*>(scratch + NA_RS_OFF);
-  const int n_tiles = cdiv(V, lm_tile_cols(&ctx, M, V));
+  const int n_tiles = lm_slots(&ctx, M, V);
   // the error word is the only scratch that must start at zero; the
   // statistics and row scales are fully rewritten by every call.  A wait
   // that gives up leaves some statistics unwritten and sets the word, and

@@ -80,8 +80,8 @@ def test_kv_refresh_ragged_rows(name):
 @pytest.mark.parametrize("n", [None, 700, 530, 513, 512, 300, 257, 200])
 def test_kv_refresh_large_m(name, n):
     """Row counts around the weight-streaming range: the host count (every
-    row) and device counts on both sides of the 512-row switch (257..512: the
-    stream-K kernel's two-MMA, single-accumulator path)."""
+    row) and device counts on both sides of the 256-row limit of the split-K
+    weight-streaming kernel and of the 512-row one of the pair kernel."""
     w, m, W, D = _setup(name)
     B, L, H, dh = w.batch, w.seq_len, w.n_heads, w.head_dim
     tok = G.integers(5, 1, w.vocab, (B, L))
@@ -102,6 +102,37 @@ def test_kv_refresh_large_m(name, n):
         for f, want in ((K.FIELD_Q, q), (K.FIELD_K, k), (K.FIELD_V, v)):
             got = read_kv(c, f, 0, w).reshape(B * L, H, dh)
             assert close(got[rows], want, w), (name, n, f, max_err(got[rows], want))
+            assert np.all(got[untouched] == 0)
+    finally:
+        K.dllm_cache_free(c)
+
+
+@pytest.mark.parametrize("n", [200, 256, 272, 300, 512])
+def test_kv_refresh_wide_projection(n):
+    """The 8B-shaped projection (d 4096, N = 3d = 12288: 96 weight tiles, the
+    weight-streaming kernel without a split of K) at device row counts up to
+    512; rows past 256 take its second MMA.  Sampled rows on both sides of
+    256, and the last, against the oracle; rows outside the list untouched."""
+    from dataclasses import replace
+    w = replace(C.get("8b_shaped"), batch=1, seq_len=640, n_prompt=576, vocab=1000)
+    B, L, H, dh = w.batch, w.seq_len, w.n_heads, w.head_dim
+    embed, wqkv = G.embed(w), G.w_qkv(w, 0)
+    tok = G.integers(8, 1, w.vocab, (B, L))
+    rows = G.choice(9 + n, B * L, n)
+    c = _fresh(w)
+    try:
+        rows_d = torch.zeros(B * L, dtype=torch.int32, device="cuda")
+        rows_d[:n] = i32(rows)
+        K.kv_refresh(c, 0, None, i32(tok), to_device(embed), to_device(wqkv), rows_d, i32([n]), 4)
+        assert K.dllm_cache_check(c) == 0
+        pick = np.unique(np.clip([0, 1, 127, 128, 255, 256, 257, 271, 272, 300, n - 1], 0, n - 1))
+        sel = rows[pick]
+        x = O.bf16_bits_to_f64(embed)[tok.reshape(-1)[sel]]
+        q, k, v = O.project_qkv(x, O.bf16_bits_to_f64(wqkv), sel % L, H, w.dtype, w.rope_theta, w.rms_eps)
+        untouched = np.setdiff1d(np.arange(B * L), rows)
+        for f, want in ((K.FIELD_Q, q), (K.FIELD_K, k), (K.FIELD_V, v)):
+            got = read_kv(c, f, 0, w).reshape(B * L, H, dh)
+            assert close(got[sel], want, w), (n, f, max_err(got[sel], want))
             assert np.all(got[untouched] == 0)
     finally:
         K.dllm_cache_free(c)
@@ -244,11 +275,15 @@ def test_lmhead_conf(name):
         K.dllm_cache_free(c)
 
 
-@pytest.mark.parametrize("V,M", [(1640, 32), (1640, 200), (4100, 256), (9, 5)])
+@pytest.mark.parametrize("V,M", [(1640, 32), (1640, 200), (4100, 256), (9, 5), (50000, 129), (50000, 200),
+                                 (50000, 256), (126464, 256)])
 def test_lmhead_conf_vocab_groups(V, M):
     """Vocab sizes whose 128-column tiles do not fill the last cluster group
-    (13 tiles in groups of 4), more than one 128-row tile, and a vocab below
-    one group (the plain persistent kernel)."""
+    (13 tiles in groups of 4), more than one 128-row tile, a vocab below one
+    group (the plain persistent kernel), and large vocabularies at 129..256
+    rows (the per-SM column ranges of the wide kernel: chunks of 192 and 160
+    columns with the last CTAs past the vocabulary at V 50000; 224 and 192
+    at V 126464)."""
     from dataclasses import replace
     w = replace(C.get("mid_bf16"), vocab=V, batch=1, block_len=min(64, M), seq_len=max(160, M))
     c = K.dllm_cache_init(K.make_cfg(w))
