@@ -251,6 +251,12 @@ __device__ __forceinline__ void prefetch_l2(const void* p, int bytes) {
   for (int o = 0; o < bytes; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(c + o));
 }
 
+// Bring [p, p + bytes) into this SM's L1 (one prefetch per 128-byte line).
+__device__ __forceinline__ void prefetch_l1(const void* p, int bytes) {
+  const char* c = static_cast<const char*>(p);
+  for (int o = 0; o < bytes; o += 128) asm volatile("prefetch.global.L1 [%0];" ::"l"(c + o));
+}
+
 // Bring one box of a tensor map into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

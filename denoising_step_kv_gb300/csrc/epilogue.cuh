@@ -94,7 +94,19 @@ struct EpiQKV {
     return ok && sc > 0.f;
   }
 
-  __device__ __forceinline__ void prefetch(int, int, int, int) const {}
+  // before the epilogue: the row's scale, its row id, its refresh-flag word
+  // and the RoPE table into L1 (the epilogue's loads then hit)
+  __device__ __forceinline__ void prefetch(int m, int n0, int M, int) const {
+    if (m >= M) return;
+    prefetch_l1(rs + m, 4);
+    if ((m & 31) == 0) prefetch_l1(rope, DH / 2 * static_cast<int>(sizeof(float2)));
+    if (!gate || streaming || n0 < d) return;
+    const int row = rows ? rows[m] : row0 + m;
+    if (row >= 0 && row < rows_cap) {
+      const int b = row / L, pos = row - b * L;
+      prefetch_l1(gate + b * Lw + (pos >> 5), 4);
+    }
+  }
 
   template <class LD>
   __device__ __forceinline__ void run_part(int m, int n0, int p, int M, int N, const LD& ld) const {
@@ -213,9 +225,11 @@ struct EpiResid {
     return embed + static_cast<size_t>(t) * N;
   }
 
+  // before the epilogue (the weight-streaming kernel calls this while its
+  // MMAs run): the residual row's slice of this tile into L1
   __device__ __forceinline__ void prefetch(int m, int n0, int M, int N) const {
     const T* rrow = resid_row(m, M, N, false);
-    if (rrow) prefetch_l2(rrow + n0, 128 * static_cast<int>(sizeof(T)));
+    if (rrow) prefetch_l1(rrow + n0, 128 * static_cast<int>(sizeof(T)));
   }
 
   template <class LD>
@@ -258,7 +272,9 @@ struct EpiGelu {
   const float* rs;
   T* out;
 
-  __device__ __forceinline__ void prefetch(int, int, int, int) const {}
+  __device__ __forceinline__ void prefetch(int m, int, int M, int) const {
+    if (m < M) prefetch_l1(rs + m, 4);
+  }
 
   template <class LD>
   __device__ __forceinline__ void run_part(int m, int n0, int p, int M, int N, const LD& ld) const {

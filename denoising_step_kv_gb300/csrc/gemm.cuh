@@ -49,6 +49,24 @@ struct Bars {
 template <int STAGES>
 constexpr size_t smem_bytes() { return 1024 + STAGES * STAGE_BYTES + sizeof(Bars); }
 
+// Column-banded tile order of the persistent kernels: bands of gw column
+// tiles (about 32 MB of weights), the column tile fastest inside a band, so
+// that the tiles in flight at once share a few row tiles and one band of
+// weights in L2 (rows fastest would stream every row tile from HBM once per
+// column tile when the rows do not fit in L2).
+__host__ __device__ __forceinline__ int band_width(int tile_cols, int K) {
+  const long long w = (32ll << 20) / (static_cast<long long>(tile_cols) * K * 2);
+  return static_cast<int>(w < 1 ? 1 : w);
+}
+__device__ __forceinline__ void band_tile(int tile, int nM, int nN, int gw, int& m, int& n) {
+  const int per = nM * gw;                      // tiles of a full band
+  const int band = tile / per;
+  const int bw = min(gw, nN - band * gw);       // this band's width
+  const int rem = tile - band * per;
+  m = rem / bw;
+  n = band * gw + rem % bw;
+}
+
 struct TmemLoader {
   uint32_t taddr;
   __device__ __forceinline__ void operator()(int col, float (&v)[32]) const { tmem_ld32(taddr + col, v); }
@@ -97,13 +115,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nM = (M + BM - 1) / BM, nN = (N + BN - 1) / BN, nK = (K + BK - 1) / BK;
   // M below M_min belongs to the kernel launched beside this one
   const int tiles = (M > 0 && M >= M_min) ? nM * nN : 0;
+  const int gw = band_width(BN, K);
 
   if (warp == 0) {
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, issued = 0, par = 0;
       for (int tile = blockIdx.x; tile < tiles && !*abort; tile += gridDim.x) {
-        const int mb = tile % nM, nb = tile / nM;
+        int mb, nb;
+        band_tile(tile, nM, nN, gw, mb, nb);
         for (int kb = 0; kb < nK; ++kb) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort, err)) break;
           mbar_expect_tx(&bars->full[stage], STAGE_BYTES);
@@ -170,7 +190,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const int mb = tile % nM, nb = tile / nM;
+      int mb, nb;
+      band_tile(tile, nM, nN, gw, mb, nb);
       const int m = mb * BM + q * 32 + lane;
       TmemLoader ld{tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN)};
       epi.run(m, nb * BN, BN / 32, M, N, ld);
@@ -252,13 +273,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nM = (M + BM - 1) / BM, nMP = (nM + 1) / 2, nN = (N + PBN - 1) / PBN, nK = (K + BK - 1) / BK;
   // the same in both CTAs of a cluster: both run the same tiles and k-blocks
   const int tiles = (M > 0 && M >= M_min) ? nMP * nN : 0;
+  const int gw = band_width(PBN, K);
 
   if (warp == 0) {
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, issued = 0, par = 0;
       for (int tile = cl; tile < tiles && !*abort; tile += n_cl) {
-        const int mp = tile % nMP, nb = tile / nMP;
+        int mp, nb;
+        band_tile(tile, nMP, nN, gw, mp, nb);
         // a half past the last row tile loads the last valid one again (its
         // rows are >= M, the epilogue stores nothing for them)
         const int mb_ld = min(2 * mp + rank, nM - 1);
@@ -330,7 +353,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const int mp = tile % nMP, nb = tile / nMP;
+      int mp, nb;
+      band_tile(tile, nMP, nN, gw, mp, nb);
       const int m = (2 * mp + rank) * BM + q * 32 + lane;
       TmemLoader ld{tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * PBN)};
       epi.run(m, nb * PBN, PBN / 32, M, N, ld);
@@ -749,7 +773,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 // barrier; the owner adds the partials in rank order (its own from TMEM)
 // into its first receive block and runs the epilogue over (row, piece)
 // items.  Without a split the accumulator is staged through shared memory
-// 128 rows at a time.  Blocks are [128 columns][tpr rows] fp32 with each
+// in one pass (up to 384 rows, else two).  Blocks are [128 columns][tpr rows] fp32 with each
 // column's 16-byte chunks rotated by the column index, so that a warp's
 // column-wise writes and its row-wise reads both spread over all banks.
 constexpr int SKN_MAX_ROWS = 512;                // without a split of K
@@ -760,7 +784,7 @@ constexpr int SKN_RING = 192 * 1024;
 constexpr int SKN_MAX_ST = 8;
 constexpr int SKN_EARLY = 2;                     // weight k-blocks loaded before the grid dependency
 constexpr int SKN_PF = 16;                       // weight k-blocks warmed in L2 before it
-constexpr int SKN_CHUNK = 128;                   // rows staged per pass without a split
+constexpr int SKN_CHUNK = 384;                   // most rows staged in one pass without a split
 constexpr uint32_t SKN_TMEM_COLS = 512;
 struct SknBars {
   uint64_t full[SKN_MAX_ST];
@@ -778,7 +802,7 @@ __host__ __device__ constexpr int skn_tpr(int M, int S) { return ((M + S - 1) / 
 static_assert(2 * 3 * 128 * skn_tpr(SKN_SPLIT_ROWS, 4) * 4 <= SKN_RING, "exchange blocks fit in the ring");
 static_assert(2 * 2 * 128 * skn_tpr(SKN_SPLIT_ROWS, 3) * 4 <= SKN_RING, "exchange blocks fit in the ring");
 static_assert(2 * 1 * 128 * skn_tpr(SKN_SPLIT_ROWS, 2) * 4 <= SKN_RING, "exchange blocks fit in the ring");
-static_assert(128 * SKN_CHUNK * 4 <= SKN_RING, "a staged chunk fits in the ring");
+static_assert(128 * SKN_CHUNK * 4 <= SKN_RING && 128 * 256 * 4 <= SKN_RING, "a staged pass fits in the ring");
 static_assert(SKN_RING / (SKN_W_BYTES + SKN_MAX_ROWS * 128) >= SKN_EARLY, "the early loads' stages exist for any M");
 
 // Element (column f, row rr) of a [128][tpr] block: column f's 16-byte
@@ -892,7 +916,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* xring = smem + n_st * SKN_W_BYTES;
   const int n1 = (min(M, 256) + 15) / 16 * 16;                   // the MMAs' N
   const int n2 = M > 256 ? (M - 256 + 15) / 16 * 16 : 0;
-  const int tpr = SPLITK > 1 ? skn_tpr(M, SPLITK) : SKN_CHUNK;
+  // rows per owner with a split; without one, rows staged per pass (all of
+  // them up to SKN_CHUNK, else halves of at most 256)
+  const int tpr = SPLITK > 1 ? skn_tpr(M, SPLITK) : (xrows <= SKN_CHUNK ? xrows : 256);
   const int r0 = rank * tpr, r1 = SPLITK > 1 ? min(M, r0 + tpr) : M;   // rows this CTA finishes
 
   int ok = 1;
@@ -1035,22 +1061,22 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     __syncthreads();     // the MMAs are done: the ring is free for staging
 #pragma unroll 1
-    for (int c0 = 0; c0 < M; c0 += SKN_CHUNK) {
-      const int nrows = min(SKN_CHUNK, M - c0);
+    for (int c0 = 0; c0 < M; c0 += tpr) {
+      const int nrows = min(tpr, M - c0);
       if (warp >= 2) {
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < (nrows + 31) / 32; ++c) {
           float v[32];
           tmem_ld32(lane_tm + c0 + c * 32, v);
-          skn_put32(blk0, f, c * 32, SKN_CHUNK, v);
+          skn_put32(blk0, f, c * 32, tpr, v);
         }
       }
       __syncthreads();
       if (live)
         for (int it = threadIdx.x; it < nrows * Epi::PARTS; it += THREADS) {
           const int rr = it % nrows, piece = it / nrows;
-          epi.run_part(c0 + rr, nb * 128, piece, M, N, SknLoader{blk0, SKN_CHUNK, rr});
+          epi.run_part(c0 + rr, nb * 128, piece, M, N, SknLoader{blk0, tpr, rr});
         }
       __syncthreads();
     }
