@@ -544,215 +544,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// LM head for 128 < M <= 256 rows and a large vocabulary: clusters of two
-// CTAs, one per SM.  Each CTA owns a contiguous range of vocabulary columns
-// and computes all M rows of it (two 128-row accumulators, TMEM columns
-// [0, 256) and [256, 512)), in chunks of up to 256 columns whose widths
-// (multiples of 32) are the same in every CTA.  The two CTAs of a cluster run
-// their chunks in lockstep, so each loads one 128-row half of the rows'
-// k-block and multicasts it into both: a k-block lands 32 KB of rows and at
-// most 32 KB of weights per SM for 2 x 128 rows of MMA work (the pair kernel
-// lands 48 KB per 128 rows), and the rows are read from L2 once per cluster.
-// The weight chunk is loaded in 32-row boxes.  Before the grid dependency
-// each CTA loads the weights of its first LW_STAGES k-blocks (no earlier
-// kernel writes them).  Every MMA commit arrives on both CTAs' empty barriers:
-// a stage is reloaded only once both have read it.  The epilogue releases the
-// first accumulator before it reads the second, so the next chunk's first
-// MMAs overlap it.  Each chunk's statistics go to partial slot
-// cta * n_chunks + chunk.
-constexpr int LW_STAGES = 3;
-constexpr int LW_BOX = 32;                               // weight rows per load
-constexpr int LW_A_BYTES = 2 * A_BYTES;                  // 256 rows x 64
-constexpr int LW_STAGE = LW_A_BYTES + 256 * BK * 2;      // + up to 256 weight rows
-struct LwBars {
-  uint64_t full[LW_STAGES];
-  uint64_t empty[LW_STAGES];
-  uint64_t tfull;
-  uint64_t tempty[2];
-  uint64_t done;
-  uint32_t tmem;
-  int abort;
-};
-constexpr size_t LW_SMEM = 1024 + LW_STAGES * LW_STAGE + sizeof(LwBars);
-
-// 32-column units of chunk k when `units` are split into n_chunks widths
-// that differ by at most one unit; `first` is the chunk's first unit.
-__host__ __device__ __forceinline__ int lw_chunk(int units, int n_chunks, int k, int& first) {
-  const int base = units / n_chunks, extra = units % n_chunks;
-  first = k * base + min(k, extra);
-  return base + (k < extra ? 1 : 0);
-}
-
-template <class Epi>
-__global__ void __launch_bounds__(THREADS, 1)
-    gemm_lmwide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       int M_host, const int* __restrict__ M_dev, int M_cap, int N, int K, int units,
-                       int n_chunks, Epi epi, unsigned* err) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  LwBars* bars = reinterpret_cast<LwBars*>(smem + LW_STAGES * LW_STAGE);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = static_cast<int>(cluster_rank());
-  const int col0 = blockIdx.x * units * 32;               // this CTA's first column
-  const int nK = (K + BK - 1) / BK;
-  const int n_early = min(nK, LW_STAGES);                 // chunk 0's first k-blocks
-  int u0_first;
-  const int u0 = lw_chunk(units, n_chunks, 0, u0_first);
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < LW_STAGES; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 2);
-    }
-    mbar_init(&bars->tfull, 1);
-    mbar_init(&bars->tempty[0], 4);
-    mbar_init(&bars->tempty[1], 4);
-    mbar_init(&bars->done, 1);
-    bars->abort = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) tmem_alloc(&bars->tmem, 512);
-  tc_fence_before();
-  __syncthreads();
-  cluster_barrier();       // the peer's barriers exist before any multicast lands
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem;
-  volatile int* abort = &bars->abort;
-  // before the grid dependency: the weights only
-  if (threadIdx.x == 0) {
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
-    for (int i = 0; i < n_early; ++i) {
-      mbar_expect_tx_only(&bars->full[i], u0 * LW_BOX * 128);
-      for (int j = 0; j < u0; ++j)
-        tma_load_2d(smem + i * LW_STAGE + LW_A_BYTES + j * (LW_BOX * 128), &tmB, i * BK, col0 + j * LW_BOX,
-                    &bars->full[i]);
-    }
-  }
-  pdl_launch();
-  pdl_wait();
-  const int M = M_dev ? min(*M_dev, M_cap) : M_host;
-  const int chunks = M > 0 ? n_chunks : 0;                 // the same in both CTAs
-
-  if (warp == 0) {
-    if (lane == 0) {
-      int stage = 0, i = 0;
-      uint32_t phase = 0, issued = 0, par = 0;
-      for (int k = 0; k < chunks && !*abort; ++k) {
-        int uf;
-        const int u = lw_chunk(units, n_chunks, k, uf);
-        const int n0 = col0 + uf * 32;
-        for (int kb = 0; kb < nK; ++kb, ++i) {
-          if (i >= n_early) {
-            if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort, err)) break;
-            mbar_expect_tx(&bars->full[stage], LW_A_BYTES + u * LW_BOX * 128);
-            for (int j = 0; j < u; ++j)
-              tma_load_2d(smem + stage * LW_STAGE + LW_A_BYTES + j * (LW_BOX * 128), &tmB, kb * BK,
-                          n0 + j * LW_BOX, &bars->full[stage]);
-          } else {
-            mbar_expect_tx(&bars->full[stage], LW_A_BYTES);   // its weight bytes are already expected
-          }
-          tma_load_2d_mc(smem + stage * LW_STAGE + rank * A_BYTES, &tmA, kb * BK, rank * BM, &bars->full[stage],
-                         0x3);
-          issued |= 1u << stage;
-          par = (par & ~(1u << stage)) | (phase << stage);
-          if (++stage == LW_STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (chunks == 0 || *abort) {
-        for (int s = 0; s < LW_STAGES; ++s)
-          if (issued & (1u << s)) mbar_wait(&bars->full[s], (par >> s) & 1u, nullptr, err);
-        for (int s = 0; s < n_early; ++s)      // early weight loads the loop never reached
-          if (!(issued & (1u << s))) {
-            mbar_arrive(&bars->full[s]);
-            mbar_wait(&bars->full[s], 0, nullptr, err);
-          }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int k = 0; k < chunks && !*abort; ++k) {
-        int uf;
-        const int u = lw_chunk(units, n_chunks, k, uf);
-        const uint32_t idesc = idesc_bf16(BM, u * 32);
-        const uint32_t tpar = (static_cast<uint32_t>(k) & 1u) ^ 1u;   // the previous chunk's release
-        bool ok = mbar_wait(&bars->tempty[0], tpar, abort, err);
-        bool ok1 = false;                                               // second accumulator released
-        for (int kb = 0; kb < nK && ok; ++kb) {
-          if (!mbar_wait(&bars->full[stage], phase, abort, err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + stage * LW_STAGE), b0 = a0 + LW_A_BYTES;
-#pragma unroll
-          for (int k16 = 0; k16 < BK / 16; ++k16)
-            tc_mma_bf16(tmem, sdesc_sw128(a0 + k16 * 32), sdesc_sw128(b0 + k16 * 32), idesc,
-                        (kb | k16) != 0 ? 1u : 0u);
-          if (!ok1) {
-            if (!mbar_wait(&bars->tempty[1], tpar, abort, err)) {
-              ok = false;
-              break;
-            }
-            ok1 = true;
-            tc_fence_after();
-          }
-#pragma unroll
-          for (int k16 = 0; k16 < BK / 16; ++k16)
-            tc_mma_bf16(tmem + 256, sdesc_sw128(a0 + A_BYTES + k16 * 32), sdesc_sw128(b0 + k16 * 32), idesc,
-                        (kb | k16) != 0 ? 1u : 0u);
-          tc_commit_mc(&bars->empty[stage], 0x3);
-          if (++stage == LW_STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        tc_commit(&bars->tfull);
-      }
-      // all MMAs (and the empty-barrier arrivals they owe the peer) complete
-      // before the cluster barrier below
-      tc_commit(&bars->done);
-      mbar_wait(&bars->done, 0, nullptr, err);
-    }
-  } else {
-    const int q = warp & 3;
-    const uint32_t lane_tm = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    for (int k = 0; k < chunks; ++k) {
-      int uf;
-      const int u = lw_chunk(units, n_chunks, k, uf);
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&bars->tfull, static_cast<uint32_t>(k) & 1u, abort, err) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      tc_fence_after();
-      const int slot = blockIdx.x * n_chunks + k;
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        TmemLoader ld{lane_tm + static_cast<uint32_t>(h * 256)};
-        epi.run_slot(h * BM + q * 32 + lane, col0 + uf * 32, u, slot, M, N, ld);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->tempty[h]);
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  cluster_barrier();       // no multicast copy or commit still targets this CTA
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
 // Weight-streaming GEMM for few rows: D^T = B . A^T.  The weights B [N][K]
 // are the MMA's A operand (128 output columns per CTA, on the TMEM lanes) and
 // the rows A [M][K] its B operand (on the TMEM columns: one MMA of N = M

@@ -237,51 +237,7 @@ int lm_tile_cols(const dllm_cache* c, int M, int V) {
   return M > tc::BM || (M > 0 && cdiv(V, tc::PBN) >= 8) ? tc::PBN : tc::BN;
 }
 
-namespace {
-// The wide LM head's split of the vocabulary: CTAs (pairs, one per SM), 32-
-// column units per CTA, chunks of at most 8 units per CTA.
-struct LwPlan {
-  int ctas, units, chunks;
-};
-LwPlan lw_plan(const dllm_cache* c, int V) {
-  LwPlan p;
-  p.ctas = std::max(2, c->num_sms / 2 * 2);
-  p.units = cdiv(cdiv(V, p.ctas), 32);
-  p.chunks = cdiv(p.units, 8);
-  return p;
-}
-// 128 < M <= 256 rows, and a vocabulary large enough that the partial slots
-// (one per chunk of every CTA) fit where the 128-column tiles' would.
-bool lw_use(const dllm_cache* c, int M, int V) {
-  if (c->cfg.dtype != DLLM_BF16 || M <= tc::BM || M > 2 * tc::BM) return false;
-  const LwPlan p = lw_plan(c, V);
-  return p.ctas * p.chunks <= cdiv(V, 128) && p.units >= 4;
-}
-
-cudaError_t launch_lmwide(dllm_cache* c, const void* A, int M, const int* M_dev, const void* W, int V, int d,
-                          const EpiLM& e, cudaStream_t st) {
-  static PerDeviceOnce attr;
-  {
-    const cudaError_t err = set_smem_once(attr, tc::gemm_lmwide_kernel<EpiLM>, tc::LW_SMEM);
-    if (err != cudaSuccess) return err;
-  }
-  CUtensorMap ta, tb;
-  if (!make_tmap_2d(&ta, A, d, M, static_cast<uint64_t>(d) * 2, tc::BK, tc::BM, true) ||
-      !make_tmap_2d(&tb, W, d, V, static_cast<uint64_t>(d) * 2, tc::BK, tc::LW_BOX, true))
-    return cudaErrorInvalidValue;
-  const LwPlan p = lw_plan(c, V);
-  return launch_ex(tc::gemm_lmwide_kernel<EpiLM>, dim3(p.ctas), dim3(tc::THREADS), tc::LW_SMEM, st, 2, ta, tb,
-                   M_dev ? 0 : M, M_dev, M, V, d, p.units, p.chunks, e, c->err);
-}
-}  // namespace
-
-int lm_slots(const dllm_cache* c, int M, int V) {
-  if (lw_use(c, M, V)) {
-    const LwPlan p = lw_plan(c, V);
-    return p.ctas * p.chunks;
-  }
-  return cdiv(V, lm_tile_cols(c, M, V));
-}
+int lm_slots(const dllm_cache* c, int M, int V) { return cdiv(V, lm_tile_cols(c, M, V)); }
 
 cudaError_t gemm_qkv(dllm_cache* c, int layer, const void* A, int M_cap, const int* M_dev, const int* rows,
                      const void* w_qkv, cudaStream_t st, void* stage, int row0) {
@@ -325,7 +281,6 @@ cudaError_t gemm_lm(dllm_cache* c, const void* A, const void* W, int M, const in
                     const float* rs, int mask_id, void* part, int n_tiles, cudaStream_t st) {
   EpiLM e{rs, mask_id, static_cast<LMPart*>(part), n_tiles};
   if (c->cfg.dtype == DLLM_BF16) {
-    if (lw_use(c, M, V)) return launch_lmwide(c, A, M, M_dev, W, V, d, e, st);
     if (M > tc::BM) {   // pairs of row tiles share each 256-column weight tile
       CUtensorMap ta, tb;
       if (!make_tmap_2d(&ta, A, d, M, static_cast<uint64_t>(d) * 2, tc::BK, tc::BM, true) ||

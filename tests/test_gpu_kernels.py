@@ -281,9 +281,8 @@ def test_lmhead_conf_vocab_groups(V, M):
     """Vocab sizes whose 128-column tiles do not fill the last cluster group
     (13 tiles in groups of 4), more than one 128-row tile, a vocab below one
     group (the plain persistent kernel), and large vocabularies at 129..256
-    rows (the per-SM column ranges of the wide kernel: chunks of 192 and 160
-    columns with the last CTAs past the vocabulary at V 50000; 224 and 192
-    at V 126464)."""
+    rows (pairs of row tiles on 256-column weight tiles; V 50000 leaves a
+    80-column tail)."""
     from dataclasses import replace
     w = replace(C.get("mid_bf16"), vocab=V, batch=1, block_len=min(64, M), seq_len=max(160, M))
     c = K.dllm_cache_init(K.make_cfg(w))
