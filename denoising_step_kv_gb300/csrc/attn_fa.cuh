@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(192, 2)
         tc_fence_after();
         const uint32_t vb = smem_u32(sm + S::OFF_RING + s * 2 * S::KV_TILE + S::KV_TILE);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
+        for (int part = 0; part < attn_tc::P_PARTS; ++part) {
           const uint32_t pt = tmem + S::S_COL + (i & 1) * KT + part * (KT / 2);
 #pragma unroll
           for (int k = 0; k < KT / 16; ++k)
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(192, 2)
           }
         const uint32_t pt = tmem + lane_off + S::S_COL + sb * KT;
         attn_tc::tmem_st32u(pt, hi);
-        attn_tc::tmem_st32u(pt + KT / 2, lo);
+        if constexpr (attn_tc::P_PARTS == 2) attn_tc::tmem_st32u(pt + KT / 2, lo);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
       tc_fence_before();

@@ -36,6 +36,11 @@ constexpr int KT = 64;                  // keys per tile
 constexpr int NSLOT = 6;                // ring slots (K and V of one tile each)
 constexpr int QROWS = 128;              // MMA M (query rows, padded)
 constexpr float LAZY = 8.f;             // log2 headroom before the reference moves
+// P in TMEM for the P V products: 2 = a (hi, lo) bf16 pair whose sum
+// carries P to about 16 bits (two MMAs per 16 keys); 1 = bf16 P alone, about
+// 14% faster, but its 8-bit rounding of P moves O by up to 1.6e-2 when few
+// keys carry the weight (a sink ring's first tokens)
+constexpr int P_PARTS = 2;
 
 template <int DH, int R>
 struct Shape {
@@ -292,7 +297,7 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t vb = smem_u32(sm + S::OFF_RING + s * 2 * S::KV_TILE + S::KV_TILE);
         // N = DH in one MMA: the V tile's 64-dim halves are MN atoms 8 KB apart
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
+        for (int part = 0; part < P_PARTS; ++part) {
           const uint32_t pt = tmem + S::S_COL + (i & 1) * KT + part * (KT / 2);   // P_i hi / lo in TMEM
 #pragma unroll
           for (int k = 0; k < KT / 16; ++k)
@@ -438,7 +443,7 @@ __global__ void __launch_bounds__(192, 1)
           }
         const uint32_t pt = tmem + lane_off + S::S_COL + sb * KT;
         tmem_st32u(pt, hi);
-        tmem_st32u(pt + KT / 2, lo);
+        if constexpr (P_PARTS == 2) tmem_st32u(pt + KT / 2, lo);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
       tc_fence_before();
