@@ -3,6 +3,7 @@
 // bf16: the tensor-core kernel of attn_tc.cuh.  fp32: one warp per (query,
 // head, sequence) with an online softmax in fp32.
 #include <algorithm>
+#include <atomic>
 
 #include "attn_tc.cuh"
 #include "attn_fa.cuh"
@@ -95,9 +96,36 @@ cudaError_t launch_rows(dllm_cache* c, const uint8_t* Ql, const uint8_t* Kl, con
     const cudaError_t e = set_smem_once(attr, attn_rows::attn_rows_kernel<DH>, S::SMEM);
     if (e != cudaSuccess) return e;
   }
+  // CTAs resident per SM (two at dh 64: twice the softmax warps to hide
+  // each one's TMEM and barrier latency), asked once per device
+  static std::atomic<int> resident[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  int per_sm = dev < 64 ? resident[dev].load(std::memory_order_acquire) : 0;
+  if (per_sm == 0) {
+    // from the SM's shared memory and registers (the largest carveout is
+    // requested, so that two CTAs' worth of shared memory is there)
+    cudaFuncSetAttribute(attn_rows::attn_rows_kernel<DH>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    cudaFuncAttributes fa;
+    int smem_sm = 0, resv = 0, regs_sm = 0;
+    per_sm = 1;
+    if (cudaFuncGetAttributes(&fa, attn_rows::attn_rows_kernel<DH>) == cudaSuccess &&
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) == cudaSuccess) {
+      const size_t per_cta = S::SMEM + fa.sharedSizeBytes + resv;
+      const int regs_cta = ((fa.numRegs + 7) / 8 * 8) * 192;
+      per_sm = static_cast<int>(std::min<size_t>(smem_sm / per_cta, regs_sm / std::max(1, regs_cta)));
+    }
+    cudaGetLastError();
+    per_sm = std::max(1, std::min(per_sm, 2));
+    if (dev < 64) resident[dev].store(per_sm, std::memory_order_release);
+  }
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(DH));
-  return launch_ex(attn_rows::attn_rows_kernel<DH>, dim3(c->num_sms), dim3(192), S::SMEM, st, 0, Ql, Kl, Vl, c->kv,
-                   c->cfg.seq_len, c->cfg.batch, c->cfg.n_heads, rows, n_rows, c->seq_rows, scale_log2, out, c->err);
+  return launch_ex(attn_rows::attn_rows_kernel<DH>, dim3(per_sm * c->num_sms), dim3(192), S::SMEM, st, 0, Ql, Kl, Vl,
+                   c->kv, c->cfg.seq_len, c->cfg.batch, c->cfg.n_heads, rows, n_rows, c->seq_rows, scale_log2, out,
+                   c->err);
 }
 
 cudaError_t attn_rows_dense(dllm_cache* c, int layer, const int* rows, const int* n_rows, void* out,

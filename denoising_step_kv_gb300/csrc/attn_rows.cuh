@@ -2,7 +2,9 @@
 // (every row that passes through the layer stack of a multi-layer step):
 // each query attends over all L cached positions of its own sequence.
 //
-// Persistent kernel, one CTA per SM.  A work item is (sequence b, query tile
+// Persistent kernel, as many CTAs per SM as fit (two at dh 64, where a CTA
+// takes about 107 KB of shared memory and 256 TMEM columns; one at dh 128).
+// A work item is (sequence b, query tile
 // of up to 128 of its rows, head h); items are numbered in (b, tile) order,
 // heads fastest, and CTA i takes items i, i + gridDim.x, ...  The per-sequence
 // row ranges come from a binary search of the sorted list at kernel start.
