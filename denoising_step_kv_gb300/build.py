@@ -44,7 +44,7 @@ def build(verbose=False, extra=()):
     if failed:
         msg = "\n".join(f"--- {s}\n{o}" for s, o in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
-    cmd = [nvcc(), *ARCH, "-shared", "-o", LIB, *objs]
+    cmd = [nvcc(), *ARCH, "-shared", "-o", LIB, *objs, "-ldl"]   # dlopen: the NVTX injection hook
     r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))

@@ -6,6 +6,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.h"
 
 namespace dllm {
@@ -49,6 +51,16 @@ dllm_status cuda_fail(cudaError_t e, const char* where) {
     if (!(c)) return fail(DLLM_EINVAL, "null dllm_cache handle"); \
   } while (0)
 
+// An NVTX range around each entry point of the step (host-side: it spans the
+// call that enqueues the work; a profiler attached to the process shows the
+// step's structure, and without one the calls cost a check of a pointer).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 #define DLLM_LAUNCH(expr, where)                 \
   do {                                           \
     cudaError_t e_ = (expr);                     \
@@ -60,7 +72,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 void free_all(dllm_cache* c) {
   void* bufs[] = {c->q, c->k, c->v, c->version, c->tok_w, c->stable, c->hist_tok, c->hist_p, c->hist_n, c->words,
                   c->rope, c->err, c->ticket, c->X, c->rs, c->lm_part, c->lm_rs, c->ffn_buf,
-                  c->fa_state, c->fa_key, c->fa_rebuilt, c->seq_done, c->m_live};
+                  c->fa_state, c->fa_key, c->fa_rebuilt, c->seq_done, c->m_live, c->stats};
   for (void* b : bufs)
     if (b) cudaFree(b);
 }
@@ -170,7 +182,8 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
             dalloc(&c->lm_rs, static_cast<size_t>(c->lm_rows_cap) * sizeof(float)) &&
             dalloc(&c->ffn_buf, sr * static_cast<size_t>(g.ffn) * c->elem);
   if (ok && !streaming)
-    ok = dalloc(&c->seq_done, static_cast<size_t>(g.batch)) && dalloc(&c->m_live, sizeof(int));
+    ok = dalloc(&c->seq_done, static_cast<size_t>(g.batch)) && dalloc(&c->m_live, sizeof(int)) &&
+         dalloc(&c->stats, static_cast<size_t>(kStatsSteps) * g.batch * 4 * sizeof(int));
   if (ok && g.facache) {
     const size_t bh = static_cast<size_t>(g.batch) * g.n_heads;
     ok = dalloc(&c->fa_state, bh * 64 * (g.head_dim + 4) * sizeof(float)) &&
@@ -284,6 +297,10 @@ dllm_status dllm_state_copy(dllm_cache* c, int field, int layer, void* host, siz
     if (!c->seq_done) return fail(DLLM_EINVAL, "dllm_state_copy: streaming caches have no block state");
     ptr = c->seq_done;
     size = g.batch;
+  } else if (field == DLLM_FIELD_STEP_STATS) {
+    if (!c->stats) return fail(DLLM_EINVAL, "dllm_state_copy: streaming caches have no block state");
+    ptr = c->stats;
+    size = static_cast<size_t>(kStatsSteps) * g.batch * 4 * sizeof(int);
   } else if (field == DLLM_FIELD_FA_REBUILT) {
     if (!c->fa_rebuilt) return fail(DLLM_EINVAL, "dllm_state_copy: the cache keeps no attention state");
     ptr = c->fa_rebuilt;
@@ -302,6 +319,7 @@ dllm_status dllm_state_copy(dllm_cache* c, int field, int layer, void* host, siz
 }
 
 dllm_status refresh_all(dllm_cache* c, int q_start, int32_t* rows_dev, int32_t* n_rows_dev, void* stream) {
+  const NvtxRange nvtx("refresh_all");
   DLLM_CHECK_HANDLE(c);
   if (c->cfg.sink > 0) return fail(DLLM_EINVAL, "refresh_all: dense mode only");
   if (!rows_dev || !n_rows_dev) return fail(DLLM_EINVAL, "refresh_all: null rows or count");
@@ -313,6 +331,7 @@ dllm_status refresh_all(dllm_cache* c, int q_start, int32_t* rows_dev, int32_t* 
 dllm_status kv_refresh(dllm_cache* c, int layer, const void* x_dev, const int32_t* tok_dev, const void* embed_dev,
                        const void* w_qkv_dev, const int32_t* rows_dev, const int32_t* n_rows_dev, int t,
                        void* stream) {
+  const NvtxRange nvtx("kv_refresh");
   DLLM_CHECK_HANDLE(c);
   const dllm_cache_cfg& g = c->cfg;
   const bool streaming = g.sink > 0;
@@ -338,6 +357,7 @@ dllm_status kv_refresh(dllm_cache* c, int layer, const void* x_dev, const int32_
 
 dllm_status kv_project(dllm_cache* c, int layer, const int32_t* tok_dev, const void* embed_dev, const void* w_qkv_dev,
                        int n, void* staged_dev, void* stream) {
+  const NvtxRange nvtx("kv_project");
   DLLM_CHECK_HANDLE(c);
   const dllm_cache_cfg& g = c->cfg;
   if (g.sink <= 0) return fail(DLLM_EINVAL, "kv_project: streaming caches only");
@@ -360,6 +380,7 @@ dllm_status kv_project(dllm_cache* c, int layer, const int32_t* tok_dev, const v
 }
 
 dllm_status ring_append(dllm_cache* c, int layer, const void* staged_dev, int n0, int count, void* stream) {
+  const NvtxRange nvtx("ring_append");
   DLLM_CHECK_HANDLE(c);
   const dllm_cache_cfg& g = c->cfg;
   if (g.sink <= 0) return fail(DLLM_EINVAL, "ring_append: streaming caches only");
@@ -372,6 +393,7 @@ dllm_status ring_append(dllm_cache* c, int layer, const void* staged_dev, int n0
 }
 
 dllm_status block_attn(dllm_cache* c, int layer, int q_start, int q_len, void* out_dev, void* stream) {
+  const NvtxRange nvtx("block_attn");
   DLLM_CHECK_HANDLE(c);
   const dllm_cache_cfg& g = c->cfg;
   if (layer < 0 || layer >= g.n_layers) return fail(DLLM_EINVAL, "block_attn: layer out of range");
@@ -400,6 +422,7 @@ dllm_status block_attn(dllm_cache* c, int layer, int q_start, int q_len, void* o
 
 dllm_status block_attn_rows(dllm_cache* c, int layer, const int32_t* q_rows_dev, const int32_t* n_q_dev,
                             void* out_dev, void* stream) {
+  const NvtxRange nvtx("block_attn_rows");
   DLLM_CHECK_HANDLE(c);
   const dllm_cache_cfg& g = c->cfg;
   if (layer < 0 || layer >= g.n_layers) return fail(DLLM_EINVAL, "block_attn_rows: layer out of range");
@@ -416,6 +439,7 @@ dllm_status block_attn_rows(dllm_cache* c, int layer, const int32_t* q_rows_dev,
 
 dllm_status active_rows(dllm_cache* c, const void* src_dev, const int32_t* rows_dev, const int32_t* n_rows_dev,
                         int q_start, int q_len, void* dst_dev, void* stream) {
+  const NvtxRange nvtx("active_rows");
   DLLM_CHECK_HANDLE(c);
   const dllm_cache_cfg& g = c->cfg;
   if (!src_dev || !rows_dev || !n_rows_dev || !dst_dev) return fail(DLLM_EINVAL, "active_rows: null pointer");
@@ -432,6 +456,7 @@ dllm_status active_rows(dllm_cache* c, const void* src_dev, const int32_t* rows_
 dllm_status attn_out(dllm_cache* c, const void* o_dev, const void* w_o_dev, const void* x_res_dev,
                      const int32_t* tok_dev, const void* embed_dev, int q_start, int q_len, const int32_t* m_dev,
                      void* h_dev, void* stream) {
+  const NvtxRange nvtx("attn_out");
   DLLM_CHECK_HANDLE(c);
   const dllm_cache_cfg& g = c->cfg;
   if (!o_dev || !w_o_dev || !h_dev) return fail(DLLM_EINVAL, "attn_out: null o, w_o or h");
@@ -461,6 +486,7 @@ dllm_status attn_out(dllm_cache* c, const void* o_dev, const void* w_o_dev, cons
 
 dllm_status ffn_gelu(dllm_cache* c, const void* h_dev, const void* w1_dev, const void* w2_dev, int F, int M,
                      const int32_t* m_dev, void* out_dev, void* stream) {
+  const NvtxRange nvtx("ffn_gelu");
   DLLM_CHECK_HANDLE(c);
   if (!h_dev || !w1_dev || !w2_dev || !out_dev) return fail(DLLM_EINVAL, "ffn_gelu: null pointer");
   if (F != c->ffn_cap || F <= 0) return fail(DLLM_EINVAL, "ffn_gelu: F must equal the cache's ffn");
@@ -478,6 +504,7 @@ dllm_status ffn_gelu(dllm_cache* c, const void* h_dev, const void* w1_dev, const
 
 dllm_status lmhead_conf(dllm_cache* c, const void* h_dev, const void* w_lm_dev, int M, int V, int d, int mask_id,
                         int32_t* argmax_dev, float* p_top1_dev, float* entropy_dev, void* stream) {
+  const NvtxRange nvtx("lmhead_conf");
   DLLM_CHECK_HANDLE(c);
   if (!h_dev || !w_lm_dev || !argmax_dev || !p_top1_dev || !entropy_dev)
     return fail(DLLM_EINVAL, "lmhead_conf: null pointer");
@@ -505,6 +532,7 @@ dllm_status lmhead_conf(dllm_cache* c, const void* h_dev, const void* w_lm_dev, 
 dllm_status stab_update(dllm_cache* c, const int32_t* argmax_dev, const float* p_top1_dev, const float* entropy_dev,
                         int32_t* tok_dev, int q_start, int t, int step_in_block, int last_step, int32_t* rows_dev,
                         int32_t* n_rows_dev, void* stream) {
+  const NvtxRange nvtx("stab_update");
   DLLM_CHECK_HANDLE(c);
   const dllm_cache_cfg& g = c->cfg;
   if (g.sink > 0) return fail(DLLM_EINVAL, "stab_update: dense mode only");

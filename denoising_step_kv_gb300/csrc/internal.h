@@ -52,12 +52,18 @@ struct dllm_cache {
   // W_o and the LM head (B * block_len, or 0 once every sequence has ended)
   uint8_t* seq_done = nullptr;  // [B]
   int* m_live = nullptr;        // [1]
+  // per-step stability counters of the dense step (the stability curve):
+  // [kStatsSteps][B][4] = (refresh rows, stable rows, expired rows,
+  // committed rows) of sequence b at global step t
+  int* stats = nullptr;
   // measurement hook: events bracketing a kernel (index = dllm_prof_kernel)
   cudaEvent_t prof_begin[8] = {};
   cudaEvent_t prof_end[8] = {};
 };
 
 namespace dllm {
+
+constexpr int kStatsSteps = 4096;   // global steps the stability counters record
 
 void set_error(const std::string& msg);
 

@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
     const int* __restrict__ tok_w, const int* __restrict__ version, uint32_t* __restrict__ words, int L, int Lw,
     int seq_rows, int n_layers, int blk, int K, float tau, int R, int q0, int t, int last, int full, int expiry,
     int active_queries, uint8_t* __restrict__ seq_done, int* __restrict__ m_live, unsigned* __restrict__ ticket,
-    int* __restrict__ rows, int* __restrict__ n_rows) {
+    int* __restrict__ rows, int* __restrict__ n_rows, int* __restrict__ stats) {
   __shared__ uint8_t s_unst[64];
   __shared__ uint8_t s_open[64];     // unstable after this update
   __shared__ int s_last;
@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
   pdl_launch();
   pdl_wait();
   const int nac = min(blk, L - q0);
+  int committed = 0, now_stable = 0;    // this row's counters
   if (threadIdx.x < nac) {
     const int j = threadIdx.x;
     const int r = b * L + q0 + j;
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
     // stays in registers, so nothing written here is read back
     constexpr int KMAX = 8;
     bool st = stable[r] != 0;
+    const bool st0 = st;
     const int a = argmax[h];
     const float pa = p1[h];
     int n = hist_n[h];
@@ -267,6 +269,8 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
       if (!st) tok[r] = a;
       hist_n[h] = 0;
     }
+    committed = (st && !st0) || (last && !st) ? 1 : 0;
+    now_stable = st ? 1 : 0;
     s_open[j] = st ? 0 : 1;
     bool flag = !st;
     if (ent && flag) {   // cache confidence at step t + 1 of this row's layer-0 entry
@@ -279,10 +283,13 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
   // early exit: every active row stable after a step that is not the
   // block's last ends this sequence's block (no refresh from now on)
   const int n_open = __syncthreads_count(threadIdx.x < nac && s_open[threadIdx.x]);
+  const int n_committed = __syncthreads_count(committed);
+  const int n_stable = __syncthreads_count(now_stable);
   const bool ended = seq_done && !last && n_open == 0;
+  int n_flag = 0, n_expired = 0;
   for (int base = 0; base < L; base += blockDim.x) {
     const int p = base + threadIdx.x;
-    bool f = false;
+    bool f = false, expired = false;
     if (p < L) {
       const int r = b * L + p;
       if (ended) {
@@ -299,14 +306,24 @@ __global__ void __launch_bounds__(1024, 1) swd_kernel(
         const int lo = max(p - R, q0), hi = min(p + R, q0 + nac - 1);
         for (int u = lo; u <= hi; ++u) f |= s_unst[u - q0] != 0;
         f |= tk != tw;
-        if (expiry >= 0) f |= (t + 1) - vmin > expiry;
+        expired = expiry >= 0 && (t + 1) - vmin > expiry;
+        f |= expired;
       }
     }
+    n_flag += __syncthreads_count(f);
+    n_expired += __syncthreads_count(expired);
     const uint32_t word = __ballot_sync(0xffffffffu, f);
     const int w = (base + (threadIdx.x & ~31)) >> 5;
     if ((threadIdx.x & 31) == 0 && w < Lw) words[b * Lw + w] = word;
   }
   if (seq_done && threadIdx.x == 0) seq_done[b] = ended ? 1 : 0;
+  if (stats && threadIdx.x == 0 && t >= 0 && t < kStatsSteps) {
+    int* o = stats + (static_cast<size_t>(t) * gridDim.x + b) * 4;
+    o[0] = n_flag;
+    o[1] = n_stable;
+    o[2] = n_expired;
+    o[3] = n_committed;
+  }
   // the last sequence block to finish compacts every sequence's flags
   __threadfence();
   __syncthreads();
@@ -564,8 +581,7 @@ cudaError_t launch_stab(dllm_cache* c, const int* argmax, const float* p1, const
   return launch_ex(swd_kernel, dim3(g.batch), dim3(1024), 0, st, 0, argmax, p1, ent, cg, tok, c->stable, c->hist_tok, c->hist_p,
                    c->hist_n, c->tok_w, c->version, c->words, g.seq_len, c->Lw, c->seq_rows, g.n_layers, g.block_len,
                    g.swd_K, g.swd_tau, R, q_start, t, last, full, g.expiry, g.active_queries, done, c->m_live,
-                   c->ticket, rows,
-                   n_rows);
+                   c->ticket, rows, n_rows, c->stats);
 }
 
 cudaError_t launch_refresh_all(dllm_cache* c, int q_start, int* rows, int* n_rows, cudaStream_t st) {
@@ -588,6 +604,10 @@ cudaError_t launch_reset(dllm_cache* c, cudaStream_t st) {
   if (c->fa_key) {   // no kept attention state is valid (block start -1 never matches)
     cudaError_t e = cudaMemsetAsync(c->fa_key, 0xff, static_cast<size_t>(g.batch) * g.n_heads * 66 * sizeof(int), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(c->fa_rebuilt, 0, sizeof(int), st);
+    if (e != cudaSuccess) return e;
+  }
+  if (c->stats) {   // no step recorded yet
+    cudaError_t e = cudaMemsetAsync(c->stats, 0, static_cast<size_t>(kStatsSteps) * g.batch * 4 * sizeof(int), st);
     if (e != cudaSuccess) return e;
   }
   const int nv = g.n_layers * c->seq_rows;

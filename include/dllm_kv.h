@@ -174,8 +174,15 @@ typedef enum {
   DLLM_FIELD_HIST_N = 8,    /* int32 [B][block_len] records pushed this block */
   DLLM_FIELD_FA_REBUILT = 9, /* int32 [1]: (sequence, head) attention states
                                rebuilt since the last reset (facache) */
-  DLLM_FIELD_SEQ_DONE = 10  /* uint8 [B]: sequences whose block has ended
+  DLLM_FIELD_SEQ_DONE = 10, /* uint8 [B]: sequences whose block has ended
                                (early_exit) */
+  /* int32 [4096][B][4], dense caches: for global step t (the t passed to
+     stab_update, t < 4096) and sequence b, the counts stab_update found:
+     rows of the next refresh set, stable rows of the active block, rows
+     refreshed because their version expired, rows committed at this step
+     (stable now, or forced at the block's last step) - the stability curve
+     of [SWD] 4.4.  Zero for steps not run since the last reset. */
+  DLLM_FIELD_STEP_STATS = 11
 } dllm_field;
 
 /* Blocking copy of one state field between the handle and HOST memory

@@ -13,13 +13,13 @@ output O, residual stream h, FFN intermediate).
 from .model import (bf16_bits_to_f64, round_store, rms_scale, rope, project_qkv,
                     attention, attention_partial, merge_partials, out_proj, ffn, lm_head_conf, gelu)
 from .swd import (SWDState, swd_update, dilate, refresh_rows, expired_rows, radius_at, full_refresh_at,
-                  confidence, confidence_rows)
+                  confidence, confidence_rows, step_stats)
 from .run import run_dense, run_stream, weights_f64, ring_positions, RingSim, NEVER
 
 __all__ = [
     "bf16_bits_to_f64", "round_store", "rms_scale", "rope", "project_qkv",
     "attention", "attention_partial", "merge_partials", "out_proj", "ffn", "lm_head_conf", "gelu", "SWDState",
     "swd_update", "dilate", "refresh_rows", "expired_rows", "radius_at", "full_refresh_at", "confidence",
-    "confidence_rows", "run_dense",
+    "confidence_rows", "step_stats", "run_dense",
     "run_stream", "weights_f64", "ring_positions", "RingSim", "NEVER",
 ]

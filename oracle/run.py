@@ -29,7 +29,7 @@ from collections import deque
 import numpy as np
 
 from . import model as M
-from .swd import SWDState, swd_update, refresh_rows, radius_at, full_refresh_at, confidence_rows
+from .swd import SWDState, swd_update, refresh_rows, radius_at, full_refresh_at, confidence_rows, step_stats
 
 NEVER = -(1 << 30)     # version of a cache entry that was never written
 
@@ -190,6 +190,9 @@ def run_dense(w, W, tok0, n_steps=None, mode="cached", force_all=False, keep_pre
                 rows_next = refresh_rows(stable, tok, tok_w, version, q0, blk, R_next, t + 1, w.expiry)
             if not last and done.any():                 # ended sequences refresh nothing
                 rows_next = rows_next[~done[rows_next // L]]
+            partial_next = not last and not full_refresh_at(s + 1, w.full_every)
+            rec["stats"] = step_stats(rows_next, stable, rec["newly"], version, q0, blk, L, t + 1, w.expiry, last,
+                                      partial_next, done)
             # the row list the next step runs on: Rf, plus the active block of
             # the running sequences when every active row queries (the next
             # step is in this block unless this was its last step, and then

@@ -168,6 +168,29 @@ def confidence_rows(stable, tok, tok_w, version, q0, blk, ent, H_max, t_next, ex
     return np.flatnonzero(rf.reshape(-1)).astype(np.int32)
 
 
+def step_stats(rf_next, stable, newly, version, q0, blk, L, t_next, expiry, last, partial_next, done):
+    """Per-sequence counters of one SWD update ([SWD] 4.4 plots the stability
+    curve: how many positions are stable, and how much is recomputed, as the
+    steps go on).  Returns int [B, 4]:
+      rows of the next step's refresh set (rf_next, flat ids);
+      stable rows of the active block after the update;
+      rows in that refresh set because their version expired ([TA] 2.3),
+        counted when the next step builds the set by the rules
+        (partial_next) and the sequence is still running;
+      rows committed by this update: newly stable ones, plus at the block's
+        last step every row still unstable (its argmax is committed)."""
+    B = stable.shape[0]
+    out = np.zeros((B, 4), dtype=np.int64)
+    exp = expired_rows(version, t_next, expiry)
+    for b in range(B):
+        out[b, 0] = int(np.sum(rf_next // L == b))
+        act = stable[b, q0:q0 + blk]
+        out[b, 1] = int(act.sum())
+        out[b, 2] = int(exp[b].sum()) if partial_next and not done[b] else 0
+        out[b, 3] = int(newly[b].sum()) + (int((~act).sum()) if last else 0)
+    return out
+
+
 def refresh_rows(stable, tok, tok_w, version, q0, blk, R, t_next, expiry):
     """Refresh set for step t_next as sorted flat row indices b*L + pos."""
     B, L = tok.shape

@@ -70,8 +70,10 @@ def test_free_running_generation(name):
     try:
         gen.run(on_step=grab)
         assert K.dllm_cache_check(gen.cache) == 0
+        stats = read_field(gen.cache, K.FIELD_STEP_STATS, 0, (K.STATS_STEPS, B, 4), "i32")
     finally:
         gen.close()
+    assert not np.any(stats[len(trace):])          # steps not run record nothing
     rtol, atol = tol(w)
     compared = 0
     for rec, g in zip(trace, got):
@@ -94,6 +96,8 @@ def test_free_running_generation(name):
             compared += 1
             break
         assert np.array_equal(g["rows"], rec["rows_next"]), (name, t, "rows")
+        # the stability curve: refresh, stable, expired and committed rows per sequence
+        assert np.array_equal(stats[t], rec["stats"]), (name, t, "stats", stats[t], rec["stats"])
         compared += 1
     assert compared >= 1 or np.any(trace[0]["margin"] <= 1e-2), (name, compared)
 

@@ -629,6 +629,45 @@ def test_sink_stream_outputs_bit_stable_sinks():
     assert all(h[:S] == list(range(S)) for n, h in held.items() if n >= S)
 
 
+@pytest.mark.parametrize("name", ["mid_bf16", "mid_bf16_sharp", "mid_bf16_exit", "mid_bf16_sched"])
+def test_step_stats_stability_curve(name):
+    """The per-step counters against what they count, independently: each
+    block commits every position of every sequence exactly once (by
+    stability or at its last step); the stable count never falls inside a
+    block and grows by exactly the positions committed by stability; the
+    refresh count is the next step's refresh set per sequence; expired rows
+    are a subset of it and vanish when expiry is off."""
+    w, W, tok0 = _load(name)
+    tr = O.run_dense(w, W, tok0, mode="cached")
+    B, L, blk = w.batch, w.seq_len, w.block_len
+    prev_stable = np.zeros(B, dtype=np.int64)
+    committed = np.zeros(B, dtype=np.int64)
+    for i, r in enumerate(tr):
+        st = r["stats"]
+        if r["s"] == 0:
+            prev_stable[:] = 0
+            committed[:] = 0
+        last = r["s"] == w.steps_per_block - 1
+        for b in range(B):
+            assert st[b, 0] == np.sum(r["rf_next"] // L == b), (r["t"], b)
+            assert st[b, 2] <= st[b, 0]
+            if w.expiry < 0:
+                assert st[b, 2] == 0
+            assert st[b, 1] >= prev_stable[b]                       # stable is absorbing
+            assert st[b, 1] == int(r["stable"][b, r["q0"]:r["q0"] + blk].sum())
+            by_stability = st[b, 1] - prev_stable[b]
+            assert st[b, 3] == by_stability + (blk - st[b, 1] if last else 0)
+        prev_stable[:] = st[:, 1]
+        committed += st[:, 3]
+        if last:
+            assert np.all(committed == blk), (r["t"], committed)
+            assert np.all(st[:, 0] == L)                             # the next block starts with a full refresh
+    if name != "mid_bf16":
+        assert sum(int(r["stats"][:, 1].sum()) for r in tr) > 0      # something stabilises
+    if w.expiry >= 0 and name == "mid_bf16":
+        assert sum(int(r["stats"][:, 2].sum()) for r in tr) > 0      # expired rows occur
+
+
 def test_sharp_variants_exercise_swd():
     for name in ("tiny_fp32_sharp", "mid_bf16_sharp"):
         w, W, tok0 = _load(name)
