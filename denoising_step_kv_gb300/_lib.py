@@ -14,7 +14,7 @@ DLLM_F32, DLLM_BF16 = 0, 1
 (FIELD_Q, FIELD_K, FIELD_V, FIELD_VERSION, FIELD_TOK_W, FIELD_STABLE, FIELD_HIST_TOK, FIELD_HIST_P, FIELD_HIST_N,
  FIELD_FA_REBUILT, FIELD_SEQ_DONE, FIELD_STEP_STATS) = range(12)
 STATS_STEPS = 4096   # global steps FIELD_STEP_STATS records: int32 [4096][batch][4]
-ERR_ROW, ERR_TOKEN, ERR_TIMEOUT, ERR_POS = 1, 2, 4, 8
+ERR_ROW, ERR_TOKEN, ERR_TIMEOUT, ERR_POS, ERR_GUARD = 1, 2, 4, 8, 16
 STATUS = {0: "OK", 1: "EINVAL", 2: "ENOMEM", 3: "ECUDA", 4: "EDEVICE", 5: "EUNSUPPORTED"}
 
 

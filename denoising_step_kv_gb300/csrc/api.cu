@@ -72,15 +72,28 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 void free_all(dllm_cache* c) {
   void* bufs[] = {c->q, c->k, c->v, c->version, c->tok_w, c->stable, c->hist_tok, c->hist_p, c->hist_n, c->words,
                   c->rope, c->err, c->ticket, c->X, c->rs, c->lm_part, c->lm_rs, c->ffn_buf,
-                  c->fa_state, c->fa_key, c->fa_rebuilt, c->seq_done, c->m_live, c->stats};
+                  c->fa_state, c->fa_key, c->fa_rebuilt, c->seq_done, c->m_live, c->stats, c->guard_dev};
   for (void* b : bufs)
     if (b) cudaFree(b);
 }
 
+constexpr unsigned kGuardBytes = 256;     // after every buffer of the handle
+constexpr unsigned kGuardByte = 0xA5;
+
 template <typename T>
-bool dalloc(T** p, size_t bytes) {
-  if (bytes == 0) bytes = 16;
-  return cudaMalloc(reinterpret_cast<void**>(p), bytes) == cudaSuccess;
+bool dalloc(dllm_cache* c, T** p, size_t bytes) {
+  bytes = (std::max<size_t>(bytes, 16) + 255) / 256 * 256;
+  if (cudaMalloc(reinterpret_cast<void**>(p), bytes + kGuardBytes) != cudaSuccess) return false;
+  void* g = reinterpret_cast<uint8_t*>(*p) + bytes;
+  c->guards.push_back(g);
+  return cudaMemset(g, kGuardByte, kGuardBytes) == cudaSuccess;
+}
+
+// One CTA per guard: every word must still hold the pattern.
+__global__ void guard_kernel(void* const* guards, unsigned* err) {
+  const uint32_t* g = static_cast<const uint32_t*>(guards[blockIdx.x]);
+  const uint32_t want = 0x01010101u * kGuardByte;
+  if (threadIdx.x < kGuardBytes / 4 && g[threadIdx.x] != want) atomicOr(err, DLLM_ERR_GUARD);
 }
 
 }  // namespace
@@ -169,25 +182,30 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
   c->lm_rows_cap = g.batch * blk;
   c->lm_tiles_cap = cdiv(g.vocab, 128);
   c->ffn_cap = g.ffn;
-  bool ok = dalloc(&c->q, nl * c->kv_layer_bytes) && dalloc(&c->k, nl * c->kv_layer_bytes) &&
-            dalloc(&c->v, nl * c->kv_layer_bytes) && dalloc(&c->version, nl * sr * sizeof(int)) &&
-            dalloc(&c->tok_w, sr * sizeof(int)) && dalloc(&c->stable, sr) &&
-            dalloc(&c->hist_tok, static_cast<size_t>(g.batch) * blk * K * sizeof(int)) &&
-            dalloc(&c->hist_p, static_cast<size_t>(g.batch) * blk * K * sizeof(float)) &&
-            dalloc(&c->hist_n, static_cast<size_t>(g.batch) * blk * sizeof(int)) &&
-            dalloc(&c->words, static_cast<size_t>(g.batch) * c->Lw * sizeof(uint32_t)) &&
-            dalloc(&c->rope, static_cast<size_t>(g.head_dim / 2) * sizeof(float2)) &&
-            dalloc(&c->err, sizeof(unsigned)) && dalloc(&c->ticket, sizeof(unsigned)) && dalloc(&c->X, sr * d * c->elem) && dalloc(&c->rs, sr * sizeof(float)) &&
-            dalloc(&c->lm_part, static_cast<size_t>(c->lm_rows_cap) * c->lm_tiles_cap * 16) &&
-            dalloc(&c->lm_rs, static_cast<size_t>(c->lm_rows_cap) * sizeof(float)) &&
-            dalloc(&c->ffn_buf, sr * static_cast<size_t>(g.ffn) * c->elem);
+  bool ok = dalloc(c, &c->q, nl * c->kv_layer_bytes) && dalloc(c, &c->k, nl * c->kv_layer_bytes) &&
+            dalloc(c, &c->v, nl * c->kv_layer_bytes) && dalloc(c, &c->version, nl * sr * sizeof(int)) &&
+            dalloc(c, &c->tok_w, sr * sizeof(int)) && dalloc(c, &c->stable, sr) &&
+            dalloc(c, &c->hist_tok, static_cast<size_t>(g.batch) * blk * K * sizeof(int)) &&
+            dalloc(c, &c->hist_p, static_cast<size_t>(g.batch) * blk * K * sizeof(float)) &&
+            dalloc(c, &c->hist_n, static_cast<size_t>(g.batch) * blk * sizeof(int)) &&
+            dalloc(c, &c->words, static_cast<size_t>(g.batch) * c->Lw * sizeof(uint32_t)) &&
+            dalloc(c, &c->rope, static_cast<size_t>(g.head_dim / 2) * sizeof(float2)) &&
+            dalloc(c, &c->err, sizeof(unsigned)) && dalloc(c, &c->ticket, sizeof(unsigned)) && dalloc(c, &c->X, sr * d * c->elem) && dalloc(c, &c->rs, sr * sizeof(float)) &&
+            dalloc(c, &c->lm_part, static_cast<size_t>(c->lm_rows_cap) * c->lm_tiles_cap * 16) &&
+            dalloc(c, &c->lm_rs, static_cast<size_t>(c->lm_rows_cap) * sizeof(float)) &&
+            dalloc(c, &c->ffn_buf, sr * static_cast<size_t>(g.ffn) * c->elem);
   if (ok && !streaming)
-    ok = dalloc(&c->seq_done, static_cast<size_t>(g.batch)) && dalloc(&c->m_live, sizeof(int)) &&
-         dalloc(&c->stats, static_cast<size_t>(kStatsSteps) * g.batch * 4 * sizeof(int));
+    ok = dalloc(c, &c->seq_done, static_cast<size_t>(g.batch)) && dalloc(c, &c->m_live, sizeof(int)) &&
+         dalloc(c, &c->stats, static_cast<size_t>(kStatsSteps) * g.batch * 4 * sizeof(int));
   if (ok && g.facache) {
     const size_t bh = static_cast<size_t>(g.batch) * g.n_heads;
-    ok = dalloc(&c->fa_state, bh * 64 * (g.head_dim + 4) * sizeof(float)) &&
-         dalloc(&c->fa_key, bh * 66 * sizeof(int)) && dalloc(&c->fa_rebuilt, sizeof(int));
+    ok = dalloc(c, &c->fa_state, bh * 64 * (g.head_dim + 4) * sizeof(float)) &&
+         dalloc(c, &c->fa_key, bh * 66 * sizeof(int)) && dalloc(c, &c->fa_rebuilt, sizeof(int));
+  }
+  if (ok) {
+    ok = cudaMalloc(reinterpret_cast<void**>(&c->guard_dev), c->guards.size() * sizeof(void*)) == cudaSuccess &&
+         cudaMemcpy(c->guard_dev, c->guards.data(), c->guards.size() * sizeof(void*), cudaMemcpyHostToDevice) ==
+             cudaSuccess;
   }
   if (!ok) {
     free_all(c);
@@ -244,6 +262,10 @@ dllm_status dllm_cache_reset(dllm_cache* c, void* stream) {
 dllm_status dllm_cache_check(dllm_cache* c, void* stream, uint32_t* err_word) {
   DLLM_CHECK_HANDLE(c);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!c->guards.empty()) {
+    guard_kernel<<<static_cast<unsigned>(c->guards.size()), kGuardBytes / 4, 0, st>>>(c->guard_dev, c->err);
+    DLLM_LAUNCH(cudaGetLastError(), "dllm_cache_check: guards");
+  }
   DLLM_LAUNCH(cudaStreamSynchronize(st), "dllm_cache_check: synchronize");
   unsigned w = 0;
   DLLM_LAUNCH(cudaMemcpy(&w, c->err, sizeof(w), cudaMemcpyDeviceToHost), "dllm_cache_check: read");
@@ -258,6 +280,7 @@ dllm_status dllm_cache_check(dllm_cache* c, void* stream, uint32_t* err_word) {
     if (w & DLLM_ERR_TOKEN) m += " (token out of range)";
     if (w & DLLM_ERR_TIMEOUT) m += " (barrier wait timed out)";
     if (w & DLLM_ERR_POS) m += " (position outside the RoPE table)";
+    if (w & DLLM_ERR_GUARD) m += " (a write past the end of a buffer of the handle)";
     return fail(DLLM_EDEVICE, m);
   }
   return DLLM_OK;

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <vector>
 
 #include "dllm_kv.h"
 #include "kv_layout.h"
@@ -56,6 +57,11 @@ struct dllm_cache {
   // [kStatsSteps][B][4] = (refresh rows, stable rows, expired rows,
   // committed rows) of sequence b at global step t
   int* stats = nullptr;
+  // guard bytes after every buffer above (a fixed pattern that
+  // dllm_cache_check verifies): the device addresses, and a device copy of
+  // the list
+  std::vector<void*> guards;
+  void** guard_dev = nullptr;
   // measurement hook: events bracketing a kernel (index = dllm_prof_kernel)
   cudaEvent_t prof_begin[8] = {};
   cudaEvent_t prof_end[8] = {};

@@ -75,6 +75,9 @@ typedef enum { DLLM_F32 = 0, DLLM_BF16 = 1 } dllm_dtype;
 #define DLLM_ERR_TOKEN    0x2u   /* token id outside [0, vocab) */
 #define DLLM_ERR_TIMEOUT  0x4u   /* a bounded wait on a barrier gave up */
 #define DLLM_ERR_POS      0x8u   /* position outside the RoPE table */
+#define DLLM_ERR_GUARD    0x10u  /* dllm_cache_check found a guard after one of the
+                                    handle's buffers overwritten: some kernel
+                                    wrote past the end of a buffer */
 
 typedef struct {
   int n_layers;      /* layers with a cache (1 for a single attention layer) */
