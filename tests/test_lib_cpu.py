@@ -74,3 +74,35 @@ def test_python_binding_has_no_fallback(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         _lib.lib()
+
+
+def _header_code():
+    src = open(os.path.join(ROOT, "include", "dllm_kv.h")).read()
+    return re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+
+
+def test_binding_matches_the_header():
+    """The ctypes mirror of dllm_cache_cfg lists the header's fields in the
+    header's order with the header's C types, and the binding's field, kernel
+    and error constants carry the header's values."""
+    from denoising_step_kv_gb300 import _lib as K
+    src = _header_code()
+    body = re.search(r"typedef struct \{(.*?)\} dllm_cache_cfg;", src, flags=re.S).group(1)
+    want = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        ctype, names = decl.split(None, 1)
+        want += [(n.strip(), ctype) for n in names.split(",")]
+    got = [(n, {ctypes.c_int: "int", ctypes.c_float: "float"}[t]) for n, t in K.CacheCfg._fields_]
+    assert got == want
+    fields = dict(re.findall(r"DLLM_FIELD_(\w+)\s*=\s*(\d+)", src))
+    assert fields and {k: int(v) for k, v in fields.items()} == {
+        k[len("FIELD_"):]: getattr(K, k) for k in dir(K) if k.startswith("FIELD_")}
+    errs = dict(re.findall(r"#define DLLM_ERR_(\w+)\s+(0x[0-9a-fA-F]+)u", src))
+    assert errs and {k: int(v, 16) for k, v in errs.items()} == {
+        k[len("ERR_"):]: getattr(K, k) for k in dir(K) if k.startswith("ERR_")}
+    profs = dict(re.findall(r"DLLM_PROF_(\w+)\s*=\s*(\d+)", src))
+    assert profs and {k: int(v) for k, v in profs.items()} == {
+        k[len("PROF_"):]: getattr(K, k) for k in dir(K) if k.startswith("PROF_")}
