@@ -614,8 +614,8 @@ struct SknLoader {
   }
 };
 
-// TMEM columns [c0, c0 + 32) of this thread's lane (column f) into a block's
-// rows [r0, r0 + 32).
+// This thread's 32 accumulator values of column f (rows r0 .. r0 + 31, as
+// read from its TMEM lane) into a staged block.
 __device__ __forceinline__ void skn_put32(float* blk, int f, int r0, int tpr, const float (&v)[32]) {
 #pragma unroll
   for (int u = 0; u < 8; ++u)
