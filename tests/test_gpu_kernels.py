@@ -107,12 +107,13 @@ def test_kv_refresh_large_m(name, n):
         K.dllm_cache_free(c)
 
 
-@pytest.mark.parametrize("n", [200, 256, 272, 300, 512])
+@pytest.mark.parametrize("n", [0, 1, 200, 256, 272, 300, 512])
 def test_kv_refresh_wide_projection(n):
     """The 8B-shaped projection (d 4096, N = 3d = 12288: 96 weight tiles, the
     weight-streaming kernel without a split of K) at device row counts up to
     512; rows past 256 take its second MMA.  Sampled rows on both sides of
-    256, and the last, against the oracle; rows outside the list untouched."""
+    256, and the last, against the oracle; rows outside the list untouched;
+    a count of 0 writes nothing."""
     from dataclasses import replace
     w = replace(C.get("8b_shaped"), batch=1, seq_len=640, n_prompt=576, vocab=1000)
     B, L, H, dh = w.batch, w.seq_len, w.n_heads, w.head_dim
@@ -125,6 +126,10 @@ def test_kv_refresh_wide_projection(n):
         rows_d[:n] = i32(rows)
         K.kv_refresh(c, 0, None, i32(tok), to_device(embed), to_device(wqkv), rows_d, i32([n]), 4)
         assert K.dllm_cache_check(c) == 0
+        if n == 0:
+            for f in (K.FIELD_Q, K.FIELD_K, K.FIELD_V):
+                assert not np.any(read_kv(c, f, 0, w))
+            return
         pick = np.unique(np.clip([0, 1, 127, 128, 255, 256, 257, 271, 272, 300, n - 1], 0, n - 1))
         sel = rows[pick]
         x = O.bf16_bits_to_f64(embed)[tok.reshape(-1)[sel]]
