@@ -7,11 +7,13 @@
 //                       the epilogue of one tile overlaps the next tile's MMAs;
 //   gemm_pair_kernel    the same with clusters of two CTAs on 128 x 256 tiles
 //                       that share (multicast) the weight tile - large M;
+//                       both persistent kernels run their tiles in column
+//                       bands so that the tiles in flight share L2;
 //   gemm_sharea_kernel  clusters of CTAs on adjacent weight tiles of the same
 //                       128 rows, which they share (multicast) - the LM head;
 //   gemm_skinny_kernel  weights as the MMA's A operand, the few rows as its B
-//                       operand, K split over a cluster - M <= 256, weight
-//                       streaming.
+//                       operand, K split over a cluster - weight streaming for
+//                       M <= 256 with a split, M <= 512 without.
 // fp32: a SIMT kernel whose "loader" computes 32 dot products on demand, used
 // only by the fp32 workload (tensor cores have no fp32 path within 1e-5).
 #pragma once
