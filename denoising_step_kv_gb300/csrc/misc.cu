@@ -183,7 +183,9 @@ __device__ void compact_words(const uint32_t* __restrict__ words, int nw, int L,
                               int* __restrict__ n_rows);
 
 // Stable-Window-Decoding update of the active block of sequence blockIdx.x,
-// then one flag bit per position for the next step's refresh set.
+// then one flag bit per position for the next step's refresh set.  With
+// `stats`, the sequence's counters of step t (refresh rows, stable rows,
+// expired rows, committed rows) go to stats[t][b][0..3].
 //
 // ent (may be null): the confidence criterion - an unstable active row joins
 // the next refresh set when alpha (1 - ent / H_max) + beta exp(-lambda age)
