@@ -281,13 +281,15 @@ def test_lmhead_conf(name):
 
 
 @pytest.mark.parametrize("V,M", [(1640, 32), (1640, 200), (4100, 256), (9, 5), (50000, 129), (50000, 200),
-                                 (50000, 256), (126464, 256)])
+                                 (50000, 256), (126464, 256), (32000, 128), (50000, 100), (126464, 64)])
 def test_lmhead_conf_vocab_groups(V, M):
     """Vocab sizes whose 128-column tiles do not fill the last cluster group
     (13 tiles in groups of 4), more than one 128-row tile, a vocab below one
-    group (the plain persistent kernel), and large vocabularies at 129..256
+    group (the plain persistent kernel), large vocabularies at 129..256
     rows (pairs of row tiles on 256-column weight tiles; V 50000 leaves a
-    80-column tail)."""
+    80-column tail), and one row tile over large vocabularies (the shared-A
+    kernel's 256-column tiles in groups of four: V 32000 leaves three tiles
+    of the last group past the vocab, V 50000 an 80-column tail)."""
     from dataclasses import replace
     w = replace(C.get("mid_bf16"), vocab=V, batch=1, block_len=min(64, M), seq_len=max(160, M))
     c = K.dllm_cache_init(K.make_cfg(w))
