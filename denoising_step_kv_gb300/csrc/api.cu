@@ -230,13 +230,14 @@ dllm_status dllm_cache_init(const dllm_cache_cfg* cfg, void* stream, dllm_cache*
     }
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaMemsetAsync(c->q, 0, nl * c->kv_layer_bytes, st);
-  cudaMemsetAsync(c->k, 0, nl * c->kv_layer_bytes, st);
-  cudaMemsetAsync(c->v, 0, nl * c->kv_layer_bytes, st);
-  cudaMemsetAsync(c->ticket, 0, sizeof(unsigned), st);
-  cudaMemsetAsync(c->hist_tok, 0, static_cast<size_t>(g.batch) * blk * K * sizeof(int), st);
-  cudaMemsetAsync(c->hist_p, 0, static_cast<size_t>(g.batch) * blk * K * sizeof(float), st);
-  if (launch_reset(c, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess) {
+  const size_t hist = static_cast<size_t>(g.batch) * blk * K;
+  if (cudaMemsetAsync(c->q, 0, nl * c->kv_layer_bytes, st) != cudaSuccess ||
+      cudaMemsetAsync(c->k, 0, nl * c->kv_layer_bytes, st) != cudaSuccess ||
+      cudaMemsetAsync(c->v, 0, nl * c->kv_layer_bytes, st) != cudaSuccess ||
+      cudaMemsetAsync(c->ticket, 0, sizeof(unsigned), st) != cudaSuccess ||
+      cudaMemsetAsync(c->hist_tok, 0, hist * sizeof(int), st) != cudaSuccess ||
+      cudaMemsetAsync(c->hist_p, 0, hist * sizeof(float), st) != cudaSuccess || launch_reset(c, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
     free_all(c);
     delete c;
     return fail(DLLM_ECUDA, "dllm_cache_init: reset failed");
@@ -293,6 +294,7 @@ dllm_status dllm_state_copy(dllm_cache* c, int field, int layer, void* host, siz
   void* ptr = nullptr;
   size_t size = 0;
   const size_t blk = g.sink > 0 ? 1 : g.block_len, K = g.sink > 0 ? 1 : g.swd_K;
+  if (field < 0) return fail(DLLM_EINVAL, "dllm_state_copy: unknown field");
   if (field <= DLLM_FIELD_V) {
     if (layer < 0 || layer >= g.n_layers) return fail(DLLM_EINVAL, "dllm_state_copy: bad layer");
     size = c->kv_layer_bytes;

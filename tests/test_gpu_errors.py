@@ -42,6 +42,29 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
         K.dllm_cache_free(c)
 
 
+def test_state_copy_refuses_unknown_fields_and_wrong_sizes():
+    """A field outside the enumeration (negative or past the last) and a byte
+    count other than the field's size are refused before anything is copied;
+    the handle keeps working."""
+    w = C.get("mid_bf16")
+    c = K.dllm_cache_init(K.make_cfg(w))
+    try:
+        for f in (-1, -7, K.FIELD_STEP_STATS + 1):
+            with pytest.raises(K.DllmError) as e:
+                K.state_size(c, f)
+            assert e.value.status == 1 and "unknown field" in K.last_error()
+        n = K.state_size(c, K.FIELD_TOK_W)
+        assert n == w.batch * w.seq_len * 4
+        with pytest.raises(K.DllmError) as e:
+            K.dllm_state_copy(c, K.FIELD_TOK_W, 0, torch.zeros(n // 4 - 1, dtype=torch.int32), False)
+        assert e.value.status == 1
+        host = torch.full((n // 4,), -5, dtype=torch.int32)
+        K.dllm_state_copy(c, K.FIELD_TOK_W, 0, host, False)
+        assert K.dllm_cache_check(c) == 0
+    finally:
+        K.dllm_cache_free(c)
+
+
 def test_out_of_range_rows_and_tokens_set_bits_and_are_skipped():
     w = C.get("mid_bf16")
     m = G.model(w)
