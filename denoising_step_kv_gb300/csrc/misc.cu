@@ -613,7 +613,7 @@ cudaError_t launch_reset(dllm_cache* c, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   const int nv = g.n_layers * c->seq_rows;
-  const int nh = g.batch * g.block_len;
+  const int nh = g.batch * (g.sink > 0 ? 1 : g.block_len);   // the history counters the handle holds
   reset_kernel<<<std::max(1, std::min(cdiv(std::max(nv, c->seq_rows), 256), 1024)), 256, 0, st>>>(
       c->version, nv, c->tok_w, c->stable, c->seq_rows, c->hist_n, nh, c->m_live, c->err);
   return cudaGetLastError();

@@ -94,7 +94,7 @@ typedef struct {
   int swd_K;         /* steps a top-1 token must persist (<= 8) */
   float swd_tau;     /* mean top-1 probability threshold (strict >) */
   int swd_R;         /* dilation radius of unstable positions */
-  int block_len;     /* active block length (<= 64) */
+  int block_len;     /* active block length (<= 64); streaming mode ignores it */
   int mask_id;       /* id of the mask token */
   int active_queries;/* 1 (multi-layer denoiser): every active-block row
                         passes through the layers as a query; the row list

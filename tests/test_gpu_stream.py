@@ -79,3 +79,19 @@ def test_sink_ring_full_size_sampled():
     for n in sample:
         assert len(held[n]) == min(n + 1, w.sink + w.window)
         assert close(out[n], ref[n].reshape(-1), w), (n, max_err(out[n], ref[n].reshape(-1)))
+
+
+def test_stream_cache_ignores_block_len():
+    """Streaming mode holds one history counter per sequence whatever
+    block_len says: handle creation and reset clear only that, so a large
+    block_len leaves every guard intact."""
+    from dataclasses import replace
+    w = replace(C.get("mid_sink"), block_len=1000)
+    c = K.dllm_cache_init(K.make_cfg(w))
+    try:
+        assert K.dllm_cache_check(c) == 0
+        K.dllm_cache_reset(c)
+        assert K.dllm_cache_check(c) == 0
+        assert K.state_size(c, K.FIELD_HIST_N) == 4 * w.batch
+    finally:
+        K.dllm_cache_free(c)
