@@ -228,8 +228,6 @@ cudaError_t qkv_dh(dllm_cache* c, int layer, const void* A, int M_cap, const int
 
 }  // namespace
 
-// Vocab columns per LM-head partial: 256 when the pair kernel runs (more
-// than one 128-row tile: two row tiles share each weight tile), else 128.
 // Vocab columns per partial of the LM head: 256 on the pair kernel (M > 128)
 // and on the shared-A kernel (M <= 128, at least 8 such tiles), else 128.
 int lm_tile_cols(const dllm_cache* c, int M, int V) {
