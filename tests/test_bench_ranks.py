@@ -78,3 +78,23 @@ def test_profile_hash_ignores_comments_only():
     c = "int f(int x) {\n  return x + 2;\n}\n"
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(b) != bench._code_only(c)
+
+
+def test_profile_summaries_are_of_the_current_sources():
+    """Every traffic line under profiles/ names a measured kernel and the hash
+    of that kernel's current sources, so the bench reports each captured
+    traffic figure and no figure of an older revision of a kernel."""
+    import re
+    pat = re.compile(r"traffic: kernel=(\S+) workload=(\S+) bytes_per_launch=(\d+) src_sha256=([0-9a-f]+)")
+    pdir = os.path.join(ROOT, "profiles")
+    seen = 0
+    for name in sorted(os.listdir(pdir)):
+        with open(os.path.join(pdir, name)) as f:
+            for m in pat.finditer(f.read()):
+                kernel, workload, nbytes, sha = m.groups()
+                assert bench._src_key(kernel) is not None, (name, kernel)
+                assert sha == bench.kernel_src_sha(kernel), (name, kernel)
+                assert bench.profiled_traffic(kernel, workload) == int(nbytes), (name, kernel, workload)
+                assert C.get(workload) is not None
+                seen += 1
+    assert seen >= 10
