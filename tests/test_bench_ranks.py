@@ -98,3 +98,17 @@ def test_profile_summaries_are_of_the_current_sources():
                 assert C.get(workload) is not None
                 seen += 1
     assert seen >= 10
+
+
+def test_cpu_baseline_sample_repeats_to_the_minimum_work():
+    """The oracle sample runs once for the reference arm's steps, and repeats
+    until the requested oracle work has run for the CPU baseline; the tiny
+    workload's generation is timed whole, not extrapolated."""
+    w = C.get("tiny_fp32")
+    m = G.model(w)
+    g1, d1 = bench.oracle_sample(w, m)
+    assert g1 > 0 and "whole generation" in d1 and "repetitions" not in d1
+    g2, d2 = bench.oracle_sample(w, m, 0.2)
+    assert g2 > 0 and "repetitions" in d2
+    n = int(d2.split("the median of ")[1].split(" ")[0])
+    assert n >= 2
